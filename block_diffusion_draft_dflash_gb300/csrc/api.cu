@@ -1,0 +1,491 @@
+// C ABI entry points (include/dflash.h): argument checks, workspace carving and the
+// launch sequences of the composite calls.  No device memory is allocated here.
+#include <stdio.h>
+
+#include <vector>
+
+#include "attention.h"
+#include "common.cuh"
+#include "gemm.h"
+#include "layers.h"
+
+namespace df {
+int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
+                  int32_t* parent, int32_t* depth, float* score, uint32_t* anc, int32_t* topk_id, float* topk_val,
+                  int* status, cudaStream_t st);
+size_t ddtree_heap_smem(int D, int K, int B);
+size_t accept_scratch_bytes(int b);
+int launch_accept(int b, int n_tree, const int32_t* choice, const int32_t* tok, const int32_t* parent,
+                  df_bf16* k_cache, df_bf16* v_cache, int n_layers, int Hkv, int cap, int32_t* cache_len,
+                  const df_bf16* tree_feat, int feat_dim, df_bf16* new_feat, int max_new, int32_t* n_new,
+                  int32_t* acc_tok, int32_t* n_acc, int32_t* new_bonus, int32_t* src_slot, void* scratch,
+                  int* status, cudaStream_t st);
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// Bump allocator over a caller-provided workspace (or a size counter when base is null).
+struct Carver {
+  unsigned char* base;
+  size_t off = kAlign;  // the first 256 bytes hold the status header
+  explicit Carver(void* b) : base(static_cast<unsigned char*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off = up(off + count * sizeof(T));
+    return p;
+  }
+};
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline int* status_of(void* ws) { return reinterpret_cast<int*>(ws); }
+
+#define DF_TRY(x)            \
+  do {                       \
+    int _rc = (x);           \
+    if (_rc != DF_OK) return _rc; \
+  } while (0)
+
+bool cfg_ok(const df_model_cfg* c) {
+  return c && c->n_layers > 0 && c->d_model > 0 && c->d_model % 64 == 0 && c->head_dim == 128 && c->n_kv_heads > 0 &&
+         c->n_q_heads % c->n_kv_heads == 0 && (128 % (c->n_q_heads / c->n_kv_heads)) == 0 &&
+         (c->n_q_heads / c->n_kv_heads) <= 8 && c->d_ff > 0 && c->d_ff % 64 == 0 && c->vocab >= 2 &&
+         c->n_feat_layers >= 0 && c->n_feat_layers <= 8;
+}
+
+struct LayerBufs {
+  float* h;         // [R][d] residual stream
+  df_bf16* x;       // [Rx][d] normed GEMM input
+  float* qkv;       // [Rx][nqkv]
+  df_bf16* q;       // [R][Hq*hd]
+  df_bf16* attn;    // [R][Hq*hd]
+  float* gu;        // [R][2F]
+  df_bf16* act;     // [R][F]
+  float* o_part;
+  float* ml_part;
+};
+
+int nsplit_for(int b, int T, int Hq, int Hkv, int max_keys) {
+  const int G = Hq / Hkv, NPT = 128 / G;
+  return attn_num_splits(b, Hkv, (T + NPT - 1) / NPT, max_keys);
+}
+
+// One pre-norm decoder layer over R rows (Rx >= R rows enter the QKV projection).
+// Attention keys: dense [0, dense_len[s] + dense_add) and an ancestor-masked tail.
+struct LayerRun {
+  const df_model_cfg* cfg;
+  const df_layer_weights* w;
+  int b, T;           // R = b*T query rows
+  int Rx;             // rows of x / qkv (R plus context rows)
+  QkRopeArgs qk;      // filled except the layer-specific fields
+  AttnArgs at;        // filled except q/k/v/out
+  df_bf16* capture;   // feature capture for this layer's input (may be null)
+  int ld_capture;
+  int* status;
+};
+
+int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
+  const df_model_cfg& c = *L.cfg;
+  const int d = c.d_model, hd = 128, Hq = c.n_q_heads, Hkv = c.n_kv_heads, F = c.d_ff;
+  const int nqkv = (Hq + 2 * Hkv) * hd;
+  const int R = L.b * L.T;
+  RmsNormArgs rn{};
+  rn.in = B.h; rn.gain = L.w->attn_norm; rn.out = B.x; rn.ld_out = d; rn.rows = R; rn.d = d; rn.eps = c.rms_eps;
+  rn.group_out = 1; rn.group_in = 1; rn.in_off = 0;
+  rn.zero = B.qkv; rn.zero_count = (long long)L.Rx * nqkv;
+  rn.capture = L.capture; rn.ld_capture = L.ld_capture;
+  DF_TRY(launch_rmsnorm(rn, st));
+  GemmDesc g{};
+  g.X = B.x; g.W = L.w->w_qkv; g.M = L.Rx; g.N = nqkv; g.K = d; g.ldx = d; g.ldw = d;
+  g.mode = kGemmAtomicAdd; g.out = B.qkv; g.ldo = nqkv; g.status = L.status;
+  DF_TRY(launch_gemm(g, st));
+  QkRopeArgs qk = L.qk;
+  qk.qkv = B.qkv; qk.ld_qkv = nqkv; qk.q_norm = L.w->q_norm; qk.k_norm = L.w->k_norm; qk.q_out = B.q;
+  DF_TRY(launch_qk_rope(qk, st));
+  AttnArgs at = L.at;
+  at.q = B.q; at.k_plane = qk.k_plane; at.v_plane = qk.v_plane; at.out = B.attn;
+  at.o_part = B.o_part; at.ml_part = B.ml_part;
+  DF_TRY(launch_attention(at, st));
+  g = GemmDesc{};
+  g.X = B.attn; g.W = L.w->w_o; g.M = R; g.N = d; g.K = Hq * hd; g.ldx = Hq * hd; g.ldw = Hq * hd;
+  g.mode = kGemmAtomicAdd; g.out = B.h; g.ldo = d; g.status = L.status;
+  DF_TRY(launch_gemm(g, st));
+  rn = RmsNormArgs{};
+  rn.in = B.h; rn.gain = L.w->mlp_norm; rn.out = B.x; rn.ld_out = d; rn.rows = R; rn.d = d; rn.eps = c.rms_eps;
+  rn.group_out = 1; rn.group_in = 1;
+  rn.zero = B.gu; rn.zero_count = (long long)R * 2 * F;
+  DF_TRY(launch_rmsnorm(rn, st));
+  g = GemmDesc{};
+  g.X = B.x; g.W = L.w->w_gate_up; g.M = R; g.N = 2 * F; g.K = d; g.ldx = d; g.ldw = d;
+  g.mode = kGemmAtomicAdd; g.out = B.gu; g.ldo = 2 * F; g.status = L.status;
+  DF_TRY(launch_gemm(g, st));
+  DF_TRY(launch_swiglu(B.gu, R, F, B.act, st));
+  g = GemmDesc{};
+  g.X = B.act; g.W = L.w->w_down; g.M = R; g.N = d; g.K = F; g.ldx = F; g.ldw = F;
+  g.mode = kGemmAtomicAdd; g.out = B.h; g.ldo = d; g.status = L.status;
+  DF_TRY(launch_gemm(g, st));
+  return DF_OK;
+}
+
+// ---------------------------------------------------------------------------- layouts
+struct TargetWs {
+  LayerBufs B;
+  unsigned long long* amax;
+};
+size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs* out) {
+  const int d = c->d_model, Hq = c->n_q_heads, Hkv = c->n_kv_heads, F = c->d_ff;
+  const size_t R = (size_t)b * n_tree, nqkv = (size_t)(Hq + 2 * Hkv) * 128;
+  Carver cv(base);
+  TargetWs w{};
+  w.B.h = cv.take<float>(R * d);
+  w.B.x = cv.take<df_bf16>(R * d);
+  w.B.qkv = cv.take<float>(R * nqkv);
+  w.B.q = cv.take<df_bf16>(R * Hq * 128);
+  w.B.attn = cv.take<df_bf16>(R * Hq * 128);
+  w.B.gu = cv.take<float>(R * 2 * F);
+  w.B.act = cv.take<df_bf16>(R * F);
+  w.amax = cv.take<unsigned long long>(R);
+  // partials sized for the largest split this call could choose (cache up to 2^20 keys)
+  const int ns = nsplit_for(b, n_tree, Hq, Hkv, 1 << 20);
+  const size_t pb = attn_partial_bytes(b, n_tree, Hq, ns);
+  w.B.o_part = cv.take<float>(pb / 4);
+  w.B.ml_part = w.B.o_part ? w.B.o_part + (size_t)ns * R * Hq * 128 : nullptr;
+  if (out) *out = w;
+  return cv.off;
+}
+
+struct DraftWs {
+  LayerBufs B;
+  float* fcacc;       // [b*max_new][d]
+  df_bf16* xl;        // [b*(L-1)][d]
+  int32_t* len_new;   // [b]
+};
+size_t draft_ws(const df_model_cfg* c, int b, int max_new, void* base, DraftWs* out) {
+  const int d = c->d_model, Hq = c->n_q_heads, Hkv = c->n_kv_heads, F = c->d_ff, L = c->block_size;
+  const size_t R = (size_t)b * L, Rc = (size_t)b * max_new, nqkv = (size_t)(Hq + 2 * Hkv) * 128;
+  Carver cv(base);
+  DraftWs w{};
+  w.B.h = cv.take<float>(R * d);
+  w.B.x = cv.take<df_bf16>((R + Rc) * d);
+  w.B.qkv = cv.take<float>((R + Rc) * nqkv);
+  w.B.q = cv.take<df_bf16>(R * Hq * 128);
+  w.B.attn = cv.take<df_bf16>(R * Hq * 128);
+  w.B.gu = cv.take<float>(R * 2 * F);
+  w.B.act = cv.take<df_bf16>(R * F);
+  w.fcacc = cv.take<float>((Rc ? Rc : 1) * d);
+  w.xl = cv.take<df_bf16>((size_t)b * (L - 1) * d);
+  w.len_new = cv.take<int32_t>(b);
+  const int ns = nsplit_for(b, L, Hq, Hkv, 1 << 20);
+  const size_t pb = attn_partial_bytes(b, L, Hq, ns);
+  w.B.o_part = cv.take<float>(pb / 4);
+  w.B.ml_part = w.B.o_part ? w.B.o_part + (size_t)ns * R * Hq * 128 : nullptr;
+  if (out) *out = w;
+  return cv.off;
+}
+
+__global__ void len_new_kernel(const int32_t* len, const int32_t* add, int32_t* out, int b) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s < b) out[s] = len[s] + add[s];
+}
+__global__ void copy_len_kernel(const int32_t* src, int32_t* dst, int b) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s < b) dst[s] = src[s];
+}
+__global__ void zero_kernel(float* p, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    p[i] = 0.f;
+}
+
+}  // namespace
+}  // namespace df
+
+using namespace df;
+
+extern "C" {
+
+const char* dflash_status_string(int s) {
+  switch (s) {
+    case DF_OK: return "ok";
+    case DF_ERR_ARG: return "invalid argument";
+    case DF_ERR_SHAPE: return "unsupported shape";
+    case DF_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case DF_ERR_CAPACITY: return "cache capacity exceeded";
+    case DF_ERR_CUDA: return "CUDA runtime error";
+    case DF_ERR_NAN: return "NaN log-probability";
+    case DF_ERR_TIMEOUT: return "device-side wait timed out";
+    case DF_ERR_NOT_IMPLEMENTED: return "not implemented";
+    case DF_ERR_WORKSPACE: return "workspace missing or too small";
+    case DF_ERR_DEVICE: return "device is not compute capability 10.3";
+    default: return "unknown status";
+  }
+}
+
+int dflash_check_device(void) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DF_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return (major == 10 && minor == 3) ? DF_OK : DF_ERR_DEVICE;
+}
+
+int dflash_workspace_status(void* ws, df_stream stream) {
+  if (!ws) return DF_ERR_WORKSPACE;
+  int h[2] = {0, 0};
+  if (cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess) return DF_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DF_ERR_CUDA;
+  if (h[0] != 0) {
+    int z[2] = {0, 0};
+    if (cudaMemcpy(ws, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return DF_ERR_CUDA;
+  }
+  return h[0];
+}
+
+// ------------------------------------------------------------------------------- ddtree
+size_t ddtree_build_workspace_size(int b, int D, int V, int B) {
+  const int K = B < V ? (B > 0 ? B : 1) : V;
+  Carver cv(nullptr);
+  cv.take<int32_t>((size_t)b * D * K);
+  cv.take<float>((size_t)b * D * K);
+  return cv.off;
+}
+
+int ddtree_build(const float* logprobs, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
+                 int32_t* parent, int32_t* depth, float* score, uint32_t* anc, void* ws, size_t ws_bytes,
+                 df_stream stream) {
+  if (b < 0 || D < 1 || D > 31 || V < 2 || B < 0 || B > 2048) return DF_ERR_ARG;
+  // B must not exceed the number of prefixes sum_{k<=D} V^k
+  {
+    double total = 0, p = 1;
+    for (int k = 1; k <= D && total < 1e9; ++k) { p *= V; total += p; }
+    if ((double)B > total) return DF_ERR_ARG;
+  }
+  if (b == 0) return DF_OK;
+  if (!logprobs || !tok || !parent || !depth || !score || !anc) return DF_ERR_ARG;
+  if (!al16(logprobs) || !al16(tok) || !al16(parent) || !al16(depth) || !al16(score) || !al16(anc)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < ddtree_build_workspace_size(b, D, V, B)) return DF_ERR_WORKSPACE;
+  const int K = B < V ? (B > 0 ? B : 1) : V;
+  if (ddtree_heap_smem(D, K, B) > 227 * 1024) return DF_ERR_SHAPE;
+  Carver cv(ws);
+  int32_t* tid = cv.take<int32_t>((size_t)b * D * K);
+  float* tval = cv.take<float>((size_t)b * D * K);
+  return launch_ddtree(logprobs, b, D, V, B, root_tok, tok, parent, depth, score, anc, tid, tval, status_of(ws),
+                       (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------------- attention
+size_t tree_verify_attention_workspace_size(int b, int n_tree, int Hq, int Hkv, int hd, int cap) {
+  (void)hd;
+  if (Hkv <= 0 || Hq % Hkv) return kAlign;
+  const int ns = nsplit_for(b, n_tree, Hq, Hkv, cap);
+  Carver cv(nullptr);
+  cv.take<unsigned char>(attn_partial_bytes(b, n_tree, Hq, ns));
+  return cv.off;
+}
+
+int tree_verify_attention(int b, int n_tree, int Hq, int Hkv, int hd, const df_bf16* q, const df_bf16* k_cache,
+                          const df_bf16* v_cache, int cap, const int32_t* cache_len, const uint32_t* anc, float scale,
+                          df_bf16* out, void* ws, size_t ws_bytes, df_stream stream) {
+  if (b < 0 || n_tree < 1 || Hkv <= 0 || Hq % Hkv || cap <= 0) return DF_ERR_ARG;
+  const int G = Hq / Hkv;
+  if (hd != 128 || G > 8 || (128 % G) || cap % 8) return DF_ERR_SHAPE;
+  if (b == 0) return DF_OK;
+  if (!q || !k_cache || !v_cache || !cache_len || !anc || !out) return DF_ERR_ARG;
+  if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(anc) || !al16(out)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < tree_verify_attention_workspace_size(b, n_tree, Hq, Hkv, hd, cap)) return DF_ERR_WORKSPACE;
+  Carver cv(ws);
+  const int ns = nsplit_for(b, n_tree, Hq, Hkv, cap);
+  float* part = cv.take<float>(attn_partial_bytes(b, n_tree, Hq, ns) / 4);
+  AttnArgs a{};
+  a.b = b; a.T = n_tree; a.Hq = Hq; a.Hkv = Hkv; a.cap = cap;
+  a.q = q; a.k_plane = k_cache; a.v_plane = v_cache;
+  a.dense_len = cache_len; a.dense_add = 0; a.tail_len = n_tree; a.anc = anc;
+  a.scale = scale; a.nsplit = ns; a.out = out;
+  a.o_part = part; a.ml_part = part ? part + (size_t)ns * b * n_tree * Hq * 128 : nullptr;
+  a.status = status_of(ws);
+  return launch_attention(a, (cudaStream_t)stream);
+}
+
+// --------------------------------------------------------------------- accept/compact
+size_t accept_and_compact_workspace_size(int b, int n_tree) {
+  (void)n_tree;
+  Carver cv(nullptr);
+  cv.take<unsigned char>(accept_scratch_bytes(b));
+  return cv.off;
+}
+
+int accept_and_compact(int b, int n_tree, const int32_t* choice, const int32_t* tok, const int32_t* parent,
+                       df_bf16* k_cache, df_bf16* v_cache, int n_layers, int Hkv, int hd, int cap,
+                       int32_t* cache_len, const df_bf16* tree_feat, int feat_dim, df_bf16* new_feat, int max_new,
+                       int32_t* n_new, int32_t* acc_tok, int32_t* n_acc, int32_t* new_bonus, int32_t* src_slot,
+                       void* ws, size_t ws_bytes, df_stream stream) {
+  if (b < 0 || n_tree < 1 || max_new < 1 || n_layers < 0 || cap <= 0) return DF_ERR_ARG;
+  if (n_layers > 0 && (hd != 128 || Hkv <= 0)) return DF_ERR_SHAPE;
+  if (b == 0) return DF_OK;
+  if (!choice || !tok || !parent || !cache_len || !n_new || !acc_tok || !n_acc || !new_bonus || !src_slot)
+    return DF_ERR_ARG;
+  if ((tree_feat == nullptr) != (new_feat == nullptr)) return DF_ERR_ARG;
+  if (tree_feat && (feat_dim <= 0 || feat_dim % 8 || !al16(tree_feat) || !al16(new_feat))) return DF_ERR_ALIGN;
+  if (n_layers > 0 && (!k_cache || !v_cache)) return DF_ERR_ARG;
+  if (k_cache && (!al16(k_cache) || !al16(v_cache))) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < accept_and_compact_workspace_size(b, n_tree)) return DF_ERR_WORKSPACE;
+  Carver cv(ws);
+  void* scratch = cv.take<unsigned char>(accept_scratch_bytes(b));
+  return launch_accept(b, n_tree, choice, tok, parent, k_cache, v_cache, n_layers, Hkv, cap, cache_len, tree_feat,
+                       feat_dim, new_feat, max_new, n_new, acc_tok, n_acc, new_bonus, src_slot, scratch,
+                       status_of(ws), (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ target tree forward
+size_t dflash_target_tree_forward_workspace_size(const df_model_cfg* tcfg, int b, int n_tree) {
+  if (!cfg_ok(tcfg) || b < 0 || n_tree < 1) return kAlign;
+  return target_ws(tcfg, b, n_tree, nullptr, nullptr);
+}
+
+int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w, int b, int n_tree, const int32_t* tok,
+                               const int32_t* depth, const uint32_t* anc, df_bf16* k_cache, df_bf16* v_cache, int cap,
+                               const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat, void* ws,
+                               size_t ws_bytes, df_stream stream) {
+  if (!cfg_ok(c)) return DF_ERR_SHAPE;
+  if (!w || !w->layers || !w->embed || !w->final_norm || b < 0 || n_tree < 1 || cap <= 0) return DF_ERR_ARG;
+  if (cap % 8) return DF_ERR_SHAPE;
+  if (b == 0) return DF_OK;
+  if (!tok || !depth || !anc || !k_cache || !v_cache || !cache_len || !choice) return DF_ERR_ARG;
+  if (!al16(k_cache) || !al16(v_cache) || !al16(anc) || (tree_feat && !al16(tree_feat))) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < dflash_target_tree_forward_workspace_size(c, b, n_tree)) return DF_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  TargetWs W;
+  target_ws(c, b, n_tree, ws, &W);
+  int* status = status_of(ws);
+  const int d = c->d_model, R = b * n_tree, nf = c->n_feat_layers, Hkv = c->n_kv_heads;
+  const size_t plane = (size_t)b * Hkv * cap * 128;
+  DF_TRY(launch_embed(w->embed, d, c->vocab, tok, nullptr, 1, 0, W.B.h, R, status, st));
+  auto feat_slot = [&](int done_layers) -> int {
+    for (int f = 0; f < nf; ++f)
+      if (c->feat_layers[f] == done_layers) return f;
+    return -1;
+  };
+  for (int li = 0; li < c->n_layers; ++li) {
+    LayerRun L{};
+    L.cfg = c; L.w = &w->layers[li]; L.b = b; L.T = n_tree; L.Rx = R; L.status = status;
+    const int f = tree_feat ? feat_slot(li) : -1;
+    L.capture = f >= 0 ? tree_feat + (size_t)f * d : nullptr;
+    L.ld_capture = nf * d;
+    QkRopeArgs& qk = L.qk;
+    qk.b = b; qk.TA = n_tree; qk.TB = 0; qk.base = cache_len; qk.nnew = nullptr; qk.depth = depth;
+    qk.Hq = c->n_q_heads; qk.Hkv = Hkv; qk.eps = c->rms_eps; qk.theta = c->rope_theta;
+    qk.k_plane = k_cache + (size_t)li * plane; qk.v_plane = v_cache + (size_t)li * plane; qk.cap = cap;
+    qk.status = status;
+    AttnArgs& at = L.at;
+    at.b = b; at.T = n_tree; at.Hq = c->n_q_heads; at.Hkv = Hkv; at.cap = cap;
+    at.dense_len = cache_len; at.dense_add = 0; at.tail_len = n_tree; at.anc = anc;
+    at.scale = 1.0f / sqrtf(128.f);
+    at.nsplit = nsplit_for(b, n_tree, c->n_q_heads, Hkv, cap);
+    at.status = status;
+    DF_TRY(run_layer(L, W.B, st));
+  }
+  RmsNormArgs rn{};
+  const int f = tree_feat ? feat_slot(c->n_layers) : -1;
+  rn.in = W.B.h; rn.gain = w->final_norm; rn.out = W.B.x; rn.ld_out = d; rn.rows = R; rn.d = d; rn.eps = c->rms_eps;
+  rn.group_out = 1; rn.group_in = 1;
+  rn.zero = reinterpret_cast<float*>(W.amax); rn.zero_count = 2LL * R;
+  rn.capture = f >= 0 ? tree_feat + (size_t)f * d : nullptr; rn.ld_capture = nf * d;
+  DF_TRY(launch_rmsnorm(rn, st));
+  GemmDesc g{};
+  g.X = W.B.x; g.W = w->embed; g.M = R; g.N = c->vocab; g.K = d; g.ldx = d; g.ldw = d;
+  g.mode = kGemmArgmax; g.amax = W.amax; g.status = status;
+  DF_TRY(launch_gemm(g, st));
+  return launch_argmax_finalize(W.amax, R, choice, st);
+}
+
+// ------------------------------------------------------------------------ draft block
+size_t dflash_draft_block_workspace_size(const df_model_cfg* dcfg, int b, int max_new) {
+  if (!cfg_ok(dcfg) || b < 0 || max_new < 0 || dcfg->block_size < 2) return kAlign;
+  return draft_ws(dcfg, b, max_new, nullptr, nullptr);
+}
+
+int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, const df_bf16* new_feat, int max_new,
+                       const int32_t* n_new, df_bf16* ctx_k, df_bf16* ctx_v, int32_t* ctx_len, int cap,
+                       const int32_t* bonus, float* logprobs, void* ws, size_t ws_bytes, df_stream stream) {
+  if (!cfg_ok(c) || c->block_size < 2 || c->n_feat_layers < 1) return DF_ERR_SHAPE;
+  if (!w || !w->layers || !w->embed || !w->final_norm || !w->fc || !w->fc_norm) return DF_ERR_ARG;
+  if (b < 0 || max_new < 0 || cap <= 0) return DF_ERR_ARG;
+  if (cap % 8) return DF_ERR_SHAPE;
+  if (b == 0) return DF_OK;
+  if ((max_new > 0 && (!new_feat || !n_new)) || !ctx_k || !ctx_v || !ctx_len || !bonus || !logprobs) return DF_ERR_ARG;
+  if ((new_feat && !al16(new_feat)) || !al16(ctx_k) || !al16(ctx_v) || !al16(logprobs)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < dflash_draft_block_workspace_size(c, b, max_new)) return DF_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  DraftWs W;
+  draft_ws(c, b, max_new, ws, &W);
+  int* status = status_of(ws);
+  const int d = c->d_model, L = c->block_size, Hkv = c->n_kv_heads, nf = c->n_feat_layers;
+  const int R = b * L, Rc = b * max_new;
+  const size_t plane = (size_t)b * Hkv * cap * 128;
+  if (max_new > 0) {
+    len_new_kernel<<<(b + 255) / 256, 256, 0, st>>>(ctx_len, n_new, W.len_new, b);
+    // context fusion: c = RMSNorm(fc . f) into the context rows of x
+    zero_kernel<<<296, 256, 0, st>>>(W.fcacc, (long long)Rc * d);
+    GemmDesc g{};
+    g.X = new_feat; g.W = w->fc; g.M = Rc; g.N = d; g.K = nf * d; g.ldx = (long long)nf * d; g.ldw = (long long)nf * d;
+    g.mode = kGemmAtomicAdd; g.out = W.fcacc; g.ldo = d; g.status = status;
+    DF_TRY(launch_gemm(g, st));
+    RmsNormArgs rn{};
+    rn.in = W.fcacc; rn.gain = w->fc_norm; rn.out = W.B.x + (size_t)R * d; rn.ld_out = d; rn.rows = Rc; rn.d = d;
+    rn.eps = c->rms_eps; rn.group_out = 1; rn.group_in = 1;
+    DF_TRY(launch_rmsnorm(rn, st));
+  } else {
+    copy_len_kernel<<<(b + 255) / 256, 256, 0, st>>>(ctx_len, W.len_new, b);
+  }
+  DF_TRY(launch_embed(w->embed, d, c->vocab, nullptr, bonus, L, c->mask_id, W.B.h, R, status, st));
+  for (int li = 0; li < c->n_layers; ++li) {
+    LayerRun Lr{};
+    Lr.cfg = c; Lr.w = &w->layers[li]; Lr.b = b; Lr.T = L; Lr.Rx = R + Rc; Lr.status = status;
+    QkRopeArgs& qk = Lr.qk;
+    qk.b = b; qk.TA = L; qk.TB = max_new; qk.base = ctx_len; qk.nnew = max_new > 0 ? n_new : nullptr;
+    qk.depth = nullptr;
+    qk.Hq = c->n_q_heads; qk.Hkv = Hkv; qk.eps = c->rms_eps; qk.theta = c->rope_theta;
+    qk.k_plane = ctx_k + (size_t)li * plane; qk.v_plane = ctx_v + (size_t)li * plane; qk.cap = cap;
+    qk.status = status;
+    AttnArgs& at = Lr.at;
+    at.b = b; at.T = L; at.Hq = c->n_q_heads; at.Hkv = Hkv; at.cap = cap;
+    at.dense_len = W.len_new; at.dense_add = L; at.tail_len = 0; at.anc = nullptr;
+    at.scale = 1.0f / sqrtf(128.f);
+    at.nsplit = nsplit_for(b, L, c->n_q_heads, Hkv, cap);
+    at.status = status;
+    DF_TRY(run_layer(Lr, W.B, st));
+  }
+  RmsNormArgs rn{};
+  rn.in = W.B.h; rn.gain = w->final_norm; rn.out = W.xl; rn.ld_out = d; rn.rows = b * (L - 1); rn.d = d;
+  rn.eps = c->rms_eps; rn.group_out = L - 1; rn.group_in = L; rn.in_off = 1;
+  DF_TRY(launch_rmsnorm(rn, st));
+  GemmDesc g{};
+  g.X = W.xl; g.W = w->embed; g.M = b * (L - 1); g.N = c->vocab; g.K = d; g.ldx = d; g.ldw = d;
+  g.mode = kGemmStore; g.out = logprobs; g.ldo = c->vocab; g.status = status;
+  DF_TRY(launch_gemm(g, st));
+  DF_TRY(launch_logsoftmax(logprobs, b * (L - 1), c->vocab, st));
+  copy_len_kernel<<<(b + 255) / 256, 256, 0, st>>>(W.len_new, ctx_len, b);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+}  // extern "C"
+
+extern "C" {
+size_t dflash_linear_workspace_size(void) { return 256; }
+
+int dflash_linear(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out, int accumulate, void* ws,
+                  size_t ws_bytes, df_stream stream) {
+  if (M < 0 || N < 0 || K <= 0) return DF_ERR_ARG;
+  if (K % 64) return DF_ERR_SHAPE;
+  if (M == 0 || N == 0) return DF_OK;
+  if (!X || !W || !out) return DF_ERR_ARG;
+  if (!al16(X) || !al16(W) || !al16(out)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < dflash_linear_workspace_size()) return DF_ERR_WORKSPACE;
+  GemmDesc g{};
+  g.X = X; g.W = W; g.M = M; g.N = N; g.K = K; g.ldx = K; g.ldw = K;
+  g.mode = accumulate ? kGemmAtomicAdd : kGemmStore;
+  g.out = out; g.ldo = N; g.status = status_of(ws);
+  return launch_gemm(g, (cudaStream_t)stream);
+}
+}

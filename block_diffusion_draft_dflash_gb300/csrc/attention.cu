@@ -1,0 +1,425 @@
+// Attention of a block of query rows over a sequence's KV cache, on tcgen05 tensor cores.
+//
+// Serves both attention calls of the speculative step:
+//   * tree verification (summary of "Accelerating Speculative Decoding with Block
+//     Diffusion Draft Trees", section "방법론 자세히 보기"): every flattened tree row
+//     sees the whole cache [0, N) and, among the tree's own slots N .. N+T-1, only its
+//     ancestors and itself (bit j of its ancestor row);
+//   * the drafter ("DFlash: Block Diffusion for Flash Speculative Decoding 논문 정리",
+//     sections "DFlash의 핵심 아이디어" and "학습 방식도 추론 시나리오에 맞춰 바꿨다"):
+//     every block row sees every injected context slot and every block row, no mask.
+// Both are "dense prefix [0, dense_len) + optional ancestor-masked tail".
+//
+// Tile: 128 query rows = (128 / G) consecutive tree nodes x the G query heads that share
+// one kv head (GQA), so one K/V tile feeds all 128 rows.  Per 128-key block:
+//   S = Q K^T   (tcgen05.mma, M=128 N=128 K=128, accumulator in TMEM, double-buffered)
+//   softmax     (4 warps, one TMEM lane = one query row per thread, exp2 domain, running
+//                max / sum; the ancestor mask is applied as 32-bit words per key group)
+//   O += P V    (P written bf16 to shared memory in the 128-byte-swizzled K-major layout,
+//                V stored transposed in the cache so that its tile is K-major too)
+// Warp roles: warps 0-3 softmax/epilogue, warp 4 TMA producer, warp 5 TMEM owner + MMA.
+// The key range of a sequence is split over CTAs (split-KV) when the grid would
+// otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
+#include "attention.h"
+#include "common.cuh"
+
+namespace df {
+
+constexpr int kAttnThreads = 192;
+constexpr int kKB = 128;     // keys per block
+constexpr int kKVStages = 2;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128x128 bf16 tile = 2 swizzled slabs
+
+DF_DEV int floordiv32(int t) { return t >= 0 ? (t >> 5) : -((-t + 31) >> 5); }
+
+// 32 ancestor bits for tail indices t0 .. t0+31 (bit c <-> t0 + c); out of range -> 0.
+DF_DEV uint32_t anc_bits32(const uint32_t* row, int W, int t0) {
+  const int w = floordiv32(t0);
+  const int sh = t0 - 32 * w;
+  const uint32_t lo = (w >= 0 && w < W) ? row[w] : 0u;
+  const uint32_t hi = (w + 1 >= 0 && w + 1 < W) ? row[w + 1] : 0u;
+  return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
+}
+
+// Dense bits for keys j0 .. j0+31: set where j < dense_len.
+DF_DEV uint32_t dense_bits32(int j0, int dense_len) {
+  const int n = dense_len - j0;
+  return n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+DF_DEV void store_p_row(unsigned char* p_smem, int r, const uint32_t* packed /*64 words = 128 bf16*/) {
+  // two 64-key slabs; row r at r*128 B; 16-byte chunk c stored at chunk (c ^ (r & 7))
+#pragma unroll
+  for (int slab = 0; slab < 2; ++slab) {
+    unsigned char* rowp = p_smem + slab * (kTileBytes / 2) + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t* w = packed + slab * 32 + c * 4;
+      *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* q_smem = smem;                               // 32 KB
+  unsigned char* kv_smem = smem + kTileBytes;                 // stages x (K 32 KB + V 32 KB)
+  unsigned char* p_smem = kv_smem + kKVStages * 2 * kTileBytes;  // 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p_smem + kTileBytes);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + kKVStages;
+  uint64_t* s_full = kv_empty + kKVStages;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* o_done = p_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // work unit -> (sequence, kv head, query tile, split)
+  int u = blockIdx.x;
+  const int split = u % p.nsplit; u /= p.nsplit;
+  const int qt = u % p.n_qtiles; u /= p.n_qtiles;
+  const int kvh = u % p.Hkv;
+  const int s = u / p.Hkv;
+  const int G = p.Hq / p.Hkv, NPT = 128 / G;
+  const int dense_len = p.dense_len[s] + p.dense_add;
+  const int Lk = dense_len + p.tail_len;
+  const int nb = (Lk + kKB - 1) / kKB;
+  const int kb0 = (int)((long long)nb * split / p.nsplit), kb1 = (int)((long long)nb * (split + 1) / p.nsplit);
+  const int nblk = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kKVStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 128); }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S0: cols 0-127, S1: 128-255, O: 256-383
+
+  if (warp == 4) {
+    if (lane == 0 && nblk > 0) {
+      // ------------------------------------------------------------ TMA producer
+      const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      const int qz = s * p.T + qt * NPT;
+      tma_load_3d(q_smem, &tmQ, q_full, 0, kvh * G, qz, pol_q);
+      tma_load_3d(q_smem + kTileBytes / 2, &tmQ, q_full, 64, kvh * G, qz, pol_q);
+      const int plane = s * p.Hkv + kvh;
+      bool ok = true;
+      for (int j = 0; j < nblk && ok; ++j) {
+        const int st = j % kKVStages;
+        if (!mbar_wait(&kv_empty[st], ((j / kKVStages) & 1) ^ 1, p.status, 11)) { ok = false; break; }
+        unsigned char* kb = kv_smem + st * 2 * kTileBytes;
+        unsigned char* vb = kb + kTileBytes;
+        const int key0 = (kb0 + j) * kKB;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
+        tma_load_2d(kb, &tmK, &kv_full[st], 0, plane * p.cap + key0, pol_kv);
+        tma_load_2d(kb + kTileBytes / 2, &tmK, &kv_full[st], 64, plane * p.cap + key0, pol_kv);
+        tma_load_2d(vb, &tmV, &kv_full[st], key0, plane * 128, pol_kv);
+        tma_load_2d(vb + kTileBytes / 2, &tmV, &kv_full[st], key0 + 64, plane * 128, pol_kv);
+      }
+      if (!ok) {
+        mbar_wait(q_full, 0, nullptr, 0);
+        for (int st = 0; st < kKVStages; ++st) mbar_wait(&kv_full[st], 0, nullptr, 0);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0 && nblk > 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(128, 128);
+      const uint32_t qa = smem_u32(q_smem), pa = smem_u32(p_smem);
+      bool ok = mbar_wait(q_full, 0, p.status, 12);
+      tc_fence_after();
+      auto issue_pv = [&](int j) -> bool {
+        if (!mbar_wait(p_full, j & 1, p.status, 13)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(kv_smem + (j % kKVStages) * 2 * kTileBytes + kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+          mma_bf16(tmem + 256, sdesc_kmajor_sw128(pa + off), sdesc_kmajor_sw128(vb + off), idesc,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(o_done);
+        mma_commit(&kv_empty[j % kKVStages]);
+        return true;
+      };
+      for (int j = 0; j < nblk && ok; ++j) {
+        const int st = j % kKVStages;
+        if (!mbar_wait(&kv_full[st], (j / kKVStages) & 1, p.status, 14)) { ok = false; break; }
+        if (!mbar_wait(&s_empty[j & 1], ((j >> 1) & 1) ^ 1, p.status, 15)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(kv_smem + st * 2 * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+          mma_bf16(tmem + (j & 1) * 128, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off), idesc,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[j & 1]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(nblk - 1);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax (warps 0-3)
+    const int r = warp * 32 + lane;  // query row == TMEM lane
+    const int node = qt * NPT + r / G, head = kvh * G + r % G;
+    const bool row_ok = node < p.T;
+    const uint32_t* anc_row = (p.anc && row_ok) ? p.anc + ((size_t)s * p.T + node) * p.W : nullptr;
+    const float scale2 = p.scale * 1.4426950408889634f;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nblk; ++j) {
+      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.status, 16)) { ok = false; break; }
+      tc_fence_after();
+      float sv[128];
+#pragma unroll
+      for (int c = 0; c < 128; c += 16) tmem_ld16(tmem + lane_base + (j & 1) * 128 + c, sv + c);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s_empty[j & 1]);
+      // admission mask for keys key0 .. key0+127
+      const int key0 = (kb0 + j) * kKB;
+      uint32_t adm[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int j0 = key0 + 32 * g;
+        uint32_t bits = dense_bits32(j0, dense_len);
+        if (anc_row) bits |= anc_bits32(anc_row, p.W, j0 - dense_len);
+        else if (!row_ok) bits |= 0u;
+        // keys of the tail beyond tail_len carry no ancestor bits, keys >= Lk none at all
+        adm[g] = bits;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const bool a = (adm[c >> 5] >> (c & 31)) & 1u;
+        sv[c] = a ? sv[c] * scale2 : -INFINITY;
+        mx = fmaxf(mx, sv[c]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+      uint32_t packed[64];
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = (m_new == -INFINITY) ? 0.f : exp2f(sv[c] - m_new);
+        const float p1 = (m_new == -INFINITY) ? 0.f : exp2f(sv[c + 1] - m_new);
+        psum += p0 + p1;
+        packed[c >> 1] = (uint32_t)f_to_bf16(p0) | ((uint32_t)f_to_bf16(p1) << 16);
+      }
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      if (j >= 1) {
+        // PV of the previous block must be complete before P is overwritten / O rescaled
+        if (!mbar_wait(o_done, (j - 1) & 1, p.status, 17)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t oaddr = tmem + lane_base + 256;
+#pragma unroll
+          for (int c = 0; c < 128; c += 16) {
+            float o[16];
+            tmem_ld16(oaddr + c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            tmem_st16(oaddr + c, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      store_p_row(p_smem, r, packed);
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok && nblk > 0) ok = mbar_wait(o_done, (nblk - 1) & 1, p.status, 18);
+    tc_fence_after();
+    const size_t grow = ((size_t)s * p.T + node) * p.Hq + head;  // global query row
+    if (p.nsplit == 1) {
+      if (row_ok) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * 128);
+#pragma unroll
+        for (int c = 0; c < 128; c += 16) {
+          float o[16];
+          if (nblk > 0) { tmem_ld16(tmem + lane_base + 256 + c, o); tmem_ld_wait(); }
+          else { for (int i = 0; i < 16; ++i) o[i] = 0.f; }
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            w[i] = (uint32_t)f_to_bf16(o[2 * i] * inv) | ((uint32_t)f_to_bf16(o[2 * i + 1] * inv) << 16);
+          dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      } else if (nblk > 0) {
+        float o[16];
+        for (int c = 0; c < 128; c += 16) { tmem_ld16(tmem + lane_base + 256 + c, o); tmem_ld_wait(); }
+      }
+    } else {
+      const size_t nrows = (size_t)p.b * p.T * p.Hq;
+      float* op = p.o_part + ((size_t)split * nrows + grow) * 128;
+#pragma unroll
+      for (int c = 0; c < 128; c += 16) {
+        float o[16];
+        if (nblk > 0) { tmem_ld16(tmem + lane_base + 256 + c, o); tmem_ld_wait(); }
+        else { for (int i = 0; i < 16; ++i) o[i] = 0.f; }
+        if (row_ok)
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(op + c + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+      }
+      if (row_ok) {
+        p.ml_part[((size_t)split * nrows + grow) * 2] = m_run;
+        p.ml_part[((size_t)split * nrows + grow) * 2 + 1] = l_run;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// One warp per query row: out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ o_part,
+                                                           const float* __restrict__ ml_part, int nsplit,
+                                                           long long nrows, df_bf16* __restrict__ out) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= nrows) return;
+  float M = -INFINITY;
+  for (int j = 0; j < nsplit; ++j) M = fmaxf(M, ml_part[((size_t)j * nrows + row) * 2]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  for (int j = 0; j < nsplit; ++j) {
+    const float m = ml_part[((size_t)j * nrows + row) * 2];
+    if (m == -INFINITY) continue;
+    const float w = exp2f(m - M);
+    L += w * ml_part[((size_t)j * nrows + row) * 2 + 1];
+    const float4 o = reinterpret_cast<const float4*>(o_part + ((size_t)j * nrows + row) * 128)[lane];
+    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint2 r;
+  r.x = (uint32_t)f_to_bf16(acc.x * inv) | ((uint32_t)f_to_bf16(acc.y * inv) << 16);
+  r.y = (uint32_t)f_to_bf16(acc.z * inv) | ((uint32_t)f_to_bf16(acc.w * inv) << 16);
+  reinterpret_cast<uint2*>(out + row * 128)[lane] = r;
+}
+
+// ----------------------------------------------------------------------------- host
+static int make_tmap(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                     const cuuint32_t* box) {
+  typedef CUresult (*Fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
+                         const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                         CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Fn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return DF_ERR_CUDA;
+    fn = reinterpret_cast<Fn>(f);
+  }
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DF_OK : DF_ERR_CUDA;
+}
+
+int attn_num_splits(int b, int Hkv, int n_qtiles, int max_keys) {
+  const int units = b * Hkv * n_qtiles;
+  const int nsm = num_sms_attn();
+  const int nb = (max_keys + kKB - 1) / kKB;
+  int ns = (nsm + units - 1) / units;
+  if (ns > nb) ns = nb;
+  if (ns > kAttnMaxSplits) ns = kAttnMaxSplits;
+  if (ns < 1) ns = 1;
+  return ns;
+}
+
+int num_sms_attn() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+int launch_attention(const AttnArgs& a, cudaStream_t st) {
+  const int G = a.Hq / a.Hkv;
+  const int NPT = 128 / G;
+  const int n_qtiles = (a.T + NPT - 1) / NPT;
+  CUtensorMap tq, tk, tv;
+  {
+    cuuint64_t dims[3] = {128, (cuuint64_t)a.Hq, (cuuint64_t)a.b * a.T};
+    cuuint64_t str[2] = {(cuuint64_t)128 * 2, (cuuint64_t)a.Hq * 128 * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)NPT};
+    if (make_tmap(&tq, a.q, 3, dims, str, box)) return DF_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[2] = {128, (cuuint64_t)a.b * a.Hkv * a.cap};
+    cuuint64_t str[1] = {(cuuint64_t)128 * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (make_tmap(&tk, a.k_plane, 2, dims, str, box)) return DF_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.cap, (cuuint64_t)a.b * a.Hkv * 128};
+    cuuint64_t str[1] = {(cuuint64_t)a.cap * 2};
+    cuuint32_t box[2] = {64, 128};
+    if (make_tmap(&tv, a.v_plane, 2, dims, str, box)) return DF_ERR_CUDA;
+  }
+  AttnParams p{};
+  p.b = a.b; p.T = a.T; p.Hq = a.Hq; p.Hkv = a.Hkv; p.cap = a.cap;
+  p.dense_len = a.dense_len; p.dense_add = a.dense_add; p.tail_len = a.tail_len;
+  p.anc = a.anc; p.W = a.anc ? (a.tail_len + 31) / 32 : 0;
+  p.scale = a.scale;
+  p.n_qtiles = n_qtiles;
+  p.nsplit = a.nsplit;
+  p.out = a.out; p.o_part = a.o_part; p.ml_part = a.ml_part;
+  p.status = a.status;
+  const size_t smem = 1024 + kTileBytes * (2 + 2 * kKVStages) + 256;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return DF_ERR_CUDA;
+    attr = true;
+  }
+  const int grid = a.b * a.Hkv * n_qtiles * a.nsplit;
+  attn_tc_kernel<<<grid, kAttnThreads, smem, st>>>(tq, tk, tv, p);
+  if (cudaGetLastError() != cudaSuccess) return DF_ERR_CUDA;
+  if (a.nsplit > 1) {
+    const long long nrows = (long long)a.b * a.T * a.Hq;
+    attn_combine_kernel<<<(unsigned)((nrows + 7) / 8), 256, 0, st>>>(a.o_part, a.ml_part, a.nsplit, nrows, a.out);
+    if (cudaGetLastError() != cudaSuccess) return DF_ERR_CUDA;
+  }
+  return DF_OK;
+}
+
+size_t attn_partial_bytes(int b, int T, int Hq, int nsplit) {
+  const size_t rows = (size_t)b * T * Hq;
+  return nsplit > 1 ? rows * nsplit * (128 * 4 + 8) : 0;
+}
+
+}  // namespace df

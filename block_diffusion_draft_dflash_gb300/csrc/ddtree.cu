@@ -1,0 +1,329 @@
+// DDTree construction on the GPU: per-position top-K, then best-first max-heap selection
+// of the B most probable prefixes, then the ancestor bitsets of the flattened tree.
+//
+// Method: summary of "Accelerating Speculative Decoding with Block Diffusion Draft
+// Trees" (bluediary8.tistory.com/1288), section "방법론 자세히 보기": the best B-node
+// tree is the set of B prefixes with the highest prefix probability under the factorized
+// per-position distribution, found by a best-first max-heap in O(B log B).
+//
+// Kernel 1 (topk_rows_kernel): one CTA per (sequence, position) row of V log-probs.
+//   Radix select on order-preserving 32-bit keys (12 + 12 + 8 bit digits, MSB first,
+//   warp-aggregated shared-memory histograms) finds the K-th largest key T.  A gather
+//   pass takes every key > T and the lowest-id keys == T, and a bitonic sort orders the
+//   K survivors by (log-prob desc, token id asc).
+// Kernel 2 (ddtree_heap_kernel): one CTA per sequence.  One thread runs the heap: each
+//   entry is a single 64-bit key whose integer order is the tree's total order
+//   (score desc, depth asc, parent index asc, rank asc), so every heap comparison is one
+//   integer compare.  The CTA then writes the node arrays and the ancestor bitsets
+//   (one warp per row; each lane owns a 32-bit word).
+#include "common.cuh"
+
+namespace df {
+
+constexpr int kTopkThreads = 1024;
+constexpr int kMaxK = 2048;
+
+DF_DEV void hist_add(uint32_t* hist, uint32_t digit, bool active) {
+  // Lanes with the same digit add once through their leader.
+  const uint32_t lanes = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const uint32_t peers = __match_any_sync(lanes, digit);
+  const int lane = threadIdx.x & 31;
+  if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[digit], __popc(peers));
+}
+
+// Inclusive block scan of one value per thread (1024 threads).
+DF_DEV uint32_t block_scan_incl(uint32_t v, uint32_t* warp_tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tmp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_tmp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_tmp[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t off = warp ? warp_tmp[warp - 1] : 0u;
+  __syncthreads();
+  return v + off;
+}
+
+template <bool kVec4>
+__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __restrict__ lp, int V, int K,
+                                                                 int32_t* __restrict__ out_id,
+                                                                 float* __restrict__ out_val, int* status) {
+  __shared__ uint32_t hist[4096];
+  __shared__ uint32_t warp_tmp[32];
+  __shared__ unsigned long long sel[kMaxK];
+  __shared__ uint32_t sh_bin, sh_above, sh_ngt, sh_eq_base, sh_nan;
+  const int tid = threadIdx.x;
+  const size_t row = blockIdx.x;
+  const float* x = lp + row * (size_t)V;
+  if (tid == 0) { sh_nan = 0; sh_ngt = 0; sh_eq_base = 0; }
+
+  uint32_t prefix = 0;
+  int krem = K;
+  const int shifts[3] = {20, 8, 0};
+  const int widths[3] = {12, 12, 8};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass], width = widths[pass], nb = 1 << width;
+    for (int i = tid; i < nb; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    const uint32_t mask = nb - 1;
+    const int hi_shift = shift + width;  // bits above this digit must equal `prefix`
+    auto visit = [&](float f, bool valid) {
+      const uint32_t k = float_key(f);
+      bool take = valid;
+      if (pass == 0) {
+        if (valid && isnan(f)) { sh_nan = 1; take = false; }
+      } else {
+        take = take && ((k >> hi_shift) == prefix);
+      }
+      hist_add(hist, (k >> shift) & mask, take);
+    };
+    if (kVec4) {
+      const float4* x4 = reinterpret_cast<const float4*>(x);
+      const int n4 = V >> 2;
+      for (int base = 0; base < n4; base += kTopkThreads) {
+        const int i = base + tid;
+        float4 f = (i < n4) ? __ldg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool ok = i < n4;
+        visit(f.x, ok); visit(f.y, ok); visit(f.z, ok); visit(f.w, ok);
+      }
+    } else {
+      for (int base = 0; base < V; base += kTopkThreads) {
+        const int i = base + tid;
+        visit(i < V ? __ldg(x + i) : 0.f, i < V);
+      }
+    }
+    __syncthreads();
+    if (sh_nan) {
+      if (tid == 0) set_status(status, DF_ERR_NAN, (int)row);
+      return;
+    }
+    // Bins in descending key order: position p <-> bin nb-1-p.  Thread t owns positions
+    // [t*per, (t+1)*per) where per = nb / 1024 (or one position for t < nb if nb < 1024).
+    const int per = nb >= kTopkThreads ? nb / kTopkThreads : 1;
+    const bool owns = nb >= kTopkThreads || tid < nb;
+    uint32_t local = 0;
+    if (owns)
+      for (int j = 0; j < per; ++j) local += hist[nb - 1 - (tid * per + j)];
+    const uint32_t incl = block_scan_incl(local, warp_tmp);
+    const uint32_t excl = incl - local;
+    if (owns && excl < (uint32_t)krem && (uint32_t)krem <= incl) {
+      uint32_t acc = excl;
+      for (int j = 0; j < per; ++j) {
+        const int bin = nb - 1 - (tid * per + j);
+        const uint32_t c = hist[bin];
+        if (acc + c >= (uint32_t)krem) { sh_bin = bin; sh_above = acc; break; }
+        acc += c;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << width) | sh_bin;
+    krem -= (int)sh_above;
+    __syncthreads();
+  }
+  // prefix == T (the K-th largest key); krem = how many keys equal to T are taken.
+  const uint32_t T = prefix;
+  const uint32_t n_eq_total = hist[T & 0xFF];
+  const int n_gt = K - krem;
+  const bool need_lowest = n_eq_total > (uint32_t)krem;  // ties straddle the cut
+  // Gather keys > T (any order), and keys == T when all of them are taken.
+  auto put = [&](float f, int i, bool valid) {
+    if (!valid) return;
+    const uint32_t k = float_key(f);
+    if (k > T || (k == T && !need_lowest)) {
+      const uint32_t pos = atomicAdd(&sh_ngt, 1u);
+      if (pos < (uint32_t)kMaxK) sel[pos] = ((unsigned long long)k << 32) | (uint32_t)(~(uint32_t)i);
+    }
+  };
+  if (kVec4) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const int n4 = V >> 2;
+    for (int i = tid; i < n4; i += kTopkThreads) {
+      const float4 f = __ldg(x4 + i);
+      put(f.x, 4 * i, true); put(f.y, 4 * i + 1, true); put(f.z, 4 * i + 2, true); put(f.w, 4 * i + 3, true);
+    }
+  } else {
+    for (int i = tid; i < V; i += kTopkThreads) put(__ldg(x + i), i, true);
+  }
+  __syncthreads();
+  if (need_lowest) {
+    // Take the krem lowest indices with key == T, scanning in index order.
+    for (int base = 0; base < V; base += kTopkThreads) {
+      const int i = base + tid;
+      const bool eq = i < V && float_key(__ldg(x + i)) == T;
+      const uint32_t incl = block_scan_incl(eq ? 1u : 0u, warp_tmp);
+      const uint32_t rank = sh_eq_base + incl - (eq ? 1u : 0u);
+      if (eq && rank < (uint32_t)krem)
+        sel[n_gt + rank] = ((unsigned long long)T << 32) | (uint32_t)(~(uint32_t)i);
+      __syncthreads();
+      if (tid == kTopkThreads - 1) sh_eq_base += incl;
+      __syncthreads();
+      if (sh_eq_base >= (uint32_t)krem) break;
+    }
+  }
+  // Bitonic sort (descending) of K entries padded to a power of two with zeros.
+  int n = 1;
+  while (n < K) n <<= 1;
+  for (int i = K + tid; i < n; i += kTopkThreads) sel[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n; i += kTopkThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const unsigned long long a = sel[i], b = sel[j];
+          const bool desc = (i & size) == 0;
+          if (desc ? (a < b) : (a > b)) { sel[i] = b; sel[j] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int r = tid; r < K; r += kTopkThreads) {
+    const unsigned long long c = sel[r];
+    out_id[row * K + r] = (int32_t)(~(uint32_t)(c & 0xFFFFFFFFull));
+    out_val[row * K + r] = key_float((uint32_t)(c >> 32));
+  }
+}
+
+// ----------------------------------------------------------------------------- heap
+// 64-bit heap key, larger = earlier in the tree's total order:
+//   [63:32] float_key(score)  [31:27] 31-depth  [26:16] 2047-parent  [15:5] 2047-rank
+DF_DEV unsigned long long heap_key(float s, int depth, int parent, int rank) {
+  return ((unsigned long long)float_key(s) << 32) | ((uint32_t)(31 - depth) << 27) |
+         ((uint32_t)(2047 - parent) << 16) | ((uint32_t)(2047 - rank) << 5);
+}
+
+__global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restrict__ topk_id,
+                                                          const float* __restrict__ topk_val, int D, int K, int B,
+                                                          const int32_t* __restrict__ root_tok,
+                                                          int32_t* __restrict__ tok, int32_t* __restrict__ parent,
+                                                          int32_t* __restrict__ depth, float* __restrict__ score,
+                                                          uint32_t* __restrict__ anc, const int* status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int s = blockIdx.x, tid = threadIdx.x;
+  const int n = B + 1;
+  const int W = (n + 31) / 32;
+  float* val = reinterpret_cast<float*>(smem);                                       // [D][K]
+  unsigned long long* heap = reinterpret_cast<unsigned long long*>(val + ((D * K + 1) & ~1));  // [B+2]
+  int32_t* n_par = reinterpret_cast<int32_t*>(heap + (B + 2));                       // [n]
+  int32_t* n_dep = n_par + n;                                                        // [n]
+  int32_t* n_rank = n_dep + n;                                                       // [n]
+  float* n_score = reinterpret_cast<float*>(n_rank + n);                             // [n]
+
+  if (status && *(volatile const int*)status == DF_ERR_NAN) return;  // NaN found by top-K
+  const float* gval = topk_val + (size_t)s * D * K;
+  for (int i = tid; i < D * K; i += blockDim.x) val[i] = gval[i];
+  __syncthreads();
+
+  if (tid == 0) {
+    n_par[0] = -1; n_dep[0] = 0; n_rank[0] = -1; n_score[0] = 0.f;
+    int hn = 0;
+    auto push = [&](unsigned long long key) {
+      int i = hn++;
+      while (i > 0) {
+        const int p = (i - 1) >> 1;
+        const unsigned long long hp = heap[p];
+        if (hp >= key) break;
+        heap[i] = hp;
+        i = p;
+      }
+      heap[i] = key;
+    };
+    if (B > 0) push(heap_key(0.f + val[0], 1, 0, 0));
+    for (int idx = 1; idx <= B; ++idx) {
+      const unsigned long long top = heap[0];
+      const unsigned long long last = heap[--hn];
+      int i = 0;
+      while (true) {  // sift `last` down from the root
+        int c = 2 * i + 1;
+        if (c >= hn) break;
+        unsigned long long hc = heap[c];
+        if (c + 1 < hn) {
+          const unsigned long long h2 = heap[c + 1];
+          if (h2 > hc) { hc = h2; ++c; }
+        }
+        if (hc <= last) break;
+        heap[i] = hc;
+        i = c;
+      }
+      if (hn > 0) heap[i] = last;
+      const uint32_t lo = (uint32_t)top;
+      const int dep = 31 - (int)(lo >> 27);
+      const int par = 2047 - (int)((lo >> 16) & 0x7FF);
+      const int r = 2047 - (int)((lo >> 5) & 0x7FF);
+      const float sc = key_float((uint32_t)(top >> 32));
+      n_par[idx] = par; n_dep[idx] = dep; n_rank[idx] = r; n_score[idx] = sc;
+      if (dep < D) push(heap_key(sc + val[dep * K], dep + 1, idx, 0));
+      if (r + 1 < K) push(heap_key(n_score[par] + val[(dep - 1) * K + r + 1], dep, par, r + 1));
+    }
+  }
+  __syncthreads();
+
+  const size_t o = (size_t)s * n;
+  const int32_t* gid = topk_id + (size_t)s * D * K;
+  for (int i = tid; i < n; i += blockDim.x) {
+    tok[o + i] = i == 0 ? (root_tok ? root_tok[s] : -1) : gid[(n_dep[i] - 1) * K + n_rank[i]];
+    parent[o + i] = n_par[i];
+    depth[o + i] = n_dep[i];
+    score[o + i] = n_score[i];
+  }
+  // Ancestor bitsets: one warp per row, lane w owns words w, w+32, ...
+  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  uint32_t* arow = anc + (size_t)s * n * W;
+  for (int i = warp; i < n; i += nwarps) {
+    for (int w0 = 0; w0 < W; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t bits = 0;
+      for (int j = i; j >= 0; j = n_par[j])
+        if ((j >> 5) == w) bits |= 1u << (j & 31);
+      if (w < W) arow[(size_t)i * W + w] = bits;
+    }
+  }
+}
+
+}  // namespace df
+
+// ----------------------------------------------------------------------------- host
+namespace df {
+size_t ddtree_heap_smem(int D, int K, int B) {
+  const int n = B + 1;
+  return (size_t)((D * K + 1) & ~1) * 4 + (size_t)(B + 2) * 8 + (size_t)n * 16;
+}
+
+int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
+                  int32_t* parent, int32_t* depth, float* score, uint32_t* anc, int32_t* topk_id,
+                  float* topk_val, int* status, cudaStream_t st) {
+  const int K = B < V ? B : V;
+  if (B > 0) {
+    const int rows = b * D;
+    if ((V & 3) == 0)
+      topk_rows_kernel<true><<<rows, kTopkThreads, 0, st>>>(lp, V, K, topk_id, topk_val, status);
+    else
+      topk_rows_kernel<false><<<rows, kTopkThreads, 0, st>>>(lp, V, K, topk_id, topk_val, status);
+  }
+  const size_t smem = ddtree_heap_smem(D, K > 0 ? K : 1, B);
+  static thread_local size_t configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    if (cudaFuncSetAttribute(ddtree_heap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DF_ERR_CUDA;
+    configured = smem;
+  }
+  ddtree_heap_kernel<<<b, 256, smem, st>>>(topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok, tok, parent, depth,
+                                           score, anc, status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+}  // namespace df

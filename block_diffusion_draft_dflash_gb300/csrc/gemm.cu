@@ -1,0 +1,343 @@
+// Weight-streaming GEMM on 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+//   out[t][n] (+)= sum_k X[t][k] * W[n][k]        X: [M tokens][K] bf16, W: [N][K] bf16
+//
+// The token count is small in every projection of the speculative step (16 to a few
+// hundred rows per sequence) while the weights are large, so the kernel is organised
+// around streaming W exactly once from HBM:
+//   * swap-AB: the MMA's 128-row A operand is a 128-row slice of W and the token tile is
+//     the MMA's N dimension (16..256, a multiple of 16), so a 16-token drafter GEMM still
+//     runs full-width tensor instructions;
+//   * persistent CTAs (one per SM) split the (tile, k-block) iteration space evenly
+//     ("stream-K"), so the grid stays full however few 128-row weight tiles there are;
+//     partial tiles are summed with fp32 reductions into the output (which, for the
+//     o- and down-projections, is the fp32 residual stream itself);
+//   * warp roles: warp 0 issues TMA loads into a multi-stage shared-memory ring,
+//     warp 1 owns the TMEM allocation and one lane issues tcgen05.mma, warps 2-5 drain
+//     double-buffered TMEM accumulators (tcgen05.ld) and write the epilogue;
+//   * epilogues: fp32 reduction-add, fp32 store (whole tiles), or fused argmax over the
+//     output features (whole tiles; the target LM head writes no logits).
+// Every mbarrier wait is bounded (common.cuh); a timeout is recorded in the status word.
+#include <mutex>
+#include <unordered_map>
+
+#include "common.cuh"
+#include "gemm.h"
+
+namespace df {
+
+constexpr int kGemmThreads = 192;
+constexpr int kBM = 128;  // weight rows per tile (MMA M)
+constexpr int kBK = 64;   // k per stage (one 128-byte swizzle row)
+
+struct GemmParams {
+  int M, N, K;
+  int n_ttiles, BN, k_iters;
+  long long total_iters;
+  int whole_tiles;  // 1: each CTA owns whole tiles (store / argmax epilogues)
+  int mode;
+  float* out;
+  int ldo;
+  unsigned long long* amax;  // argmax keys [M]
+  int* status;
+  int stages;
+};
+
+struct Segment {
+  long long tile;
+  int k0, k1;
+};
+
+// Iteration range of CTA c and its decomposition into per-tile segments.
+DF_DEV void cta_range(const GemmParams& p, long long& it0, long long& it1) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  if (p.whole_tiles) {
+    const long long tiles = p.total_iters / p.k_iters;
+    it0 = (tiles * c / G) * p.k_iters;
+    it1 = (tiles * (c + 1) / G) * p.k_iters;
+  } else {
+    it0 = p.total_iters * c / G;
+    it1 = p.total_iters * (c + 1) / G;
+  }
+}
+DF_DEV bool next_segment(const GemmParams& p, long long& it, long long it1, Segment& s) {
+  if (it >= it1) return false;
+  s.tile = it / p.k_iters;
+  s.k0 = (int)(it - s.tile * p.k_iters);
+  const long long tile_end = (s.tile + 1) * p.k_iters;
+  const long long e = tile_end < it1 ? tile_end : it1;
+  s.k1 = s.k0 + (int)(e - it);
+  it = e;
+  return true;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                        const GemmParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = p.BN, S = p.stages;
+  const uint32_t w_bytes = kBM * kBK * 2, x_bytes = (uint32_t)BN * kBK * 2;
+  const uint32_t stage_bytes = w_bytes + x_bytes;  // multiple of 1024 (BN multiple of 16... see host)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tmem_cols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 128); }
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, tmem_cols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  long long it0, it1;
+  cta_range(p, it0, it1);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    long long it = it0;
+    Segment sg;
+    bool ok = true;
+    long long issued = 0;
+    while (ok && next_segment(p, it, it1, sg)) {
+      const int wt = (int)(sg.tile / p.n_ttiles), tt = (int)(sg.tile % p.n_ttiles);
+      for (int k = sg.k0; k < sg.k1; ++k) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 1)) { ok = false; break; }
+        unsigned char* sb = smem + (size_t)stage * stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], stage_bytes);
+        tma_load_2d(sb, &tmW, &full[stage], k * kBK, wt * kBM, pol_w);
+        tma_load_2d(sb + w_bytes, &tmX, &full[stage], k * kBK, tt * BN, pol_x);
+        ++issued;
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (!ok) {
+      // Drain: wait (bounded) for the loads still in flight before the CTA may exit.
+      const long long n = issued < S ? issued : S;
+      int st = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < n; ++i) {
+        if (--st < 0) { st = S - 1; ph ^= 1; }
+        mbar_wait(&full[st], ph, nullptr, 0);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(kBM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    long long it = it0;
+    Segment sg;
+    int si = 0;
+    bool ok = true;
+    while (ok && next_segment(p, it, it1, sg)) {
+      const int acc = si & 1;
+      if (!mbar_wait(&tempty[acc], ((si >> 1) & 1) ^ 1, p.status, 2)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int k = sg.k0; k < sg.k1; ++k) {
+        if (!mbar_wait(&full[stage], phase, p.status, 3)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + (size_t)stage * stage_bytes);
+        const uint64_t adesc = sdesc_kmajor_sw128(sa);
+        const uint64_t bdesc = sdesc_kmajor_sw128(sa + w_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (k > sg.k0 || kk > 0) ? 1u : 0u);
+        mma_commit(&empty[stage]);
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+      mma_commit(&tfull[acc]);
+      ++si;
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    long long it = it0;
+    Segment sg;
+    int si = 0;
+    while (next_segment(p, it, it1, sg)) {
+      const int acc = si & 1;
+      if (!mbar_wait(&tfull[acc], (si >> 1) & 1, p.status, 4)) break;
+      tc_fence_after();
+      const int wt = (int)(sg.tile / p.n_ttiles), tt = (int)(sg.tile % p.n_ttiles);
+      const int n = wt * kBM + q * 32 + lane;
+      const bool n_ok = n < p.N;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + c0, v);
+        tmem_ld_wait();
+        const int t0 = tt * BN + c0;
+        if (p.mode == kGemmAtomicAdd) {
+          if (n_ok)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (t0 + j < p.M) atomicAdd(p.out + (size_t)(t0 + j) * p.ldo + n, v[j]);
+        } else if (p.mode == kGemmStore) {
+          if (n_ok)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (t0 + j < p.M) p.out[(size_t)(t0 + j) * p.ldo + n] = v[j];
+        } else {  // kGemmArgmax: max over this warp's 32 rows, per token column
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            unsigned long long key =
+                n_ok ? (((unsigned long long)float_key(v[j]) << 32) | (uint32_t)(~(uint32_t)n)) : 0ull;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+              key = other > key ? other : key;
+            }
+            if (lane == j && t0 + j < p.M) atomicMax(p.amax + t0 + j, key);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      ++si;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+// ----------------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Encodes (and caches) a 2D bf16 tensor map: `rows` x `cols` (cols contiguous, row
+// stride `ld` elements), box = box_rows x 64 columns, 128-byte swizzle.
+int make_tmap_2d(CUtensorMap* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows) {
+  struct Key {
+    const void* p; long long r, c, ld; int b;
+    bool operator==(const Key& o) const { return p == o.p && r == o.r && c == o.c && ld == o.ld && b == o.b; }
+  };
+  struct H {
+    size_t operator()(const Key& k) const {
+      return std::hash<const void*>()(k.p) ^ (std::hash<long long>()(k.r * 1315423911ll + k.c * 2654435761ll + k.ld) << 1) ^ k.b;
+    }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, CUtensorMap, H> cache;
+  const Key key{ptr, rows, cols, ld, box_rows};
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto itc = cache.find(key);
+    if (itc != cache.end()) { *out = itc->second; return DF_OK; }
+  }
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return DF_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return DF_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache.emplace(key, m);
+  }
+  *out = m;
+  return DF_OK;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// Token tile: the smallest multiple of 16 that splits M into ceil(M/256) equal tiles.
+int gemm_token_tile(int M) {
+  const int nt = (M + 255) / 256;
+  int bn = (M + nt - 1) / nt;
+  return (bn + 15) / 16 * 16;
+}
+
+int launch_gemm(const GemmDesc& g, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0) return DF_OK;
+  if (g.K % kBK != 0 || g.K <= 0) return DF_ERR_SHAPE;
+  const int BN = gemm_token_tile(g.M);
+  CUtensorMap tw, tx;
+  int rc = make_tmap_2d(&tw, g.W, g.N, g.K, g.ldw, kBM);
+  if (rc) return rc;
+  rc = make_tmap_2d(&tx, g.X, g.M, g.K, g.ldx, BN);
+  if (rc) return rc;
+  GemmParams p{};
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.n_ttiles = (g.M + BN - 1) / BN;
+  p.BN = BN;
+  p.k_iters = g.K / kBK;
+  const long long tiles = (long long)((g.N + kBM - 1) / kBM) * p.n_ttiles;
+  p.total_iters = tiles * p.k_iters;
+  p.mode = g.mode;
+  p.whole_tiles = g.mode != kGemmAtomicAdd;
+  p.out = g.out;
+  p.ldo = g.ldo;
+  p.amax = g.amax;
+  p.status = g.status;
+  const uint32_t stage_bytes = kBM * kBK * 2 + BN * kBK * 2;
+  int stages = (int)((200 * 1024) / stage_bytes);
+  if (stages > 8) stages = 8;
+  if (stages < 2) stages = 2;
+  p.stages = stages;
+  const size_t smem = 1024 + (size_t)stages * stage_bytes + (2 * stages + 4) * 8 + 16;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  if (attr_err != cudaSuccess) return DF_ERR_CUDA;
+  long long grid = num_sms();
+  const long long work = p.whole_tiles ? tiles : p.total_iters;
+  if (grid > work) grid = work;
+  if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;
+  gemm_bf16_tc_kernel<<<(unsigned)grid, kGemmThreads, smem, st>>>(tw, tx, p);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+}  // namespace df

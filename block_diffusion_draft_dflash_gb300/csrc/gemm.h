@@ -1,0 +1,27 @@
+// Host-side description of one weight-streaming GEMM launch (see gemm.cu).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace df {
+
+enum GemmMode { kGemmAtomicAdd = 0, kGemmStore = 1, kGemmArgmax = 2 };
+
+struct GemmDesc {
+  const void* X;   // [M][K] bf16, row stride ldx elements
+  const void* W;   // [N][K] bf16, row stride ldw elements
+  int M, N, K;
+  long long ldx, ldw;
+  int mode;
+  float* out;      // kGemmAtomicAdd: out[t*ldo + n] += ...;  kGemmStore: out[t*ldo + n] = ...
+  int ldo;
+  unsigned long long* amax;  // kGemmArgmax: per-token packed (value key << 32 | ~index), max-reduced
+  int* status;
+  int max_ctas;    // 0 = one CTA per SM
+};
+
+int launch_gemm(const GemmDesc& g, cudaStream_t st);
+int make_tmap_2d(struct CUtensorMap_st* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows);
+int num_sms();
+
+}  // namespace df

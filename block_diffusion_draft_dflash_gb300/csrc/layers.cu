@@ -1,0 +1,260 @@
+// Row-wise kernels around the GEMMs of a decoder layer (all memory-bound, SIMT):
+//   embed_rows_kernel      residual stream <- token embedding rows (fp32)
+//   rmsnorm_kernel         bf16 GEMM input <- RMSNorm(fp32 residual) * gain; can also
+//                          zero the next GEMM's fp32 accumulator and capture the residual
+//                          rows as bf16 feature rows (the drafter's context features)
+//   qk_norm_rope_kernel    per-head RMSNorm of q and k, rotary embedding, q to its buffer,
+//                          k and v into their cache slots (v transposed)
+//   swiglu_kernel          bf16 act <- silu(gate) * up from the fp32 gate/up accumulator
+//   logsoftmax_rows_kernel fp32 log-softmax of each logits row, in place
+//   argmax_finalize_kernel token id from the packed argmax keys
+// Readings: Qwen3-style pre-norm layer (see the oracle); RMSNorm eps and rotary base
+// come from the model config.
+#include "common.cuh"
+#include "layers.h"
+
+namespace df {
+
+// grid: rows; block 256.  tok_mode 0: tok[r]; 1: drafter block row (bonus / mask).
+__global__ void __launch_bounds__(256) embed_rows_kernel(const df_bf16* __restrict__ E, int d, int V,
+                                                         const int32_t* __restrict__ tok, const int32_t* __restrict__ bonus,
+                                                         int L, int mask_id, float* __restrict__ h, int* status) {
+  const int r = blockIdx.x;
+  int t;
+  if (bonus) {
+    const int s = r / L, i = r % L;
+    t = i == 0 ? bonus[s] : mask_id;
+  } else {
+    t = tok[r];
+  }
+  if (t < 0 || t >= V) {
+    if (threadIdx.x == 0) set_status(status, DF_ERR_ARG, r);
+    t = 0;
+  }
+  const uint2* src = reinterpret_cast<const uint2*>(E + (size_t)t * d);  // 4 bf16
+  float4* dst = reinterpret_cast<float4*>(h + (size_t)r * d);
+  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+    const uint2 u = src[i];
+    dst[i] = make_float4(bf16_to_f(u.x & 0xFFFF), bf16_to_f(u.x >> 16), bf16_to_f(u.y & 0xFFFF), bf16_to_f(u.y >> 16));
+  }
+}
+
+// grid: out rows (+ extra blocks that only zero); block 256.  d multiple of 4.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(RmsNormArgs a) {
+  __shared__ float red[8];
+  const int o = blockIdx.x;
+  // zeroing of the next accumulator, spread over all blocks
+  if (a.zero && a.zero_count) {
+    const long long per = (a.zero_count + gridDim.x - 1) / gridDim.x;
+    const long long z0 = per * o, z1 = min(z0 + per, a.zero_count);
+    for (long long i = z0 + threadIdx.x; i < z1; i += blockDim.x) a.zero[i] = 0.f;
+  }
+  if (o >= a.rows) return;
+  const int in_row = (o / a.group_out) * a.group_in + a.in_off + (o % a.group_out);
+  const float4* x = reinterpret_cast<const float4*>(a.in + (size_t)in_row * a.d);
+  const int n4 = a.d / 4;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = x[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+  const float inv = rsqrtf(tot / a.d + a.eps);
+  const uint2* g = reinterpret_cast<const uint2*>(a.gain);
+  uint2* y = reinterpret_cast<uint2*>(a.out + (size_t)o * a.ld_out);
+  uint2* cap = a.capture ? reinterpret_cast<uint2*>(a.capture + (size_t)in_row * a.ld_capture) : nullptr;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = x[i];
+    const uint2 gw = g[i];
+    const float g0 = bf16_to_f(gw.x & 0xFFFF), g1 = bf16_to_f(gw.x >> 16), g2 = bf16_to_f(gw.y & 0xFFFF),
+                g3 = bf16_to_f(gw.y >> 16);
+    uint2 r;
+    r.x = (uint32_t)f_to_bf16(v.x * inv * g0) | ((uint32_t)f_to_bf16(v.y * inv * g1) << 16);
+    r.y = (uint32_t)f_to_bf16(v.z * inv * g2) | ((uint32_t)f_to_bf16(v.w * inv * g3) << 16);
+    y[i] = r;
+    if (cap) {
+      uint2 c;
+      c.x = (uint32_t)f_to_bf16(v.x) | ((uint32_t)f_to_bf16(v.y) << 16);
+      c.y = (uint32_t)f_to_bf16(v.z) | ((uint32_t)f_to_bf16(v.w) << 16);
+      cap[i] = c;
+    }
+  }
+}
+
+// grid: rows; block 32 * warps; warp w handles heads w, w + warps, ... over Hq + 2 Hkv heads.
+// Lane l owns elements l, l+32, l+64, l+96 of a 128-wide head, so both rotary pairs
+// (i, i+64) of the lane stay in the lane.
+__global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
+  constexpr int HD = 128;
+  const int r = blockIdx.x;
+  const int nA = a.b * a.TA;
+  int s, slot, pos;
+  bool write_q;
+  if (r < nA) {
+    s = r / a.TA;
+    const int i = r % a.TA;
+    const int base = a.base[s] + (a.nnew ? a.nnew[s] : 0);
+    slot = base + i;
+    pos = base + (a.depth ? a.depth[r] : i);
+    write_q = true;
+  } else {
+    const int rr = r - nA;
+    s = rr / a.TB;
+    const int j = rr % a.TB;
+    if (j >= a.nnew[s]) return;
+    slot = pos = a.base[s] + j;
+    write_q = false;
+  }
+  if (slot >= a.cap) {
+    if (threadIdx.x == 0) set_status(a.status, DF_ERR_CAPACITY, r);
+    return;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float* row = a.qkv + (size_t)r * a.ld_qkv;
+  // rotary angles for pairs (lane) and (lane + 32): theta^(-2i/hd), computed in fp64
+  float c0, s0, c1, s1;
+  {
+    const double lt = log2((double)a.theta);
+    const double f0 = exp2(-(2.0 * lane / HD) * lt), f1 = exp2(-(2.0 * (lane + 32) / HD) * lt);
+    const double twopi = 6.283185307179586476925286766559;
+    double a0 = fmod((double)pos * f0, twopi), a1 = fmod((double)pos * f1, twopi);
+    sincosf((float)a0, &s0, &c0);
+    sincosf((float)a1, &s1, &c1);
+  }
+  const int nh = a.Hq + 2 * a.Hkv;
+  for (int h = warp; h < nh; h += nw) {
+    if (!write_q && h < a.Hq) continue;
+    const float* x = row + h * HD;
+    float v0 = x[lane], v1 = x[lane + 32], v2 = x[lane + 64], v3 = x[lane + 96];
+    if (h < a.Hq + a.Hkv) {
+      const df_bf16* gain = h < a.Hq ? a.q_norm : a.k_norm;
+      const float ms = warp_sum(v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3) / HD;
+      const float inv = rsqrtf(ms + a.eps);
+      v0 *= inv * bf16_to_f(gain[lane]);
+      v1 *= inv * bf16_to_f(gain[lane + 32]);
+      v2 *= inv * bf16_to_f(gain[lane + 64]);
+      v3 *= inv * bf16_to_f(gain[lane + 96]);
+      // rotate-half: (x_i, x_{i+64}) -> (x_i c - x_{i+64} s, x_{i+64} c + x_i s)
+      const float r0 = v0 * c0 - v2 * s0, r2 = v2 * c0 + v0 * s0;
+      const float r1 = v1 * c1 - v3 * s1, r3 = v3 * c1 + v1 * s1;
+      v0 = r0; v1 = r1; v2 = r2; v3 = r3;
+    }
+    if (h < a.Hq) {
+      df_bf16* q = a.q_out + ((size_t)r * a.Hq + h) * HD;
+      q[lane] = f_to_bf16(v0); q[lane + 32] = f_to_bf16(v1); q[lane + 64] = f_to_bf16(v2); q[lane + 96] = f_to_bf16(v3);
+    } else if (h < a.Hq + a.Hkv) {
+      const int kh = h - a.Hq;
+      df_bf16* k = a.k_plane + (((size_t)s * a.Hkv + kh) * a.cap + slot) * HD;
+      k[lane] = f_to_bf16(v0); k[lane + 32] = f_to_bf16(v1); k[lane + 64] = f_to_bf16(v2); k[lane + 96] = f_to_bf16(v3);
+    } else {
+      const int vh = h - a.Hq - a.Hkv;
+      df_bf16* vt = a.v_plane + ((size_t)s * a.Hkv + vh) * HD * (size_t)a.cap + slot;
+      vt[(size_t)lane * a.cap] = f_to_bf16(v0);
+      vt[(size_t)(lane + 32) * a.cap] = f_to_bf16(v1);
+      vt[(size_t)(lane + 64) * a.cap] = f_to_bf16(v2);
+      vt[(size_t)(lane + 96) * a.cap] = f_to_bf16(v3);
+    }
+  }
+}
+
+// act[r][f] = silu(gu[r][f]) * gu[r][F + f]
+__global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ gu, int rows, int F,
+                                                     df_bf16* __restrict__ act) {
+  const long long n4 = (long long)rows * F / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    const long long e = i * 4;
+    const long long r = e / F;
+    const int f = (int)(e % F);
+    const float4 g = *reinterpret_cast<const float4*>(gu + r * 2 * F + f);
+    const float4 u = *reinterpret_cast<const float4*>(gu + r * 2 * F + F + f);
+    auto sl = [](float x) { return x / (1.f + __expf(-x)); };
+    uint2 o;
+    o.x = (uint32_t)f_to_bf16(sl(g.x) * u.x) | ((uint32_t)f_to_bf16(sl(g.y) * u.y) << 16);
+    o.y = (uint32_t)f_to_bf16(sl(g.z) * u.z) | ((uint32_t)f_to_bf16(sl(g.w) * u.w) << 16);
+    *reinterpret_cast<uint2*>(act + e) = o;
+  }
+}
+
+// grid: rows; block 1024.  Two passes: online max/sum, then x - (max + log(sum)).
+__global__ void __launch_bounds__(1024) logsoftmax_rows_kernel(float* __restrict__ x, int V) {
+  __shared__ float sm[32], ss[32];
+  float* row = x + (size_t)blockIdx.x * V;
+  float m = -INFINITY, s = 0.f;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float v = row[i];
+    if (v > m) { s = s * __expf(m - v) + 1.f; m = v; }
+    else s += __expf(v - m);
+  }
+  // combine (m, s) pairs: warp, then block
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mm = fmaxf(m, m2);
+    s = (m == -INFINITY ? 0.f : s * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
+    m = mm;
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) { sm[w] = m; ss[w] = s; }
+  __syncthreads();
+  float M = -INFINITY;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, sm[i]);
+  float S = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += sm[i] == -INFINITY ? 0.f : ss[i] * __expf(sm[i] - M);
+  const float lse = M + logf(S);
+  for (int i = threadIdx.x; i < V; i += blockDim.x) row[i] = row[i] - lse;
+}
+
+__global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ amax, int rows, int32_t* __restrict__ out) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < rows) out[r] = (int32_t)(~(uint32_t)(amax[r] & 0xFFFFFFFFull));
+}
+
+__global__ void add_lengths_kernel(int32_t* len, const int32_t* __restrict__ add, int b) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s < b) len[s] += add[s];
+}
+
+// ----------------------------------------------------------------------------- launchers
+int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
+                 float* h, int rows, int* status, cudaStream_t st) {
+  embed_rows_kernel<<<rows, 256, 0, st>>>(E, d, V, tok, bonus, L, mask_id, h, status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st) {
+  int grid = a.rows;
+  if (a.zero && a.zero_count && grid < 296) grid = 296;
+  rmsnorm_kernel<<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st) {
+  const int rows = a.b * (a.TA + a.TB);
+  if (rows == 0) return DF_OK;
+  qk_norm_rope_kernel<<<rows, 256, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st) {
+  const long long n4 = (long long)rows * F / 4;
+  long long grid = (n4 + 255) / 256;
+  if (grid > 4 * 152) grid = 4 * 152;
+  if (grid < 1) grid = 1;
+  swiglu_kernel<<<(unsigned)grid, 256, 0, st>>>(gu, rows, F, act);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st) {
+  logsoftmax_rows_kernel<<<rows, 1024, 0, st>>>(x, V);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st) {
+  argmax_finalize_kernel<<<(rows + 255) / 256, 256, 0, st>>>(amax, rows, out);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_add_lengths(int32_t* len, const int32_t* add, int b, cudaStream_t st) {
+  add_lengths_kernel<<<(b + 255) / 256, 256, 0, st>>>(len, add, b);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+}  // namespace df

@@ -1,0 +1,52 @@
+// Launch arguments of the row-wise layer kernels (see layers.cu).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dflash.h"
+
+namespace df {
+
+struct RmsNormArgs {
+  const float* in;        // fp32 residual rows, row stride d
+  const df_bf16* gain;    // [d]
+  df_bf16* out;           // bf16 rows, row stride ld_out
+  int ld_out;
+  int rows, d;
+  float eps;
+  // output row o reads input row (o / group_out) * group_in + in_off + o % group_out
+  int group_out, group_in, in_off;
+  float* zero;            // optional buffer to clear (next GEMM's accumulator)
+  long long zero_count;
+  df_bf16* capture;       // optional: bf16 copy of the input rows (row stride ld_capture)
+  int ld_capture;
+};
+
+struct QkRopeArgs {
+  const float* qkv;       // [rows][ld_qkv] fp32: q heads, k heads, v heads (hd 128)
+  int ld_qkv;
+  int b, TA, TB;          // rows: b*TA "query" rows, then b*TB context rows
+  const int32_t* base;    // [b] first slot (cache length before the step)
+  const int32_t* nnew;    // [b] context rows per sequence (TB rows) and offset of TA rows; may be null
+  const int32_t* depth;   // [b][TA] position offsets of TA rows; null = row index
+  int Hq, Hkv;
+  const df_bf16* q_norm;
+  const df_bf16* k_norm;
+  float eps, theta;
+  df_bf16* q_out;         // [b*TA][Hq][128]
+  df_bf16* k_plane;       // [b][Hkv][cap][128]
+  df_bf16* v_plane;       // [b][Hkv][128][cap]
+  int cap;
+  int* status;
+};
+
+int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
+                 float* h, int rows, int* status, cudaStream_t st);
+int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st);
+int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st);
+int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st);
+int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st);
+int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st);
+int launch_add_lengths(int32_t* len, const int32_t* add, int b, cudaStream_t st);
+
+}  // namespace df

@@ -1,0 +1,96 @@
+"""ddtree_build (top-K + best-first heap + ancestor bitsets) vs the oracle: bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from block_diffusion_draft_dflash_gb300 import _lib
+from oracle import ddtree
+
+from gpu_util import gpu_ddtree
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_same(g, lp, B, root=None):
+    b = lp.shape[0]
+    for s in range(b):
+        o = ddtree.build_tree(lp[s], B)
+        tok = g["tok"][s]
+        assert tok[0] == (-1 if root is None else root[s])
+        np.testing.assert_array_equal(tok[1:], o["tok"][1:], err_msg=f"tok seq {s}")
+        np.testing.assert_array_equal(g["parent"][s], o["parent"], err_msg=f"parent seq {s}")
+        np.testing.assert_array_equal(g["depth"][s], o["depth"], err_msg=f"depth seq {s}")
+        np.testing.assert_array_equal(g["score"][s].view(np.uint32), o["score"].view(np.uint32))
+        np.testing.assert_array_equal(g["anc"][s], ddtree.ancestor_mask(o["parent"]))
+
+
+@pytest.mark.parametrize("V,D", [(2, 3), (3, 3), (5, 2), (6, 4), (7, 1)])
+@pytest.mark.parametrize("mode", ["plain", "ties", "neginf"])
+def test_tiny_vocab_bit_exact(V, D, mode):
+    g = np.random.default_rng(V * 100 + D)
+    x = g.normal(0, 2, size=(3, D, V))
+    if mode == "ties":
+        x = np.round(x)
+    lp = ddtree.log_softmax(x)
+    if mode == "neginf":
+        lp[g.random(lp.shape) < 0.25] = -np.inf
+    total = ddtree.n_prefixes(V, D)
+    for B in sorted({0, 1, 2, 5, min(17, total), total}):
+        out, st = gpu_ddtree(lp, B, root=[3, 4, 5])
+        assert st == 0
+        _check_same(out, lp, B, root=[3, 4, 5])
+        # the brute-force enumeration agrees too (independent of the heap)
+        for s in range(3):
+            bf = ddtree.brute_force_tree(lp[s], B)
+            np.testing.assert_array_equal(out["parent"][s], bf["parent"])
+
+
+@pytest.mark.parametrize("B", [16, 64, 256, 512, 1024])
+def test_config_shape_budget_sweep(B):
+    # DDTree build in isolation: block 16 (15 draft depths), vocab 151936, N(0, 3^2) logits
+    # plus a +8 spike per position; 4 sequences per budget here, the full batch below.
+    lp = ddtree.log_softmax(synth.ddtree_logits(1002, 4, 15, 151936))
+    out, st = gpu_ddtree(lp, B)
+    assert st == 0
+    _check_same(out, lp, B)
+
+
+def test_config_full_batch_b64():
+    lp = ddtree.log_softmax(synth.ddtree_logits(1002, 64, 15, 151936))
+    out, st = gpu_ddtree(lp, 256)
+    assert st == 0
+    _check_same(out, lp, 256)
+
+
+def test_ragged_vocab_and_equal_rows():
+    # V not a multiple of 4 (scalar path), and rows of all-equal log-probs (every key ties)
+    lp = ddtree.log_softmax(np.random.default_rng(1).normal(0, 1, size=(2, 5, 1001)))
+    lp[1, 2, :] = np.float32(-np.log(1001.0))
+    out, st = gpu_ddtree(lp, 300)
+    assert st == 0
+    _check_same(out, lp, 300)
+
+
+@pytest.mark.parametrize("D,B", [(15, 2048), (31, 64)])
+def test_max_budget_and_depth(D, B):
+    lp = ddtree.log_softmax(np.random.default_rng(2).normal(0, 1, size=(1, D, 4096)))
+    out, st = gpu_ddtree(lp, B)
+    assert st == 0
+    _check_same(out, lp, B)
+
+
+def test_nan_is_reported():
+    lp = ddtree.log_softmax(np.random.default_rng(3).normal(size=(2, 3, 500)))
+    lp[1, 1, 17] = np.nan
+    _, st = gpu_ddtree(lp, 10)
+    assert st == -6
+
+
+def test_budget_over_prefix_count_rejected():
+    lp = torch.zeros(1, 2, 3, device="cuda")
+    with pytest.raises(_lib.StatusError) as e:
+        _lib.ddtree_build(lp, 13, {k: torch.zeros(1, 14, dtype=torch.int32, device="cuda")
+                                   for k in ("tok", "parent", "depth", "anc")} |
+                          {"score": torch.zeros(1, 14, device="cuda")}, _lib.Workspace(4096))
+    assert e.value.code == -1

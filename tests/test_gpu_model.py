@@ -1,0 +1,157 @@
+"""dflash_target_tree_forward and dflash_draft_block vs the oracle, and the whole
+speculative loop on the GPU against the target's own greedy decoding."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from block_diffusion_draft_dflash_gb300 import _lib, engine
+from oracle import ddtree, model, step
+
+from gpu_util import bf16_dev, cache_to_oracle, rel_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+TS, DS = synth.SMALL_TARGET, synth.SMALL_DRAFTER
+
+
+@pytest.fixture(scope="module")
+def models():
+    tw = synth.target_weights(TS, 2001)
+    dw = synth.drafter_weights(DS, tw, TS.n_feat, 2001)
+    tm = engine.DeviceModel.from_host(tw)
+    dm = engine.DeviceModel.from_host(dw, embed=tm.embed, n_feat=TS.n_feat)
+    return tw, dw, tm, dm
+
+
+def _clear_choice(gpu_choice, o_choice, o_logits, frac=0.02):
+    """Greedy choices must match wherever the oracle's top-2 margin is clear of bf16 noise."""
+    top2 = np.sort(o_logits, axis=-1)[:, -2:]
+    clear = (top2[:, 1] - top2[:, 0]) > frac * np.abs(o_logits).max()
+    np.testing.assert_array_equal(gpu_choice[clear], o_choice[clear])
+    assert clear.mean() > 0.7
+    # where it is not clear, the GPU's choice is still (nearly) a maximum under the oracle
+    sel = o_logits[np.arange(len(gpu_choice)), gpu_choice]
+    assert np.all(o_logits.max(-1) - sel <= frac * np.abs(o_logits).max())
+
+
+@pytest.mark.parametrize("b,B,Ns", [(2, 20, [37, 150]), (1, 64, [300]), (3, 0, [5, 0, 77])])
+def test_target_tree_forward_matches_oracle(models, b, B, Ns):
+    tw, _, tm, _ = models
+    T, cap = B + 1, 512
+    rng = np.random.default_rng(B)
+    kc = synth.normal(B, "tk", (TS.n_layers, b, TS.n_kv_heads, cap, 128))
+    vc = synth.normal(B, "tv", (TS.n_layers, b, TS.n_kv_heads, cap, 128))
+    trees = []
+    for s in range(b):
+        kc[:, s, :, Ns[s]:] = 0
+        vc[:, s, :, Ns[s]:] = 0
+        t = ddtree.build_tree(ddtree.log_softmax(rng.normal(0, 2, size=(7, TS.vocab))), B)
+        t["tok"][0] = int(rng.integers(0, TS.vocab))
+        trees.append(t)
+    k = bf16_dev(kc)
+    v = bf16_dev(vc).transpose(-1, -2).contiguous()
+    st = lambda key: torch.from_numpy(np.stack([t[key] for t in trees]).astype(np.int32)).cuda()
+    anc = torch.from_numpy(np.stack([ddtree.ancestor_mask(t["parent"]) for t in trees]).view(np.int32)).cuda()
+    clen = torch.tensor(Ns, dtype=torch.int32, device="cuda")
+    choice = torch.zeros(b, T, dtype=torch.int32, device="cuda")
+    feat = torch.zeros(b, T, TS.n_feat * TS.d_model, dtype=torch.bfloat16, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T))
+    _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k, v, clen, choice, feat, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert clen.cpu().tolist() == Ns  # not modified
+    for s in range(b):
+        cache = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), s)
+        och, ofeat, ologits = step.target_tree_forward(tw, trees[s]["tok"], trees[s]["parent"], trees[s]["depth"],
+                                                       cache, Ns[s])
+        rel_close(to_np(feat[s]), ofeat)
+        _clear_choice(choice[s].cpu().numpy(), och, ologits)
+        # tree K/V written to slots N .. N+T-1 of every layer (V transposed)
+        gk = to_np(k[:, s, :, Ns[s]:Ns[s] + T])          # [L][Hkv][T][hd]
+        gv = to_np(v[:, s, :, :, Ns[s]:Ns[s] + T])       # [L][Hkv][hd][T]
+        for l in range(TS.n_layers):
+            rel_close(gk[l], cache.k[l][Ns[s]:Ns[s] + T].transpose(1, 0, 2))
+            rel_close(gv[l], cache.v[l][Ns[s]:Ns[s] + T].transpose(1, 2, 0))
+
+
+@pytest.mark.parametrize("b,ctx0,n_new", [(2, [0, 40], [5, 8]), (1, [123], [1]), (2, [9, 0], [0, 3])])
+def test_draft_block_matches_oracle(models, b, ctx0, n_new):
+    _, dw, _, dm = models
+    cap, max_new, L = 256, 8, DS.block_size
+    feat = synth.normal(31, "df", (b, max_new, TS.n_feat * TS.d_model))
+    kc = synth.normal(31, "dk", (DS.n_layers, b, DS.n_kv_heads, cap, 128))
+    vc = synth.normal(31, "dv", (DS.n_layers, b, DS.n_kv_heads, cap, 128))
+    for s in range(b):
+        kc[:, s, :, ctx0[s]:] = 0
+        vc[:, s, :, ctx0[s]:] = 0
+    bonus = [17 + 5 * s for s in range(b)]
+    k = bf16_dev(kc)
+    v = bf16_dev(vc).transpose(-1, -2).contiguous()
+    ctx_len = torch.tensor(ctx0, dtype=torch.int32, device="cuda")
+    lp = torch.zeros(b, L - 1, DS.vocab, dtype=torch.float32, device="cuda")
+    ws = _lib.Workspace(_lib.draft_block_workspace_size(dm.cfg, b, max_new))
+    _lib.draft_block(dm.cfg, dm.weights, bf16_dev(feat), torch.tensor(n_new, dtype=torch.int32, device="cuda"),
+                     k, v, ctx_len, torch.tensor(bonus, dtype=torch.int32, device="cuda"), lp, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert ctx_len.cpu().tolist() == [c + n for c, n in zip(ctx0, n_new)]
+    g_lp = lp.cpu().numpy()
+    for s in range(b):
+        ctx = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), s)
+        olp, n1, ologits = step.draft_block(dw, feat[s, :n_new[s]].astype(np.float64), ctx, ctx0[s], bonus[s])
+        assert n1 == ctx0[s] + n_new[s]
+        rel_close(g_lp[s], olp)
+        np.testing.assert_allclose(np.exp(g_lp[s].astype(np.float64)).sum(-1), 1.0, atol=1e-3)
+        # injected context rows
+        gk = to_np(k[:, s, :, ctx0[s]:n1])
+        gv = to_np(v[:, s, :, :, ctx0[s]:n1])
+        for l in range(DS.n_layers):
+            if n_new[s]:
+                rel_close(gk[l], ctx.k[l][ctx0[s]:n1].transpose(1, 0, 2))
+                rel_close(gv[l], ctx.v[l][ctx0[s]:n1].transpose(1, 2, 0))
+
+
+def test_speculative_loop_is_lossless(models):
+    """Spec output equals the target's greedy choice at every position whose margin is clear."""
+    tw, dw, tm, dm = models
+    b, P, B, n_gen, cap = 2, 40, 16, 48, 512
+    prompt = synth.uniform_ints(2001, "prompt", (b, P), 0, TS.vocab)
+    ref = [step.greedy_generate(tw, prompt[s], n_gen + 16, cap) for s in range(b)]
+    dec = engine.SpecDecoder(tm, dm, b, B, cap, prompt_len=P)
+    dec.prefill(torch.from_numpy(prompt).cuda())
+    outs = [[int(x)] for x in dec.bonus.cpu().tolist()]
+    rng = np.random.default_rng(5)
+
+    def plant(d):
+        # harness: bias the drafter's log-probs towards the oracle's greedy continuation
+        lp = d.logprobs
+        for s in range(b):
+            k = len(outs[s])
+            for j in range(d.D):
+                if k + j < len(ref[s]) and rng.random() < 0.8:
+                    lp[s, j, ref[s][k + j]] += 12.0
+    dec.plant = plant
+    n_acc_total = 0
+    while min(len(o) for o in outs) < n_gen:
+        dec.step()
+        torch.cuda.synchronize()
+        assert dec.status() == 0
+        acc = dec.acc["acc_tok"].cpu().numpy()
+        na = dec.acc["n_acc"].cpu().numpy()
+        n_acc_total += int(na.sum())
+        for s in range(b):
+            outs[s].extend(int(t) for t in acc[s, :na[s] + 1])
+    assert n_acc_total > n_gen // 2, n_acc_total
+    # teacher-forced oracle pass over prompt + spec output: margins and greedy choices
+    for s in range(b):
+        seq = list(prompt[s]) + outs[s][:n_gen]
+        cache = step.KVCache.empty(tw.shape, len(seq) + 8)
+        T = len(seq)
+        och, _, ologits = step.target_tree_forward(tw, seq, np.arange(-1, T - 1), np.arange(T), cache, 0)
+        pred = och[P - 1:T - 1]           # oracle's choice for each generated position
+        got = np.array(outs[s][:n_gen])
+        top2 = np.sort(ologits[P - 1:T - 1], axis=-1)[:, -2:]
+        clear = (top2[:, 1] - top2[:, 0]) > 0.02 * np.abs(ologits).max()
+        bad = np.nonzero(clear & (pred != got))[0]
+        assert len(bad) == 0, (s, bad, pred[bad], got[bad])
