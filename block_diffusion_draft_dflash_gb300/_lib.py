@@ -49,6 +49,7 @@ _SIGS = {
     "ddtree_build_workspace_size": (C.c_size_t, [C.c_int] * 4),
     "ddtree_build": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int] + [C.c_void_p] * 7 +
                      [C.c_size_t, C.c_void_p]),
+    "ddtree_build_static": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int] + [C.c_void_p] * 7),
     "tree_verify_attention_workspace_size": (C.c_size_t, [C.c_int] * 6),
     "tree_verify_attention": (C.c_int, [C.c_int] * 5 + [C.c_void_p] * 3 + [C.c_int, C.c_void_p, C.c_void_p,
                               C.c_float, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -148,6 +149,15 @@ def ddtree_build(logprobs, B, out, ws: Workspace, root_tok=None):
     _check("ddtree_build", load().ddtree_build(
         _p(logprobs), b, D, V, B, _p(root_tok), _p(out["tok"]), _p(out["parent"]), _p(out["depth"]),
         _p(out["score"]), _p(out["anc"]), ws.ptr, ws.nbytes, _stream()))
+
+
+def ddtree_build_static(logprobs, B, out, root_tok=None):
+    """ddtree_build without a workspace (the library's fixed device scratch; see dflash.h)."""
+    b, D, V = logprobs.shape
+    _dev(logprobs, torch.float32, "logprobs")
+    _check("ddtree_build_static", load().ddtree_build_static(
+        _p(logprobs), b, D, V, B, _p(root_tok), _p(out["tok"]), _p(out["parent"]), _p(out["depth"]),
+        _p(out["score"]), _p(out["anc"]), _stream()))
 
 
 def tree_verify_attention_workspace_size(b, n_tree, Hq, Hkv, hd, cap):

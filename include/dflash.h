@@ -156,6 +156,31 @@ int ddtree_build(const float* logprobs, int b, int D, int V, int B, const int32_
                  void* ws, size_t ws_bytes, df_stream stream);
 
 /* ------------------------------------------------------------------------------------
+ * ddtree_build_static -- ddtree_build for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call: it exists for integration only.  Some
+ * callers cannot call cudaMalloc or hand over a workspace, e.g. a host framework that
+ * owns every device allocation and exposes none to plug-ins, a serving loop that may not
+ * allocate while a CUDA graph is being captured, or a runtime whose memory pool is fixed
+ * at start-up.  This variant takes the same inputs and outputs as ddtree_build (same
+ * layouts, limits and results) but keeps its scratch -- the per-position top-K lists and
+ * a status word -- in a fixed array inside the library's device image (about 2 MiB,
+ * present on every GPU that loads the library until the process exits).  It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *   - Size limit: b * D * min(B, V) <= 262144; larger calls return DF_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call shares the one array, so calls that may overlap on the GPU (other
+ *     streams, other host threads) race: serialise them.  Each call clears the status
+ *     word first; the top-K lists are fully rewritten before they are read.
+ *   - Device-side errors cannot be handed back (there is no workspace to read): when a
+ *     log-probability is NaN the outputs of that call are left unwritten.
+ * ------------------------------------------------------------------------------------ */
+int ddtree_build_static(const float* logprobs, int b, int D, int V, int B, const int32_t* root_tok,
+                        int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* anc,
+                        df_stream stream);
+
+/* ------------------------------------------------------------------------------------
  * tree_verify_attention -- ancestor-only attention of flattened tree rows (DDTree).
  *
  * [DDTree] "방법론 자세히 보기": the flattened tree goes through the target in one pass;
