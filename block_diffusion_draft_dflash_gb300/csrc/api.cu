@@ -12,8 +12,9 @@
 namespace df {
 int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
                   int32_t* parent, int32_t* depth, float* score, uint32_t* anc, int32_t* topk_id, float* topk_val,
-                  int* status, cudaStream_t st);
+                  int* status, cudaStream_t st, void* chunk_scratch);
 size_t ddtree_heap_smem(int D, int K, int B);
+size_t topk_chunked_scratch_bytes(int rows);
 size_t accept_scratch_bytes(int b);
 int launch_accept(int b, int n_tree, const int32_t* choice, const int32_t* tok, const int32_t* parent,
                   df_bf16* k_cache, df_bf16* v_cache, int n_layers, int Hkv, int cap, int32_t* cache_len,
@@ -161,6 +162,8 @@ struct DraftWs {
   float* fcacc;       // [b*max_new][d]
   df_bf16* xl;        // [b*(L-1)][d]
   int32_t* len_new;   // [b]
+  float* stats;       // [b*(L-1)][4*ceil(V/128)][2] LM-head softmax partials
+  float* lse;         // [b*(L-1)]
 };
 size_t draft_ws(const df_model_cfg* c, int b, int max_new, void* base, DraftWs* out) {
   const int d = c->d_model, Hq = c->n_q_heads, Hkv = c->n_kv_heads, F = c->d_ff, L = c->block_size;
@@ -177,6 +180,8 @@ size_t draft_ws(const df_model_cfg* c, int b, int max_new, void* base, DraftWs* 
   w.fcacc = cv.take<float>((Rc ? Rc : 1) * d);
   w.xl = cv.take<df_bf16>((size_t)b * (L - 1) * d);
   w.len_new = cv.take<int32_t>(b);
+  w.stats = cv.take<float>((size_t)b * (L - 1) * 4 * ((c->vocab + 127) / 128) * 2);
+  w.lse = cv.take<float>((size_t)b * (L - 1));
   const int ns = nsplit_for(b, L, Hq, Hkv, 1 << 20);
   const size_t pb = attn_partial_bytes(b, L, Hq, ns);
   w.B.o_part = cv.take<float>(pb / 4);
@@ -248,6 +253,7 @@ size_t ddtree_build_workspace_size(int b, int D, int V, int B) {
   Carver cv(nullptr);
   cv.take<int32_t>((size_t)b * D * K);
   cv.take<float>((size_t)b * D * K);
+  cv.take<unsigned char>(topk_chunked_scratch_bytes(b * D));
   return cv.off;
 }
 
@@ -270,8 +276,9 @@ int ddtree_build(const float* logprobs, int b, int D, int V, int B, const int32_
   Carver cv(ws);
   int32_t* tid = cv.take<int32_t>((size_t)b * D * K);
   float* tval = cv.take<float>((size_t)b * D * K);
+  void* chunk = cv.take<unsigned char>(topk_chunked_scratch_bytes(b * D));
   return launch_ddtree(logprobs, b, D, V, B, root_tok, tok, parent, depth, score, anc, tid, tval, status_of(ws),
-                       (cudaStream_t)stream);
+                       (cudaStream_t)stream, chunk);
 }
 
 // ------------------------------------------------------------------------- attention
@@ -462,9 +469,10 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
   DF_TRY(launch_rmsnorm(rn, st));
   GemmDesc g{};
   g.X = W.xl; g.W = w->embed; g.M = b * (L - 1); g.N = c->vocab; g.K = d; g.ldx = d; g.ldw = d;
-  g.mode = kGemmStore; g.out = logprobs; g.ldo = c->vocab; g.status = status;
+  g.mode = kGemmStore; g.out = logprobs; g.ldo = c->vocab; g.status = status; g.stats = W.stats;
   DF_TRY(launch_gemm(g, st));
-  DF_TRY(launch_logsoftmax(logprobs, b * (L - 1), c->vocab, st));
+  DF_TRY(launch_logsoftmax_from_stats(logprobs, b * (L - 1), c->vocab, W.stats, 4 * ((c->vocab + 127) / 128), W.lse,
+                                      st));
   copy_len_kernel<<<(b + 255) / 256, 256, 0, st>>>(W.len_new, ctx_len, b);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

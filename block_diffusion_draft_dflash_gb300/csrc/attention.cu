@@ -13,11 +13,13 @@
 // Tile: 128 query rows = (128 / G) consecutive tree nodes x the G query heads that share
 // one kv head (GQA), so one K/V tile feeds all 128 rows.  Per 128-key block:
 //   S = Q K^T   (tcgen05.mma, M=128 N=128 K=128, accumulator in TMEM, double-buffered)
-//   softmax     (4 warps, one TMEM lane = one query row per thread, exp2 domain, running
-//                max / sum; the ancestor mask is applied as 32-bit words per key group)
+//   softmax     (one TMEM lane = one query row, exp2 domain, running max / sum; the
+//                ancestor mask is applied as 32-bit words per key group)
 //   O += P V    (P written bf16 to shared memory in the 128-byte-swizzled K-major layout,
 //                V stored transposed in the cache so that its tile is K-major too)
-// Warp roles: warps 0-3 softmax/epilogue, warp 4 TMA producer, warp 5 TMEM owner + MMA.
+// Warp roles: warps 0-7 softmax/epilogue (two warps per row group, one per 64-column
+// half, exchanging row maxima through shared memory), warp 8 TMA producer, warp 9 TMEM
+// owner + MMA issuer.
 // The key range of a sequence is split over CTAs (split-KV) when the grid would
 // otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
 #include "attention.h"
@@ -25,7 +27,7 @@
 
 namespace df {
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 320;  // 8 softmax warps, 1 TMA warp, 1 MMA warp
 constexpr int kKB = 128;     // keys per block
 constexpr int kKVStages = 2;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128x128 bf16 tile = 2 swizzled slabs
@@ -47,26 +49,24 @@ DF_DEV uint32_t dense_bits32(int j0, int dense_len) {
   return n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
-DF_DEV void store_p_row(unsigned char* p_smem, int r, const uint32_t* packed /*64 words = 128 bf16*/) {
-  // two 64-key slabs; row r at r*128 B; 16-byte chunk c stored at chunk (c ^ (r & 7))
-#pragma unroll
-  for (int slab = 0; slab < 2; ++slab) {
-    unsigned char* rowp = p_smem + slab * (kTileBytes / 2) + r * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t* w = packed + slab * 32 + c * 4;
-      *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
+// Named-barrier AND over the 256 softmax threads (barrier 1): every thread gets the same
+// answer, so the group leaves its loop together.
+DF_DEV bool group_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r) : "r"((uint32_t)v) : "memory");
+  return r != 0;
 }
+DF_DEV void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* q_smem = smem;                               // 32 KB
-  unsigned char* kv_smem = smem + kTileBytes;                 // stages x (K 32 KB + V 32 KB)
+  unsigned char* q_smem = smem;                                  // 32 KB
+  unsigned char* kv_smem = smem + kTileBytes;                    // stages x (K 32 KB + V 32 KB)
   unsigned char* p_smem = kv_smem + kKVStages * 2 * kTileBytes;  // 32 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(p_smem + kTileBytes);
   uint64_t* q_full = bars;
@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* p_full = s_empty + 2;
   uint64_t* o_done = p_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  __shared__ float red_max[2][2][128];  // [block parity][column half][row]
+  __shared__ float red_sum[2][128];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // work unit -> (sequence, kv head, query tile, split)
@@ -95,18 +97,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kKVStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 128); }
-    mbar_init(p_full, 128);
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 256); }
+    mbar_init(p_full, 256);
     mbar_init(o_done, 1);
     fence_barrier_init();
   }
-  if (warp == 5) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S0: cols 0-127, S1: 128-255, O: 256-383
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0 && nblk > 0) {
       // ------------------------------------------------------------ TMA producer
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int st = 0; st < kKVStages; ++st) mbar_wait(&kv_full[st], 0, nullptr, 0);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0 && nblk > 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc = idesc_bf16_f32(128, 128);
@@ -172,64 +174,80 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ok) issue_pv(nblk - 1);
     }
   } else {
-    // -------------------------------------------------------------- softmax (warps 0-3)
-    const int r = warp * 32 + lane;  // query row == TMEM lane
+    // ------------------------------------------------ softmax / epilogue (warps 0-7)
+    // Warp w owns TMEM lanes 32*(w%4)..+31 (one query row per thread) and column half
+    // w/4: S columns [64h, 64h+64) (keys) and O columns [64h, 64h+64) (head dims).
+    const int half = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // query row == TMEM lane
     const int node = qt * NPT + r / G, head = kvh * G + r % G;
     const bool row_ok = node < p.T;
+    const bool warp_live = __any_sync(0xffffffffu, row_ok);
     const uint32_t* anc_row = (p.anc && row_ok) ? p.anc + ((size_t)s * p.T + node) * p.W : nullptr;
     const float scale2 = p.scale * 1.4426950408889634f;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float m_run = -INFINITY, l_part = 0.f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
-      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.status, 16)) { ok = false; break; }
-      tc_fence_after();
-      float sv[128];
+      // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
+      const bool w1 = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.status, 16));
+      float sv[64];
+      float mpart = -INFINITY;
+      if (w1) {
+        tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 128; c += 16) tmem_ld16(tmem + lane_base + (j & 1) * 128 + c, sv + c);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&s_empty[j & 1]);
-      // admission mask for keys key0 .. key0+127
-      const int key0 = (kb0 + j) * kKB;
-      uint32_t adm[4];
+        for (int c = 0; c < 64; c += 16) tmem_ld16(tmem + lane_base + (j & 1) * 128 + half * 64 + c, sv + c);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_empty[j & 1]);
+        const int key0 = (kb0 + j) * kKB + half * 64;
+        uint32_t adm[2];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int j0 = key0 + 32 * g;
-        uint32_t bits = dense_bits32(j0, dense_len);
-        if (anc_row) bits |= anc_bits32(anc_row, p.W, j0 - dense_len);
-        else if (!row_ok) bits |= 0u;
-        // keys of the tail beyond tail_len carry no ancestor bits, keys >= Lk none at all
-        adm[g] = bits;
+        for (int g = 0; g < 2; ++g) {
+          const int j0 = key0 + 32 * g;
+          uint32_t bits = row_ok ? dense_bits32(j0, dense_len) : 0u;
+          if (anc_row) bits |= anc_bits32(anc_row, p.W, j0 - dense_len);
+          adm[g] = bits;
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const bool a = (adm[c >> 5] >> (c & 31)) & 1u;
+          sv[c] = a ? sv[c] * scale2 : -INFINITY;
+          m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+        }
+        mpart = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sv[c] = -INFINITY;
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const bool a = (adm[c >> 5] >> (c & 31)) & 1u;
-        sv[c] = a ? sv[c] * scale2 : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
-      }
+      red_max[j & 1][half][r] = mpart;
+      if (!group_and(w1 && ok)) { ok = false; break; }  // uniform across the 256 threads
+      const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);
       const float m_new = fmaxf(m_run, mx);
       const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-      uint32_t packed[64];
-      float psum = 0.f;
+      uint32_t packed[32];
+      if (warp_live && m_new != -INFINITY) {
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float p0 = (m_new == -INFINITY) ? 0.f : exp2f(sv[c] - m_new);
-        const float p1 = (m_new == -INFINITY) ? 0.f : exp2f(sv[c + 1] - m_new);
-        psum += p0 + p1;
-        packed[c >> 1] = (uint32_t)f_to_bf16(p0) | ((uint32_t)f_to_bf16(p1) << 16);
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = exp2f(sv[c] - m_new), p1 = exp2f(sv[c + 1] - m_new);
+          s4[(c >> 1) & 3] += p0 + p1;
+          packed[c >> 1] = (uint32_t)f_to_bf16(p0) | ((uint32_t)f_to_bf16(p1) << 16);
+        }
+        l_part = l_part * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) packed[c] = 0u;
       }
-      l_run = l_run * alpha + psum;
       m_run = m_new;
       if (j >= 1) {
         // PV of the previous block must be complete before P is overwritten / O rescaled
-        if (!mbar_wait(o_done, (j - 1) & 1, p.status, 17)) { ok = false; break; }
+        ok = mbar_wait(o_done, (j - 1) & 1, p.status, 17) && ok;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t oaddr = tmem + lane_base + 256;
+          const uint32_t oaddr = tmem + lane_base + 256 + half * 64;
 #pragma unroll
-          for (int c = 0; c < 128; c += 16) {
+          for (int c = 0; c < 64; c += 16) {
             float o[16];
             tmem_ld16(oaddr + c, o);
             tmem_ld_wait();
@@ -240,7 +258,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_st_wait();
         }
       }
-      store_p_row(p_smem, r, packed);
+      // this half's 64 keys = one 64-key slab of the P tile; row r at r*128 B, 16-byte
+      // chunk c stored at chunk (c ^ (r & 7)) (128-byte swizzle)
+      unsigned char* rowp = p_smem + half * (kTileBytes / 2) + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) =
+            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -248,41 +272,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ---------------------------------------------------------------- epilogue
     if (ok && nblk > 0) ok = mbar_wait(o_done, (nblk - 1) & 1, p.status, 18);
     tc_fence_after();
+    red_sum[half][r] = l_part;
+    group_sync();
+    const float l_run = red_sum[0][r] + red_sum[1][r];
     const size_t grow = ((size_t)s * p.T + node) * p.Hq + head;  // global query row
+    const uint32_t oaddr = tmem + lane_base + 256 + half * 64;
     if (p.nsplit == 1) {
-      if (row_ok) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + grow * 128);
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + grow * 128 + half * 64);
 #pragma unroll
-        for (int c = 0; c < 128; c += 16) {
-          float o[16];
-          if (nblk > 0) { tmem_ld16(tmem + lane_base + 256 + c, o); tmem_ld_wait(); }
-          else { for (int i = 0; i < 16; ++i) o[i] = 0.f; }
-          uint32_t w[8];
+      for (int c = 0; c < 64; c += 16) {
+        float o[16];
+        if (nblk > 0) { tmem_ld16(oaddr + c, o); tmem_ld_wait(); }
+        else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            w[i] = (uint32_t)f_to_bf16(o[2 * i] * inv) | ((uint32_t)f_to_bf16(o[2 * i + 1] * inv) << 16);
+          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        }
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = (uint32_t)f_to_bf16(o[2 * i] * inv) | ((uint32_t)f_to_bf16(o[2 * i + 1] * inv) << 16);
+        if (row_ok) {
           dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
           dst[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
-      } else if (nblk > 0) {
-        float o[16];
-        for (int c = 0; c < 128; c += 16) { tmem_ld16(tmem + lane_base + 256 + c, o); tmem_ld_wait(); }
       }
     } else {
       const size_t nrows = (size_t)p.b * p.T * p.Hq;
-      float* op = p.o_part + ((size_t)split * nrows + grow) * 128;
+      float* op = p.o_part + ((size_t)split * nrows + grow) * 128 + half * 64;
 #pragma unroll
-      for (int c = 0; c < 128; c += 16) {
+      for (int c = 0; c < 64; c += 16) {
         float o[16];
-        if (nblk > 0) { tmem_ld16(tmem + lane_base + 256 + c, o); tmem_ld_wait(); }
-        else { for (int i = 0; i < 16; ++i) o[i] = 0.f; }
+        if (nblk > 0) { tmem_ld16(oaddr + c, o); tmem_ld_wait(); }
+        else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        }
         if (row_ok)
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
             *reinterpret_cast<float4*>(op + c + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
       }
-      if (row_ok) {
+      if (row_ok && half == 0) {
         p.ml_part[((size_t)split * nrows + grow) * 2] = m_run;
         p.ml_part[((size_t)split * nrows + grow) * 2 + 1] = l_run;
       }
@@ -291,7 +322,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
@@ -349,7 +380,8 @@ int attn_num_splits(int b, int Hkv, int n_qtiles, int max_keys) {
   const int units = b * Hkv * n_qtiles;
   const int nsm = num_sms_attn();
   const int nb = (max_keys + kKB - 1) / kKB;
-  int ns = (nsm + units - 1) / units;
+  // fill one wave: as many splits as whole copies of the unit set fit on the SMs
+  int ns = units >= nsm ? 1 : nsm / units;
   if (ns > nb) ns = nb;
   if (ns > kAttnMaxSplits) ns = kAttnMaxSplits;
   if (ns < 1) ns = 1;

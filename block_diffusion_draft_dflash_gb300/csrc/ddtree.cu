@@ -57,16 +57,16 @@ DF_DEV uint32_t block_scan_incl(uint32_t v, uint32_t* warp_tmp) {
   return v + off;
 }
 
+// Whole-row radix top-K by one CTA of 1024 threads (also the fallback of the chunked
+// path when the threshold bin holds too many candidates, e.g. rows of equal values).
 template <bool kVec4>
-__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __restrict__ lp, int V, int K,
-                                                                 int32_t* __restrict__ out_id,
-                                                                 float* __restrict__ out_val, int* status) {
+DF_DEV void topk_row_full(const float* __restrict__ lp, size_t row, int V, int K, int32_t* __restrict__ out_id,
+                          float* __restrict__ out_val, int* status) {
   __shared__ uint32_t hist[4096];
   __shared__ uint32_t warp_tmp[32];
   __shared__ unsigned long long sel[kMaxK];
   __shared__ uint32_t sh_bin, sh_above, sh_ngt, sh_eq_base, sh_nan;
   const int tid = threadIdx.x;
-  const size_t row = blockIdx.x;
   const float* x = lp + row * (size_t)V;
   if (tid == 0) { sh_nan = 0; sh_ngt = 0; sh_eq_base = 0; }
 
@@ -198,6 +198,171 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
   }
 }
 
+template <bool kVec4>
+__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __restrict__ lp, int V, int K,
+                                                                 int32_t* __restrict__ out_id,
+                                                                 float* __restrict__ out_val, int* status) {
+  topk_row_full<kVec4>(lp, blockIdx.x, V, K, out_id, out_val, status);
+}
+
+// ----------------------------------------------------------------------------- chunked top-K
+// Pass A: per (chunk, row) CTA, histogram of the top 12 key bits into hist[row][4096].
+// Pass B: per (chunk, row) CTA, threshold bin t from hist (the bin holding the K-th
+//         largest key); keys in bins above t go to hi[row] (all of them are selected),
+//         keys in bin t to eq[row] (candidates), with per-row counters.
+// Pass C: per row, the K - |hi| best candidates of eq by (key desc, id asc) join hi and
+//         the K winners are sorted.  If eq overflowed, the row is redone by topk_row_full.
+constexpr int kChunk = 8192;
+constexpr int kCapEq = 4096;
+constexpr int kChunkThreads = 512;
+
+struct TopkScratch {     // per row
+  uint32_t cnt_hi, cnt_eq, thr_bin, above;
+};
+
+__global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const float* __restrict__ lp, int V,
+                                                                  uint32_t* __restrict__ ghist, int* status) {
+  __shared__ uint32_t hist[4096];
+  __shared__ uint32_t sh_nan;
+  const size_t row = blockIdx.y;
+  const float* x = lp + row * (size_t)V;
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x) hist[i] = 0;
+  if (threadIdx.x == 0) sh_nan = 0;
+  __syncthreads();
+  const int i0 = blockIdx.x * kChunk, i1 = min(V, i0 + kChunk);
+  for (int base = i0; base < i1; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const bool ok = i < i1;
+    const float f = ok ? __ldg(x + i) : 0.f;
+    const bool nan = ok && isnan(f);
+    if (nan) sh_nan = 1;
+    hist_add(hist, float_key(f) >> 20, ok && !nan);
+  }
+  __syncthreads();
+  if (sh_nan && threadIdx.x == 0) set_status(status, DF_ERR_NAN, (int)row);
+  uint32_t* g = ghist + row * 4096;
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x)
+    if (hist[i]) atomicAdd(g + i, hist[i]);
+}
+
+__global__ void __launch_bounds__(kChunkThreads) topk_collect_kernel(const float* __restrict__ lp, int V, int K,
+                                                                     const uint32_t* __restrict__ ghist,
+                                                                     TopkScratch* __restrict__ sc,
+                                                                     unsigned long long* __restrict__ hi,
+                                                                     unsigned long long* __restrict__ eq) {
+  __shared__ uint32_t warp_tmp[32];
+  __shared__ uint32_t sh_bin, sh_above;
+  const size_t row = blockIdx.y;
+  const uint32_t* h = ghist + row * 4096;
+  // descending bins, 8 per thread (512 threads x 8 = 4096)
+  uint32_t local = 0;
+  for (int j = 0; j < 8; ++j) local += h[4095 - (threadIdx.x * 8 + j)];
+  // inclusive scan over 512 threads
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t v = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_tmp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < (kChunkThreads >> 5) ? warp_tmp[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < (kChunkThreads >> 5)) warp_tmp[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t incl = v + (warp ? warp_tmp[warp - 1] : 0u);
+  const uint32_t excl = incl - local;
+  if (excl < (uint32_t)K && (uint32_t)K <= incl) {
+    uint32_t acc = excl;
+    for (int j = 0; j < 8; ++j) {
+      const int bin = 4095 - (threadIdx.x * 8 + j);
+      if (acc + h[bin] >= (uint32_t)K) { sh_bin = bin; sh_above = acc; break; }
+      acc += h[bin];
+    }
+  }
+  __syncthreads();
+  const uint32_t tb = sh_bin;
+  if (blockIdx.x == 0 && threadIdx.x == 0) { sc[row].thr_bin = tb; sc[row].above = sh_above; }
+  const float* x = lp + row * (size_t)V;
+  const int i0 = blockIdx.x * kChunk, i1 = min(V, i0 + kChunk);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    const uint32_t k = float_key(__ldg(x + i));
+    const uint32_t d = k >> 20;
+    if (d < tb) continue;
+    const unsigned long long c = ((unsigned long long)k << 32) | (uint32_t)(~(uint32_t)i);
+    if (d > tb) {
+      const uint32_t pos = atomicAdd(&sc[row].cnt_hi, 1u);
+      if (pos < (uint32_t)kMaxK) hi[row * kMaxK + pos] = c;
+    } else {
+      const uint32_t pos = atomicAdd(&sc[row].cnt_eq, 1u);
+      if (pos < (uint32_t)kCapEq) eq[row * kCapEq + pos] = c;
+    }
+  }
+}
+
+DF_DEV void bitonic_desc(unsigned long long* a, int n) {  // n power of two, block-wide
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const unsigned long long x = a[i], y = a[j];
+          const bool desc = (i & size) == 0;
+          if (desc ? (x < y) : (x > y)) { a[i] = y; a[j] = x; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <bool kVec4>
+__global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(const float* __restrict__ lp, int V, int K,
+                                                                  const TopkScratch* __restrict__ sc,
+                                                                  const unsigned long long* __restrict__ hi,
+                                                                  const unsigned long long* __restrict__ eq,
+                                                                  int32_t* __restrict__ out_id,
+                                                                  float* __restrict__ out_val, int* status) {
+  extern __shared__ unsigned long long cand[];  // [kCapEq] then [kMaxK]
+  const size_t row = blockIdx.x;
+  if (status && *(volatile int*)status == DF_ERR_NAN) return;
+  const uint32_t n_eq = sc[row].cnt_eq, n_hi = sc[row].above;
+  if (n_eq > (uint32_t)kCapEq) {  // threshold bin too crowded: whole-row path
+    topk_row_full<kVec4>(lp, row, V, K, out_id, out_val, status);
+    return;
+  }
+  unsigned long long* e = cand;
+  unsigned long long* w = cand + kCapEq;
+  int n = 1;
+  while (n < (int)n_eq) n <<= 1;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) e[i] = i < (int)n_eq ? eq[row * kCapEq + i] : 0ull;
+  int nk = 1;
+  while (nk < K) nk <<= 1;
+  for (int i = threadIdx.x; i < nk; i += blockDim.x) w[i] = i < (int)n_hi ? hi[row * kMaxK + i] : 0ull;
+  __syncthreads();
+  bitonic_desc(e, n);
+  const int need = K - (int)n_hi;
+  for (int i = threadIdx.x; i < need; i += blockDim.x) w[n_hi + i] = e[i];
+  __syncthreads();
+  bitonic_desc(w, nk);
+  for (int r = threadIdx.x; r < K; r += blockDim.x) {
+    const unsigned long long c = w[r];
+    out_id[row * K + r] = (int32_t)(~(uint32_t)(c & 0xFFFFFFFFull));
+    out_val[row * K + r] = key_float((uint32_t)(c >> 32));
+  }
+}
+
+size_t topk_chunked_scratch_bytes(int rows) {
+  return (size_t)rows * (4096 * 4 + sizeof(TopkScratch) + kMaxK * 8 + kCapEq * 8) + 1024;
+}
+
 // ----------------------------------------------------------------------------- heap
 // 64-bit heap key, larger = earlier in the tree's total order:
 //   [63:32] float_key(score)  [31:27] 31-depth  [26:16] 2047-parent  [15:5] 2047-rank
@@ -303,16 +468,46 @@ size_t ddtree_heap_smem(int D, int K, int B) {
   return (size_t)((D * K + 1) & ~1) * 4 + (size_t)(B + 2) * 8 + (size_t)n * 16;
 }
 
+__global__ void zero_u32_kernel(uint32_t* p, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = 0;
+}
+
 int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
                   int32_t* parent, int32_t* depth, float* score, uint32_t* anc, int32_t* topk_id,
-                  float* topk_val, int* status, cudaStream_t st) {
+                  float* topk_val, int* status, cudaStream_t st, void* chunk_scratch) {
   const int K = B < V ? B : V;
   if (B > 0) {
     const int rows = b * D;
-    if ((V & 3) == 0)
+    if (chunk_scratch) {
+      // chunked path: histogram, collect, final select (falls back per row when needed)
+      unsigned char* base = static_cast<unsigned char*>(chunk_scratch);
+      uint32_t* ghist = reinterpret_cast<uint32_t*>(base);
+      TopkScratch* sc = reinterpret_cast<TopkScratch*>(ghist + (size_t)rows * 4096);
+      unsigned long long* hi = reinterpret_cast<unsigned long long*>(
+          (reinterpret_cast<uintptr_t>(sc + rows) + 255) & ~uintptr_t(255));
+      unsigned long long* eq = hi + (size_t)rows * kMaxK;
+      const size_t nzero = (size_t)rows * 4096 + (size_t)rows * (sizeof(TopkScratch) / 4);
+      zero_u32_kernel<<<(unsigned)((nzero + 1023) / 1024 < 1024 ? (nzero + 1023) / 1024 : 1024), 1024, 0, st>>>(
+          ghist, nzero);
+      const dim3 grid((V + kChunk - 1) / kChunk, rows);
+      topk_hist_kernel<<<grid, kChunkThreads, 0, st>>>(lp, V, ghist, status);
+      topk_collect_kernel<<<grid, kChunkThreads, 0, st>>>(lp, V, K, ghist, sc, hi, eq);
+      const size_t smem = (size_t)(kCapEq + kMaxK) * 8;
+      static bool attr = false;
+      if (!attr) {
+        cudaFuncSetAttribute(topk_final_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(topk_final_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
+      }
+      if ((V & 3) == 0)
+        topk_final_kernel<true><<<rows, kTopkThreads, smem, st>>>(lp, V, K, sc, hi, eq, topk_id, topk_val, status);
+      else
+        topk_final_kernel<false><<<rows, kTopkThreads, smem, st>>>(lp, V, K, sc, hi, eq, topk_id, topk_val, status);
+    } else if ((V & 3) == 0) {
       topk_rows_kernel<true><<<rows, kTopkThreads, 0, st>>>(lp, V, K, topk_id, topk_val, status);
-    else
+    } else {
       topk_rows_kernel<false><<<rows, kTopkThreads, 0, st>>>(lp, V, K, topk_id, topk_val, status);
+    }
   }
   const size_t smem = ddtree_heap_smem(D, K > 0 ? K : 1, B);
   static thread_local size_t configured = 0;

@@ -9,7 +9,7 @@
 namespace df {
 int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
                   int32_t* parent, int32_t* depth, float* score, uint32_t* anc, int32_t* topk_id, float* topk_val,
-                  int* status, cudaStream_t st);
+                  int* status, cudaStream_t st, void* chunk_scratch);
 size_t ddtree_heap_smem(int D, int K, int B);
 }  // namespace df
 
@@ -73,6 +73,7 @@ extern "C" int ddtree_build_static(const float* logprobs, int b, int D, int V, i
   if (cudaMemsetAsync(base, 0, kHeaderBytes, st) != cudaSuccess) return DF_ERR_CUDA;
   int32_t* topk_id = reinterpret_cast<int32_t*>(base + kHeaderBytes);
   float* topk_val = reinterpret_cast<float*>(base + kHeaderBytes + (size_t)kStaticTopkEntries * 4);
+  // the whole-row top-K path needs no scratch beyond the top-K lists
   return df::launch_ddtree(logprobs, b, D, V, B, root_tok, tok, parent, depth, score, anc, topk_id, topk_val,
-                           reinterpret_cast<int*>(base), st);
+                           reinterpret_cast<int*>(base), st, nullptr);
 }

@@ -33,12 +33,17 @@ constexpr int kBK = 64;   // k per stage (one 128-byte swizzle row)
 struct GemmParams {
   int M, N, K;
   int n_ttiles, BN, k_iters;
+  int sub0, sub1;   // token tile = two MMA widths (sub1 = 0 when BN <= 256)
+  int nbuf;         // TMEM accumulator buffers (2 when 2*BN fits in 512 columns)
+  int w_keep;       // 1: weights are re-read by later token tiles (keep them in L2)
   long long total_iters;
   int whole_tiles;  // 1: each CTA owns whole tiles (store / argmax epilogues)
   int mode;
   float* out;
   int ldo;
   unsigned long long* amax;  // argmax keys [M]
+  float2* stats;             // kGemmStore: optional per (token, weight tile, warp) (max, sum exp(x - max))
+  int n_stats;               // = 4 * number of weight tiles
   int* status;
   int stages;
 };
@@ -73,7 +78,7 @@ DF_DEV bool next_segment(const GemmParams& p, long long& it, long long it1, Segm
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmX1, const GemmParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int BN = p.BN, S = p.stages;
@@ -87,7 +92,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t tmem_cols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+  const int acc_cols = p.nbuf * BN;
+  const uint32_t tmem_cols = acc_cols <= 32 ? 32 : acc_cols <= 64 ? 64 : acc_cols <= 128 ? 128 : acc_cols <= 256 ? 256 : 512;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
@@ -95,6 +101,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    if (p.sub1) tma_prefetch_desc(&tmX1);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, tmem_cols); tmem_relinquish(); }
   tc_fence_before();
@@ -107,7 +114,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
-    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    const uint64_t pol_w = p.w_keep ? policy_evict_last() : policy_evict_first(), pol_x = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
     long long it = it0;
@@ -122,6 +129,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_arrive_expect_tx(&full[stage], stage_bytes);
         tma_load_2d(sb, &tmW, &full[stage], k * kBK, wt * kBM, pol_w);
         tma_load_2d(sb + w_bytes, &tmX, &full[stage], k * kBK, tt * BN, pol_x);
+        if (p.sub1) tma_load_2d(sb + w_bytes + p.sub0 * 128, &tmX1, &full[stage], k * kBK, tt * BN + p.sub0, pol_x);
         ++issued;
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
@@ -138,7 +146,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(kBM, BN);
+    const uint32_t idesc0 = idesc_bf16_f32(kBM, p.sub0);
+    const uint32_t idesc1 = idesc_bf16_f32(kBM, p.sub1 ? p.sub1 : 16);
     int stage = 0;
     uint32_t phase = 0;
     long long it = it0;
@@ -146,8 +155,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int si = 0;
     bool ok = true;
     while (ok && next_segment(p, it, it1, sg)) {
-      const int acc = si & 1;
-      if (!mbar_wait(&tempty[acc], ((si >> 1) & 1) ^ 1, p.status, 2)) break;
+      const int acc = si % p.nbuf, use = si / p.nbuf;
+      if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 2)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int k = sg.k0; k < sg.k1; ++k) {
@@ -156,9 +165,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t sa = smem_u32(smem + (size_t)stage * stage_bytes);
         const uint64_t adesc = sdesc_kmajor_sw128(sa);
         const uint64_t bdesc = sdesc_kmajor_sw128(sa + w_bytes);
+        const uint64_t bdesc1 = sdesc_kmajor_sw128(sa + w_bytes + p.sub0 * 128);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (k > sg.k0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t accum = (k > sg.k0 || kk > 0) ? 1u : 0u;
+          mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc0, accum);
+          if (p.sub1) mma_bf16(d_tmem + p.sub0, adesc + 2 * kk, bdesc1 + 2 * kk, idesc1, accum);
+        }
         mma_commit(&empty[stage]);
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
@@ -172,8 +185,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     Segment sg;
     int si = 0;
     while (next_segment(p, it, it1, sg)) {
-      const int acc = si & 1;
-      if (!mbar_wait(&tfull[acc], (si >> 1) & 1, p.status, 4)) break;
+      const int acc = si % p.nbuf, use = si / p.nbuf;
+      // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], use & 1, p.status, 4))) break;
       tc_fence_after();
       const int wt = (int)(sg.tile / p.n_ttiles), tt = (int)(sg.tile % p.n_ttiles);
       const int n = wt * kBM + q * 32 + lane;
@@ -194,6 +208,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (t0 + j < p.M) p.out[(size_t)(t0 + j) * p.ldo + n] = v[j];
+          if (p.stats) {
+            // softmax statistics of this warp's 32 output rows, per token column
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float x = n_ok ? v[j] : -INFINITY;
+              const float m = warp_max(x);
+              const float e = (m == -INFINITY) ? 0.f : warp_sum(__expf(x - m));
+              if (lane == j && t0 + j < p.M)
+                p.stats[(size_t)(t0 + j) * p.n_stats + wt * 4 + q] = make_float2(m, e);
+            }
+          }
         } else {  // kGemmArgmax: max over this warp's 32 rows, per token column
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -291,8 +316,11 @@ int num_sms() {
   return n;
 }
 
-// Token tile: the smallest multiple of 16 that splits M into ceil(M/256) equal tiles.
+// Token tile.  Up to 512 tokens form one tile (two MMAs of N <= 256 per k-step, one
+// TMEM buffer), so every weight k-chunk is streamed once; beyond that, equal tiles of at
+// most 256 (double-buffered TMEM) with the weights kept in L2 for the later tiles.
 int gemm_token_tile(int M) {
+  if (M <= 512) return (M + 15) / 16 * 16;
   const int nt = (M + 255) / 256;
   int bn = (M + nt - 1) / nt;
   return (bn + 15) / 16 * 16;
@@ -302,14 +330,24 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return DF_OK;
   if (g.K % kBK != 0 || g.K <= 0) return DF_ERR_SHAPE;
   const int BN = gemm_token_tile(g.M);
-  CUtensorMap tw, tx;
+  const int sub0 = BN < 256 ? BN : 256, sub1 = BN - sub0;
+  CUtensorMap tw, tx, tx1;
   int rc = make_tmap_2d(&tw, g.W, g.N, g.K, g.ldw, kBM);
   if (rc) return rc;
-  rc = make_tmap_2d(&tx, g.X, g.M, g.K, g.ldx, BN);
+  rc = make_tmap_2d(&tx, g.X, g.M, g.K, g.ldx, sub0);
   if (rc) return rc;
+  tx1 = tx;
+  if (sub1) {
+    rc = make_tmap_2d(&tx1, g.X, g.M, g.K, g.ldx, sub1);
+    if (rc) return rc;
+  }
   GemmParams p{};
+  p.sub0 = sub0;
+  p.sub1 = sub1;
+  p.nbuf = 2 * BN <= 512 ? 2 : 1;
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.n_ttiles = (g.M + BN - 1) / BN;
+  p.w_keep = p.n_ttiles > 1;
   p.BN = BN;
   p.k_iters = g.K / kBK;
   const long long tiles = (long long)((g.N + kBM - 1) / kBM) * p.n_ttiles;
@@ -319,6 +357,8 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   p.out = g.out;
   p.ldo = g.ldo;
   p.amax = g.amax;
+  p.stats = reinterpret_cast<float2*>(g.stats);
+  p.n_stats = 4 * ((g.N + kBM - 1) / kBM);
   p.status = g.status;
   const uint32_t stage_bytes = kBM * kBK * 2 + BN * kBK * 2;
   int stages = (int)((200 * 1024) / stage_bytes);
@@ -336,7 +376,7 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   const long long work = p.whole_tiles ? tiles : p.total_iters;
   if (grid > work) grid = work;
   if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;
-  gemm_bf16_tc_kernel<<<(unsigned)grid, kGemmThreads, smem, st>>>(tw, tx, p);
+  gemm_bf16_tc_kernel<<<(unsigned)grid, kGemmThreads, smem, st>>>(tw, tx, tx1, p);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

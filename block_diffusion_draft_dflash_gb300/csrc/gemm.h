@@ -16,6 +16,7 @@ struct GemmDesc {
   float* out;      // kGemmAtomicAdd: out[t*ldo + n] += ...;  kGemmStore: out[t*ldo + n] = ...
   int ldo;
   unsigned long long* amax;  // kGemmArgmax: per-token packed (value key << 32 | ~index), max-reduced
+  float* stats;    // kGemmStore, optional: [M][4 * ceil(N/128)] float2 (max, sum exp(x - max)) partials
   int* status;
   int max_ctas;    // 0 = one CTA per SM
 };

@@ -115,13 +115,14 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const float* row = a.qkv + (size_t)r * a.ld_qkv;
-  // rotary angles for pairs (lane) and (lane + 32): theta^(-2i/hd), computed in fp64
+  // rotary angles of pairs (lane) and (lane + 32): pos * theta^(-2i/hd), reduced mod 2 pi
+  // in fp64 so that large positions keep full fp32 accuracy in sincosf
   float c0, s0, c1, s1;
   {
-    const double lt = log2((double)a.theta);
-    const double f0 = exp2(-(2.0 * lane / HD) * lt), f1 = exp2(-(2.0 * (lane + 32) / HD) * lt);
-    const double twopi = 6.283185307179586476925286766559;
-    double a0 = fmod((double)pos * f0, twopi), a1 = fmod((double)pos * f1, twopi);
+    const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
+    double a0 = (double)pos * a.inv_freq[lane], a1 = (double)pos * a.inv_freq[lane + 32];
+    a0 -= twopi * rint(a0 * inv_twopi);
+    a1 -= twopi * rint(a1 * inv_twopi);
     sincosf((float)a0, &s0, &c0);
     sincosf((float)a1, &s1, &c1);
   }
@@ -208,6 +209,47 @@ __global__ void __launch_bounds__(1024) logsoftmax_rows_kernel(float* __restrict
   for (int i = threadIdx.x; i < V; i += blockDim.x) row[i] = row[i] - lse;
 }
 
+// lse[r] from the GEMM epilogue's (max, sum exp) partials of row r.
+__global__ void __launch_bounds__(1024) lse_from_stats_kernel(const float2* __restrict__ stats, int n_stats,
+                                                              float* __restrict__ lse) {
+  __shared__ float sm[32], ss[32];
+  const float2* st = stats + (size_t)blockIdx.x * n_stats;
+  float m = -INFINITY, s = 0.f;
+  for (int i = threadIdx.x; i < n_stats; i += blockDim.x) {
+    const float2 v = st[i];
+    if (v.x == -INFINITY) continue;
+    if (v.x > m) { s = s * __expf(m - v.x) + v.y; m = v.x; }
+    else s += v.y * __expf(v.x - m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mm = fmaxf(m, m2);
+    s = (m == -INFINITY ? 0.f : s * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
+    m = mm;
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) { sm[w] = m; ss[w] = s; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, sm[i]);
+    float S = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += sm[i] == -INFINITY ? 0.f : ss[i] * __expf(sm[i] - M);
+    lse[blockIdx.x] = M + logf(S);
+  }
+}
+
+// x[r][i] -= lse[r] over a grid of (row, chunk) blocks.
+__global__ void __launch_bounds__(256) sub_lse_kernel(float* __restrict__ x, int V, const float* __restrict__ lse) {
+  const int r = blockIdx.y;
+  const float l = lse[r];
+  float* row = x + (size_t)r * V;
+  const int chunk = (V + gridDim.x - 1) / gridDim.x;
+  const int i0 = blockIdx.x * chunk, i1 = min(V, i0 + chunk);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) row[i] -= l;
+}
+
 __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ amax, int rows, int32_t* __restrict__ out) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < rows) out[r] = (int32_t)(~(uint32_t)(amax[r] & 0xFFFFFFFFull));
@@ -230,9 +272,11 @@ int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st) {
   rmsnorm_kernel<<<grid, 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
-int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st) {
-  const int rows = a.b * (a.TA + a.TB);
+int launch_qk_rope(const QkRopeArgs& a_in, cudaStream_t st) {
+  const int rows = a_in.b * (a_in.TA + a_in.TB);
   if (rows == 0) return DF_OK;
+  QkRopeArgs a = a_in;
+  for (int i = 0; i < 64; ++i) a.inv_freq[i] = pow((double)a.theta, -2.0 * i / 128.0);
   qk_norm_rope_kernel<<<rows, 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
@@ -246,6 +290,12 @@ int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t s
 }
 int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st) {
   logsoftmax_rows_kernel<<<rows, 1024, 0, st>>>(x, V);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
+                                 cudaStream_t st) {
+  lse_from_stats_kernel<<<rows, 1024, 0, st>>>(reinterpret_cast<const float2*>(stats), n_stats, lse);
+  sub_lse_kernel<<<dim3(32, rows), 256, 0, st>>>(x, V, lse);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st) {

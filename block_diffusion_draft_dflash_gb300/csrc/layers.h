@@ -38,6 +38,7 @@ struct QkRopeArgs {
   df_bf16* v_plane;       // [b][Hkv][128][cap]
   int cap;
   int* status;
+  double inv_freq[64];    // theta^(-2i/128), filled by launch_qk_rope
 };
 
 int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
@@ -46,6 +47,9 @@ int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st);
 int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st);
 int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st);
 int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st);
+// In-place log-softmax of rows whose (max, sum exp) partials came from the LM-head GEMM.
+int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
+                                 cudaStream_t st);
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st);
 int launch_add_lengths(int32_t* len, const int32_t* add, int b, cudaStream_t st);
 
