@@ -39,8 +39,10 @@ def parse():
     ap.add_argument("--ctx", type=int, default=4096)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree", "draft"],
+    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree"],
                     help="run one small isolated case of a kernel a few times (for ncu captures), no JSON")
+    ap.add_argument("--case-n", type=int, default=24576, help="gemm case: weight rows (output features)")
+    ap.add_argument("--case-k", type=int, default=4096, help="gemm case: reduction length")
     return ap.parse_args()
 
 
@@ -176,47 +178,50 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def gemm_roofline(tm, b, T, peak_gbs, dev):
-    """Live CUDA-event timing of the step's target projections through dflash_linear.
+# kernels launched per traced call of each class (the rest launch one kernel per call)
+KERNELS_PER_CALL = {"topk": 4, "accept_compact": 3, "logsoftmax": 2}
 
-    Algorithmic bytes per launch = weight bytes (N*K*2) + activation rows in (M*K*2) +
-    fp32 rows out (M*N*4).  Returns the aggregate over the four per-layer projections.
+
+def gemm_algorithmic(b, B, nd_ctx_rows=16):
+    """Algorithmic bytes and flops of one step's projection GEMMs (class "gemm").
+
+    Per launch: weights N*K*2 + input rows M*K*2 + output rows M*N*2 (bf16-sized);
+    flops 2*M*N*K.  Target: 36 layers on b*(B+1) tree rows.  Drafter: 5 layers on b*16
+    block rows (q/k/v also on b*16 context rows) and the context fusion (K = 5*4096).
     """
+    d, F, nqkv = 4096, 12288, 6144
+    byts = flops = 0
+
+    def add(M, N, K, n=1):
+        nonlocal byts, flops
+        byts += n * (N * K * 2 + M * K * 2 + M * N * 2)
+        flops += n * 2 * M * N * K
+    Mt = b * (B + 1)
+    for (N, K) in ((nqkv, d), (d, d), (2 * F, d), (d, F)):
+        add(Mt, N, K, 36)
+    Md = b * 16
+    add(Md + b * nd_ctx_rows, nqkv, d, 5)
+    for (N, K) in ((d, d), (2 * F, d), (d, F)):
+        add(Md, N, K, 5)
+    add(b * nd_ctx_rows, d, 5 * d)
+    return byts, flops
+
+
+def traced_breakdown(dec, n_steps):
+    """Per-class device time of eager steps, from the library's CUDA-event tracing."""
     import torch
 
     from block_diffusion_draft_dflash_gb300 import _lib
-    L = tm.layers[0]
-    M = b * T
-    shapes = [("w_qkv", L["w_qkv"]), ("w_o", L["w_o"]), ("w_gate_up", L["w_gate_up"]), ("w_down", L["w_down"])]
-    ws = _lib.Workspace(256, dev)
-    tot_bytes, tot_ms, tot_flops, per = 0, 0.0, 0, {}
-    for name, W in shapes:
-        N, K = W.shape
-        X = torch.randn(M, K, device=dev).to(torch.bfloat16)
-        out = torch.zeros(M, N, device=dev, dtype=torch.float32)
-        for _ in range(3):
-            _lib.linear(X, W, out, accumulate=True, ws=ws)
-        torch.cuda.synchronize()
-        reps = 20
-        # other layers' weights are cycled so every launch streams its weights from HBM
-        Ws = [tm.layers[i][name] for i in range(len(tm.layers))]
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for r in range(reps):
-            _lib.linear(X, Ws[r % len(Ws)], out, accumulate=True, ws=ws)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        byts = N * K * 2 + M * K * 2 + M * N * 4
-        per[name] = {"M": M, "N": N, "K": K, "us": round(ms * 1e3, 2), "GBps": round(byts / ms / 1e6, 1)}
-        tot_bytes += byts
-        tot_ms += ms
-        tot_flops += 2 * M * N * K
-    achieved = tot_bytes / tot_ms / 1e6
-    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
-            "frac": round(achieved / peak_gbs, 4), "traffic": None,
-            "kernel": "gemm_bf16_tc_kernel (target q/k/v, o, gate/up, down projections)",
-            "per_launch": per, "tflops": round(tot_flops / tot_ms / 1e9, 1)}
+    torch.cuda.synchronize()
+    _lib.trace_read()
+    _lib.trace_enable(True)
+    for _ in range(n_steps):
+        dec.step()
+    torch.cuda.synchronize()
+    rec = _lib.trace_read()
+    _lib.trace_enable(False)
+    return {k: {"ms_per_step": round(ms / n_steps, 4), "launches_per_step": cnt / n_steps}
+            for k, (ms, cnt) in sorted(rec.items(), key=lambda kv: -kv[1][0])}
 
 
 def step_roofline_ms(b, B, N, hbm_gbs, tc_tflops):
@@ -338,69 +343,23 @@ def run_gpu(a, rank, world, local_rank):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_s = float(t.item())
 
-    roof = gemm_roofline(tm, b, B + 1, hbm, dev) if rank == 0 else None
+    # live per-kernel breakdown (CUDA events around every library launch, eager steps)
+    kern = traced_breakdown(dec, 3)
+    g_ms = kern["gemm"]["ms_per_step"]
+    g_bytes, g_flops = gemm_algorithmic(b, B)
+    achieved = g_bytes / (g_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": None,
+            "kernel": "gemm_bf16_tc_kernel, projection launches of one step (36 target + 5 drafter layers)",
+            "algorithmic_bytes_per_step": g_bytes, "ms_per_step": g_ms,
+            "launches_per_step": kern["gemm"]["launches_per_step"],
+            "tflops": round(g_flops / (g_ms * 1e-3) / 1e12, 1)}
     t_star_ms, step_bytes = step_roofline_ms(b, B, N, hbm, tc_sust)
     clk = clocks.summary(local_rank)
+    launches = sum(v["launches_per_step"] * KERNELS_PER_CALL.get(k, 1) for k, v in kern.items())
     return dict(ms=ms, e2e_s=e2e_s, emitted=emitted, roof=roof, t_star_ms=t_star_ms, step_bytes=step_bytes,
                 clocks=clk, peak_src=peak_src, hbm=hbm, tc=tc_sust, tau=emitted / (a.steps * b),
-                launches=count_launches(b))
-
-
-def count_launches(b):
-    """Kernels one captured step launches (all from libdflash.so)."""
-    per_layer = 9 + 1  # norm, qkv gemm, qk/rope, attention (+combine), o gemm, norm, gate/up, swiglu, down
-    # len, zero, fc gemm, fc norm, embed; layers; final norm, LM head, log-softmax, len
-    drafter = 5 + 5 * per_layer + 4
-    tree = 2
-    target = 1 + 36 * per_layer + 1 + 1 + 1
-    accept = 3
-    return drafter + tree + target + accept
-
-
-def kernel_case(a):
-    """Small isolated launches of one kernel at the step's shapes (device footprint < 2 GB)."""
-    import numpy as np
-    import torch
-
-    import synth
-    from block_diffusion_draft_dflash_gb300 import _lib
-    from oracle import ddtree
-    dev = "cuda:0"
-    if a.kernel_case == "gemm":
-        # gate/up projection of one target layer: W 24576 x 4096 (201 MB > L2), 257 tree rows
-        W = synth.device_normal((24576, 4096), 0.02, 5, "case.W", dev)
-        X = synth.device_normal((a.batch * (a.budget + 1), 4096), 1.0, 5, "case.X", dev)
-        out = torch.zeros(X.shape[0], 24576, device=dev)
-        ws = _lib.Workspace(256, dev)
-        for _ in range(4):
-            _lib.linear(X, W, out, accumulate=True, ws=ws)
-    elif a.kernel_case == "attn":
-        b, T, N = a.batch, a.budget + 1, a.ctx
-        cap = (N + T + 127) // 128 * 128
-        q = synth.device_normal((b, T, 32, 128), 1.0, 5, "case.q", dev)
-        k = synth.device_normal((b, 8, cap, 128), 1.0, 5, "case.k", dev)
-        v = synth.device_normal((b, 8, 128, cap), 1.0, 5, "case.v", dev)
-        lp = ddtree.log_softmax(synth.ddtree_logits(1002, 1, 15, 2000)[0])
-        anc = ddtree.ancestor_mask(ddtree.build_tree(lp, T - 1)["parent"])
-        anc_t = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(anc, (b,) + anc.shape)).view(np.int32)).to(dev)
-        out = torch.zeros_like(q)
-        ws = _lib.Workspace(_lib.tree_verify_attention_workspace_size(b, T, 32, 8, 128, cap), dev)
-        clen = torch.full((b,), N, dtype=torch.int32, device=dev)
-        for _ in range(4):
-            _lib.tree_verify_attention(q, k, v, clen, anc_t, 1 / np.sqrt(128), out, ws)
-    elif a.kernel_case == "ddtree":
-        b = 64
-        lp = torch.from_numpy(ddtree.log_softmax(synth.ddtree_logits(1002, b, 15, 151936))).to(dev)
-        from block_diffusion_draft_dflash_gb300 import engine  # noqa: F401
-        T = a.budget + 1
-        W = (T + 31) // 32
-        z = lambda *sh, dt=torch.int32: torch.zeros(sh, dtype=dt, device=dev)
-        out = dict(tok=z(b, T), parent=z(b, T), depth=z(b, T), score=z(b, T, dt=torch.float32), anc=z(b, T, W))
-        ws = _lib.Workspace(_lib.ddtree_build_workspace_size(b, 15, 151936, a.budget), dev)
-        for _ in range(4):
-            _lib.ddtree_build(lp, a.budget, out, ws)
-    torch.cuda.synchronize()
-    print("kernel case", a.kernel_case, "done")
+                launches=launches, kernels=kern)
 
 
 def main():
@@ -455,7 +414,8 @@ def main():
         "e2e": {"value": round(e2e, 3), "unit": "spec steps/s", "h2d_bytes_per_step": 4 * b,
                 "d2h_bytes_per_step": 4 * b * 16 + 4 * b},
         "tokens_per_step": round(r["tau"], 3),
-        "gpu_launches": r["launches"] * a.steps,
+        "gpu_launches": int(round(r["launches"] * a.steps)),
+        "kernels": r["kernels"],
         "clocks": r["clocks"],
     }
     print(json.dumps(line))

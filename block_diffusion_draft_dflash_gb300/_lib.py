@@ -46,6 +46,8 @@ _SIGS = {
     "dflash_status_string": (C.c_char_p, [C.c_int]),
     "dflash_check_device": (C.c_int, []),
     "dflash_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "dflash_trace_enable": (C.c_int, [C.c_int]),
+    "dflash_trace_read": (C.c_int, [C.c_int, C.c_char_p, C.POINTER(C.c_double), C.POINTER(C.c_int)]),
     "ddtree_build_workspace_size": (C.c_size_t, [C.c_int] * 4),
     "ddtree_build": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int] + [C.c_void_p] * 7 +
                      [C.c_size_t, C.c_void_p]),
@@ -231,6 +233,22 @@ def linear(X, W, out, accumulate=False, ws: Workspace = None):
     _check("dflash_linear", load().dflash_linear(_p(X), _p(W), M, N, K, _p(out), int(accumulate), ws.ptr,
                                                  ws.nbytes, _stream()))
     return ws
+
+
+def trace_enable(on=True):
+    load().dflash_trace_enable(int(on))
+
+
+def trace_read(max_entries=64):
+    """{kernel class: (total ms, launches)} since the last read (synchronises)."""
+    names = C.create_string_buffer(32 * max_entries)
+    ms = (C.c_double * max_entries)()
+    cnt = (C.c_int * max_entries)()
+    n = load().dflash_trace_read(max_entries, names, ms, cnt)
+    if n < 0:
+        raise StatusError("dflash_trace_read", n)
+    raw = names.raw
+    return {raw[32 * i:32 * i + 32].split(b"\0")[0].decode(): (ms[i], cnt[i]) for i in range(n)}
 
 
 def exported_symbols():

@@ -15,6 +15,7 @@
 // gather_feat_kernel: copies the feature rows of the root and the accepted path into the
 //   drafter's pending-context buffer.
 #include "common.cuh"
+#include "trace.h"
 
 namespace df {
 
@@ -147,6 +148,7 @@ int launch_accept(int b, int n_tree, const int32_t* choice, const int32_t* tok, 
                   const df_bf16* tree_feat, int feat_dim, df_bf16* new_feat, int max_new, int32_t* n_new,
                   int32_t* acc_tok, int32_t* n_acc, int32_t* new_bonus, int32_t* src_slot, void* scratch,
                   int* status, cudaStream_t st) {
+  DF_TRACE("accept_compact", st);
   AcceptScratch* sc = reinterpret_cast<AcceptScratch*>(scratch);
   accept_walk_kernel<<<b, 32, 0, st>>>(n_tree, max_new, choice, tok, parent, cache_len, cap, n_new, acc_tok, n_acc,
                                        new_bonus, src_slot, sc, status);

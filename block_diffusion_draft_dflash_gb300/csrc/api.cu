@@ -2,6 +2,7 @@
 // launch sequences of the composite calls.  No device memory is allocated here.
 #include <stdio.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "attention.h"
@@ -58,13 +59,12 @@ bool cfg_ok(const df_model_cfg* c) {
 
 struct LayerBufs {
   float* h;         // [R][d] residual stream
-  df_bf16* x;       // [Rx][d] normed GEMM input
-  float* qkv;       // [Rx][nqkv]
+  df_bf16* x;       // [Rx][d] normed GEMM input (query rows, then context rows)
   df_bf16* q;       // [R][Hq*hd]
   df_bf16* attn;    // [R][Hq*hd]
-  float* gu;        // [R][2F]
   df_bf16* act;     // [R][F]
-  float* o_part;
+  float* part;      // GEMM partial-tile slots, reused by every projection
+  float* o_part;    // attention split-KV partials
   float* ml_part;
 };
 
@@ -73,17 +73,29 @@ int nsplit_for(int b, int T, int Hq, int Hkv, int max_keys) {
   return attn_num_splits(b, Hkv, (T + NPT - 1) / NPT, max_keys);
 }
 
-// One pre-norm decoder layer over R rows (Rx >= R rows enter the QKV projection).
-// Attention keys: dense [0, dense_len[s] + dense_add) and an ancestor-masked tail.
+// Largest partial-slot buffer any projection of a layer needs.
+size_t layer_partial_bytes(const df_model_cfg* c, int R, int Rx) {
+  const int d = c->d_model, F = c->d_ff, qd = c->n_q_heads * 128, nqkv = (c->n_q_heads + 2 * c->n_kv_heads) * 128;
+  size_t m = gemm_partial_bytes(Rx, nqkv, d);
+  m = std::max(m, gemm_partial_bytes(R, d, qd));
+  m = std::max(m, gemm_partial_bytes(R, 2 * F, d));
+  m = std::max(m, gemm_partial_bytes(R, d, F));
+  return m;
+}
+
+// One pre-norm decoder layer over R query rows; x already holds RMSNorm(h) * attn_norm
+// for them (and the context rows R .. Rx-1, which only enter the q/k/v projection).
+// Each projection writes partial tiles that the next kernel reduces and consumes:
+//   q/k/v -> q/k norm + rotation + cache;  o -> residual + RMSNorm;
+//   gate/up -> SwiGLU;  down -> residual + the next RMSNorm (+ feature capture).
 struct LayerRun {
   const df_model_cfg* cfg;
   const df_layer_weights* w;
-  int b, T;           // R = b*T query rows
-  int Rx;             // rows of x / qkv (R plus context rows)
-  QkRopeArgs qk;      // filled except the layer-specific fields
-  AttnArgs at;        // filled except q/k/v/out
-  df_bf16* capture;   // feature capture for this layer's input (may be null)
-  int ld_capture;
+  int b, T;            // R = b*T query rows
+  int Rx;              // rows of the q/k/v projection (R plus context rows)
+  QkRopeArgs qk;       // filled except the layer-specific fields
+  AttnArgs at;         // filled except q/k/v/out
+  ResNormArgs out;     // down consumer: gain, destination rows and mapping, capture
   int* status;
 };
 
@@ -92,18 +104,13 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
   const int d = c.d_model, hd = 128, Hq = c.n_q_heads, Hkv = c.n_kv_heads, F = c.d_ff;
   const int nqkv = (Hq + 2 * Hkv) * hd;
   const int R = L.b * L.T;
-  RmsNormArgs rn{};
-  rn.in = B.h; rn.gain = L.w->attn_norm; rn.out = B.x; rn.ld_out = d; rn.rows = R; rn.d = d; rn.eps = c.rms_eps;
-  rn.group_out = 1; rn.group_in = 1; rn.in_off = 0;
-  rn.zero = B.qkv; rn.zero_count = (long long)L.Rx * nqkv;
-  rn.capture = L.capture; rn.ld_capture = L.ld_capture;
-  DF_TRY(launch_rmsnorm(rn, st));
+  PartialView pv{};
   GemmDesc g{};
   g.X = B.x; g.W = L.w->w_qkv; g.M = L.Rx; g.N = nqkv; g.K = d; g.ldx = d; g.ldw = d;
-  g.mode = kGemmAtomicAdd; g.out = B.qkv; g.ldo = nqkv; g.status = L.status;
+  g.mode = kGemmPartial; g.part = B.part; g.view = &pv; g.status = L.status;
   DF_TRY(launch_gemm(g, st));
   QkRopeArgs qk = L.qk;
-  qk.qkv = B.qkv; qk.ld_qkv = nqkv; qk.q_norm = L.w->q_norm; qk.k_norm = L.w->k_norm; qk.q_out = B.q;
+  qk.qkv = nullptr; qk.pv = pv; qk.ld_qkv = nqkv; qk.q_norm = L.w->q_norm; qk.k_norm = L.w->k_norm; qk.q_out = B.q;
   DF_TRY(launch_qk_rope(qk, st));
   AttnArgs at = L.at;
   at.q = B.q; at.k_plane = qk.k_plane; at.v_plane = qk.v_plane; at.out = B.attn;
@@ -111,22 +118,26 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
   DF_TRY(launch_attention(at, st));
   g = GemmDesc{};
   g.X = B.attn; g.W = L.w->w_o; g.M = R; g.N = d; g.K = Hq * hd; g.ldx = Hq * hd; g.ldw = Hq * hd;
-  g.mode = kGemmAtomicAdd; g.out = B.h; g.ldo = d; g.status = L.status;
+  g.mode = kGemmPartial; g.part = B.part; g.view = &pv; g.status = L.status;
   DF_TRY(launch_gemm(g, st));
-  rn = RmsNormArgs{};
-  rn.in = B.h; rn.gain = L.w->mlp_norm; rn.out = B.x; rn.ld_out = d; rn.rows = R; rn.d = d; rn.eps = c.rms_eps;
-  rn.group_out = 1; rn.group_in = 1;
-  rn.zero = B.gu; rn.zero_count = (long long)R * 2 * F;
-  DF_TRY(launch_rmsnorm(rn, st));
+  ResNormArgs rn{};
+  rn.pv = pv; rn.h = B.h; rn.d = d; rn.gain = L.w->mlp_norm; rn.eps = c.rms_eps; rn.out = B.x; rn.ld_out = d;
+  rn.rows = R; rn.group_out = 1; rn.group_in = 1; rn.in_off = 0;
+  DF_TRY(launch_res_norm(rn, st));
   g = GemmDesc{};
   g.X = B.x; g.W = L.w->w_gate_up; g.M = R; g.N = 2 * F; g.K = d; g.ldx = d; g.ldw = d;
-  g.mode = kGemmAtomicAdd; g.out = B.gu; g.ldo = 2 * F; g.status = L.status;
+  g.mode = kGemmPartial; g.part = B.part; g.view = &pv; g.status = L.status;
   DF_TRY(launch_gemm(g, st));
-  DF_TRY(launch_swiglu(B.gu, R, F, B.act, st));
+  SwigluArgs sw{};
+  sw.pv = pv; sw.rows = R; sw.F = F; sw.act = B.act;
+  DF_TRY(launch_swiglu_partial(sw, st));
   g = GemmDesc{};
   g.X = B.act; g.W = L.w->w_down; g.M = R; g.N = d; g.K = F; g.ldx = F; g.ldw = F;
-  g.mode = kGemmAtomicAdd; g.out = B.h; g.ldo = d; g.status = L.status;
+  g.mode = kGemmPartial; g.part = B.part; g.view = &pv; g.status = L.status;
   DF_TRY(launch_gemm(g, st));
+  rn = L.out;
+  rn.pv = pv; rn.h = B.h; rn.d = d; rn.eps = c.rms_eps;
+  DF_TRY(launch_res_norm(rn, st));
   return DF_OK;
 }
 
@@ -137,18 +148,17 @@ struct TargetWs {
 };
 size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs* out) {
   const int d = c->d_model, Hq = c->n_q_heads, Hkv = c->n_kv_heads, F = c->d_ff;
-  const size_t R = (size_t)b * n_tree, nqkv = (size_t)(Hq + 2 * Hkv) * 128;
+  const size_t R = (size_t)b * n_tree;
   Carver cv(base);
   TargetWs w{};
   w.B.h = cv.take<float>(R * d);
   w.B.x = cv.take<df_bf16>(R * d);
-  w.B.qkv = cv.take<float>(R * nqkv);
   w.B.q = cv.take<df_bf16>(R * Hq * 128);
   w.B.attn = cv.take<df_bf16>(R * Hq * 128);
-  w.B.gu = cv.take<float>(R * 2 * F);
   w.B.act = cv.take<df_bf16>(R * F);
+  w.B.part = cv.take<float>(layer_partial_bytes(c, (int)R, (int)R) / 4 + 1);
   w.amax = cv.take<unsigned long long>(R);
-  // partials sized for the largest split this call could choose (cache up to 2^20 keys)
+  // split-KV partials sized for the largest split this call could choose (cache up to 2^20 keys)
   const int ns = nsplit_for(b, n_tree, Hq, Hkv, 1 << 20);
   const size_t pb = attn_partial_bytes(b, n_tree, Hq, ns);
   w.B.o_part = cv.take<float>(pb / 4);
@@ -159,7 +169,6 @@ size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs*
 
 struct DraftWs {
   LayerBufs B;
-  float* fcacc;       // [b*max_new][d]
   df_bf16* xl;        // [b*(L-1)][d]
   int32_t* len_new;   // [b]
   float* stats;       // [b*(L-1)][4*ceil(V/128)][2] LM-head softmax partials
@@ -167,17 +176,17 @@ struct DraftWs {
 };
 size_t draft_ws(const df_model_cfg* c, int b, int max_new, void* base, DraftWs* out) {
   const int d = c->d_model, Hq = c->n_q_heads, Hkv = c->n_kv_heads, F = c->d_ff, L = c->block_size;
-  const size_t R = (size_t)b * L, Rc = (size_t)b * max_new, nqkv = (size_t)(Hq + 2 * Hkv) * 128;
+  const size_t R = (size_t)b * L, Rc = (size_t)b * max_new;
   Carver cv(base);
   DraftWs w{};
   w.B.h = cv.take<float>(R * d);
   w.B.x = cv.take<df_bf16>((R + Rc) * d);
-  w.B.qkv = cv.take<float>((R + Rc) * nqkv);
   w.B.q = cv.take<df_bf16>(R * Hq * 128);
   w.B.attn = cv.take<df_bf16>(R * Hq * 128);
-  w.B.gu = cv.take<float>(R * 2 * F);
   w.B.act = cv.take<df_bf16>(R * F);
-  w.fcacc = cv.take<float>((Rc ? Rc : 1) * d);
+  size_t pbytes = layer_partial_bytes(c, (int)R, (int)(R + Rc));
+  if (Rc) pbytes = std::max(pbytes, gemm_partial_bytes((int)Rc, d, c->n_feat_layers * d));
+  w.B.part = cv.take<float>(pbytes / 4 + 1);
   w.xl = cv.take<df_bf16>((size_t)b * (L - 1) * d);
   w.len_new = cv.take<int32_t>(b);
   w.stats = cv.take<float>((size_t)b * (L - 1) * 4 * ((c->vocab + 127) / 128) * 2);
@@ -198,11 +207,6 @@ __global__ void copy_len_kernel(const int32_t* src, int32_t* dst, int b) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < b) dst[s] = src[s];
 }
-__global__ void zero_kernel(float* p, long long n) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-    p[i] = 0.f;
-}
-
 }  // namespace
 }  // namespace df
 
@@ -373,12 +377,16 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
       if (c->feat_layers[f] == done_layers) return f;
     return -1;
   };
+  {
+    RmsNormArgs rn{};
+    rn.in = W.B.h; rn.gain = w->layers[0].attn_norm; rn.out = W.B.x; rn.ld_out = d; rn.rows = R; rn.d = d;
+    rn.eps = c->rms_eps; rn.group_out = 1; rn.group_in = 1;
+    rn.zero = reinterpret_cast<float*>(W.amax); rn.zero_count = 2LL * R;  // LM-head argmax keys start at 0
+    DF_TRY(launch_rmsnorm(rn, st));
+  }
   for (int li = 0; li < c->n_layers; ++li) {
     LayerRun L{};
     L.cfg = c; L.w = &w->layers[li]; L.b = b; L.T = n_tree; L.Rx = R; L.status = status;
-    const int f = tree_feat ? feat_slot(li) : -1;
-    L.capture = f >= 0 ? tree_feat + (size_t)f * d : nullptr;
-    L.ld_capture = nf * d;
     QkRopeArgs& qk = L.qk;
     qk.b = b; qk.TA = n_tree; qk.TB = 0; qk.base = cache_len; qk.nnew = nullptr; qk.depth = depth;
     qk.Hq = c->n_q_heads; qk.Hkv = Hkv; qk.eps = c->rms_eps; qk.theta = c->rope_theta;
@@ -390,15 +398,14 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
     at.scale = 1.0f / sqrtf(128.f);
     at.nsplit = nsplit_for(b, n_tree, c->n_q_heads, Hkv, cap);
     at.status = status;
+    ResNormArgs& o = L.out;  // after the down projection: next layer's input norm (or the final norm)
+    o.gain = li + 1 < c->n_layers ? w->layers[li + 1].attn_norm : w->final_norm;
+    o.out = W.B.x; o.ld_out = d; o.rows = R; o.group_out = 1; o.group_in = 1; o.in_off = 0;
+    const int f = tree_feat ? feat_slot(li + 1) : -1;
+    o.capture = f >= 0 ? tree_feat + (size_t)f * d : nullptr;
+    o.ld_capture = nf * d;
     DF_TRY(run_layer(L, W.B, st));
   }
-  RmsNormArgs rn{};
-  const int f = tree_feat ? feat_slot(c->n_layers) : -1;
-  rn.in = W.B.h; rn.gain = w->final_norm; rn.out = W.B.x; rn.ld_out = d; rn.rows = R; rn.d = d; rn.eps = c->rms_eps;
-  rn.group_out = 1; rn.group_in = 1;
-  rn.zero = reinterpret_cast<float*>(W.amax); rn.zero_count = 2LL * R;
-  rn.capture = f >= 0 ? tree_feat + (size_t)f * d : nullptr; rn.ld_capture = nf * d;
-  DF_TRY(launch_rmsnorm(rn, st));
   GemmDesc g{};
   g.X = W.B.x; g.W = w->embed; g.M = R; g.N = c->vocab; g.K = d; g.ldx = d; g.ldw = d;
   g.mode = kGemmArgmax; g.amax = W.amax; g.status = status;
@@ -433,19 +440,25 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
   if (max_new > 0) {
     len_new_kernel<<<(b + 255) / 256, 256, 0, st>>>(ctx_len, n_new, W.len_new, b);
     // context fusion: c = RMSNorm(fc . f) into the context rows of x
-    zero_kernel<<<296, 256, 0, st>>>(W.fcacc, (long long)Rc * d);
+    PartialView pv{};
     GemmDesc g{};
     g.X = new_feat; g.W = w->fc; g.M = Rc; g.N = d; g.K = nf * d; g.ldx = (long long)nf * d; g.ldw = (long long)nf * d;
-    g.mode = kGemmAtomicAdd; g.out = W.fcacc; g.ldo = d; g.status = status;
+    g.mode = kGemmPartial; g.part = W.B.part; g.view = &pv; g.status = status;
     DF_TRY(launch_gemm(g, st));
-    RmsNormArgs rn{};
-    rn.in = W.fcacc; rn.gain = w->fc_norm; rn.out = W.B.x + (size_t)R * d; rn.ld_out = d; rn.rows = Rc; rn.d = d;
-    rn.eps = c->rms_eps; rn.group_out = 1; rn.group_in = 1;
-    DF_TRY(launch_rmsnorm(rn, st));
+    ResNormArgs rn{};
+    rn.pv = pv; rn.h = nullptr; rn.d = d; rn.gain = w->fc_norm; rn.eps = c->rms_eps; rn.out = W.B.x + (size_t)R * d;
+    rn.ld_out = d; rn.rows = Rc; rn.group_out = 1; rn.group_in = 1; rn.in_off = 0;
+    DF_TRY(launch_res_norm(rn, st));
   } else {
     copy_len_kernel<<<(b + 255) / 256, 256, 0, st>>>(ctx_len, W.len_new, b);
   }
   DF_TRY(launch_embed(w->embed, d, c->vocab, nullptr, bonus, L, c->mask_id, W.B.h, R, status, st));
+  {
+    RmsNormArgs rn{};
+    rn.in = W.B.h; rn.gain = w->layers[0].attn_norm; rn.out = W.B.x; rn.ld_out = d; rn.rows = R; rn.d = d;
+    rn.eps = c->rms_eps; rn.group_out = 1; rn.group_in = 1;
+    DF_TRY(launch_rmsnorm(rn, st));
+  }
   for (int li = 0; li < c->n_layers; ++li) {
     LayerRun Lr{};
     Lr.cfg = c; Lr.w = &w->layers[li]; Lr.b = b; Lr.T = L; Lr.Rx = R + Rc; Lr.status = status;
@@ -461,12 +474,15 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
     at.scale = 1.0f / sqrtf(128.f);
     at.nsplit = nsplit_for(b, L, c->n_q_heads, Hkv, cap);
     at.status = status;
+    ResNormArgs& o = Lr.out;
+    if (li + 1 < c->n_layers) {
+      o.gain = w->layers[li + 1].attn_norm; o.out = W.B.x; o.rows = R; o.group_out = 1; o.group_in = 1; o.in_off = 0;
+    } else {  // final norm of rows 1..L-1 of every block, straight into the LM-head input
+      o.gain = w->final_norm; o.out = W.xl; o.rows = b * (L - 1); o.group_out = L - 1; o.group_in = L; o.in_off = 1;
+    }
+    o.ld_out = d;
     DF_TRY(run_layer(Lr, W.B, st));
   }
-  RmsNormArgs rn{};
-  rn.in = W.B.h; rn.gain = w->final_norm; rn.out = W.xl; rn.ld_out = d; rn.rows = b * (L - 1); rn.d = d;
-  rn.eps = c->rms_eps; rn.group_out = L - 1; rn.group_in = L; rn.in_off = 1;
-  DF_TRY(launch_rmsnorm(rn, st));
   GemmDesc g{};
   g.X = W.xl; g.W = w->embed; g.M = b * (L - 1); g.N = c->vocab; g.K = d; g.ldx = d; g.ldw = d;
   g.mode = kGemmStore; g.out = logprobs; g.ldo = c->vocab; g.status = status; g.stats = W.stats;

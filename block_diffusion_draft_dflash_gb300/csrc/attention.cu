@@ -24,6 +24,7 @@
 // otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
 #include "attention.h"
 #include "common.cuh"
+#include "trace.h"
 
 namespace df {
 
@@ -67,14 +68,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* q_smem = smem;                                  // 32 KB
   unsigned char* kv_smem = smem + kTileBytes;                    // stages x (K 32 KB + V 32 KB)
-  unsigned char* p_smem = kv_smem + kKVStages * 2 * kTileBytes;  // 32 KB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p_smem + kTileBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + kKVStages * 2 * kTileBytes);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kKVStages;
   uint64_t* s_full = kv_empty + kKVStages;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
+  uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
   __shared__ float red_max[2][2][128];  // [block parity][column half][row]
@@ -97,7 +96,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kKVStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 256); }
+    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     mbar_init(p_full, 256);
     mbar_init(o_done, 1);
     fence_barrier_init();
@@ -106,7 +105,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S0: cols 0-127, S1: 128-255, O: 256-383
+  // TMEM: S/P of even blocks at cols 0-127, of odd blocks at 128-255, O at 256-383.  P
+  // (bf16 pairs) overwrites its own S in place: half h at cols [64h, 64h+32).
+  const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
     if (lane == 0 && nblk > 0) {
@@ -139,27 +140,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0 && nblk > 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc = idesc_bf16_f32(128, 128);
-      const uint32_t qa = smem_u32(q_smem), pa = smem_u32(p_smem);
+      const uint32_t qa = smem_u32(q_smem);
       bool ok = mbar_wait(q_full, 0, p.status, 12);
       tc_fence_after();
       auto issue_pv = [&](int j) -> bool {
         if (!mbar_wait(p_full, j & 1, p.status, 13)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(kv_smem + (j % kKVStages) * 2 * kTileBytes + kTileBytes);
+        const uint32_t pt = tmem + (j & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          mma_bf16(tmem + 256, sdesc_kmajor_sw128(pa + off), sdesc_kmajor_sw128(vb + off), idesc,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: P columns (kk/4)*64 + (kk%4)*8
+          const uint32_t boff = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+          mma_bf16_ts(tmem + 256, pt + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_kmajor_sw128(vb + boff), idesc,
+                      (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(o_done);
         mma_commit(&kv_empty[j % kKVStages]);
         return true;
       };
+      // S_{j+1} is always issued after PV_{j-1}, and the tensor core runs one CTA's MMAs in
+      // issue order, so an S region is rewritten only after the PV that read its P.
       for (int j = 0; j < nblk && ok; ++j) {
         const int st = j % kKVStages;
         if (!mbar_wait(&kv_full[st], (j / kKVStages) & 1, p.status, 14)) { ok = false; break; }
-        if (!mbar_wait(&s_empty[j & 1], ((j >> 1) & 1) ^ 1, p.status, 15)) { ok = false; break; }
         tc_fence_after();
         const uint32_t kb = smem_u32(kv_smem + st * 2 * kTileBytes);
 #pragma unroll
@@ -187,18 +190,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float m_run = -INFINITY, l_part = 0.f;
     bool ok = true;
+    // Lazy rescaling: the running max m_run only moves when a block raises the row max
+    // by more than 8 (log2 units); P = 2^(s - m_run) then stays below 2^8, and O and the
+    // running sum are rescaled only on those rare moves.
+    constexpr float kRescale = 8.f;
     for (int j = 0; j < nblk; ++j) {
       // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
       const bool w1 = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.status, 16));
       float sv[64];
       float mpart = -INFINITY;
+      const uint32_t sp = tmem + lane_base + (j & 1) * 128 + half * 64;  // this half's S (then P)
       if (w1) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) tmem_ld16(tmem + lane_base + (j & 1) * 128 + half * 64 + c, sv + c);
+        for (int c = 0; c < 64; c += 16) tmem_ld16(sp + c, sv + c);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&s_empty[j & 1]);
         const int key0 = (kb0 + j) * kKB + half * 64;
         uint32_t adm[2];
 #pragma unroll
@@ -223,14 +229,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       red_max[j & 1][half][r] = mpart;
       if (!group_and(w1 && ok)) { ok = false; break; }  // uniform across the 256 threads
       const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+      float alpha = 1.f;
+      if (mx > m_run + kRescale) {  // also taken on the first admitted key (m_run = -inf)
+        alpha = exp2f(m_run - mx);   // 0 when m_run = -inf
+        m_run = mx;
+      }
       uint32_t packed[32];
-      if (warp_live && m_new != -INFINITY) {
+      if (warp_live && m_run != -INFINITY) {
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = exp2f(sv[c] - m_new), p1 = exp2f(sv[c + 1] - m_new);
+          const float p0 = exp2f(sv[c] - m_run), p1 = exp2f(sv[c + 1] - m_run);
           s4[(c >> 1) & 3] += p0 + p1;
           packed[c >> 1] = (uint32_t)f_to_bf16(p0) | ((uint32_t)f_to_bf16(p1) << 16);
         }
@@ -239,33 +248,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) packed[c] = 0u;
       }
-      m_run = m_new;
-      if (j >= 1) {
-        // PV of the previous block must be complete before P is overwritten / O rescaled
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O must hold PV of every earlier block before it is rescaled
         ok = mbar_wait(o_done, (j - 1) & 1, p.status, 17) && ok;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t oaddr = tmem + lane_base + 256 + half * 64;
+        const uint32_t oaddr = tmem + lane_base + 256 + half * 64;
 #pragma unroll
-          for (int c = 0; c < 64; c += 16) {
-            float o[16];
-            tmem_ld16(oaddr + c, o);
-            tmem_ld_wait();
+        for (int c = 0; c < 64; c += 16) {
+          float o[16];
+          tmem_ld16(oaddr + c, o);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tmem_st16(oaddr + c, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 16; ++i) o[i] *= alpha;
+          tmem_st16(oaddr + c, o);
         }
       }
-      // this half's 64 keys = one 64-key slab of the P tile; row r at r*128 B, 16-byte
-      // chunk c stored at chunk (c ^ (r & 7)) (128-byte swizzle)
-      unsigned char* rowp = p_smem + half * (kTileBytes / 2) + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-      fence_proxy_async();
+      tmem_st32(sp, packed);  // P over this half's (already loaded) S columns
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
     }
@@ -431,7 +430,7 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
   p.nsplit = a.nsplit;
   p.out = a.out; p.o_part = a.o_part; p.ml_part = a.ml_part;
   p.status = a.status;
-  const size_t smem = 1024 + kTileBytes * (2 + 2 * kKVStages) + 256;
+  const size_t smem = 1024 + kTileBytes * (1 + 2 * kKVStages) + 256;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -439,9 +438,13 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
     attr = true;
   }
   const int grid = a.b * a.Hkv * n_qtiles * a.nsplit;
-  attn_tc_kernel<<<grid, kAttnThreads, smem, st>>>(tq, tk, tv, p);
+  {
+    DF_TRACE(a.anc ? "attention_tree" : "attention_draft", st);
+    attn_tc_kernel<<<grid, kAttnThreads, smem, st>>>(tq, tk, tv, p);
+  }
   if (cudaGetLastError() != cudaSuccess) return DF_ERR_CUDA;
   if (a.nsplit > 1) {
+    DF_TRACE("attention_combine", st);
     const long long nrows = (long long)a.b * a.T * a.Hq;
     attn_combine_kernel<<<(unsigned)((nrows + 7) / 8), 256, 0, st>>>(a.o_part, a.ml_part, a.nsplit, nrows, a.out);
     if (cudaGetLastError() != cudaSuccess) return DF_ERR_CUDA;

@@ -17,6 +17,7 @@
 //   integer compare.  The CTA then writes the node arrays and the ancestor bitsets
 //   (one warp per row; each lane owns a 32-bit word).
 #include "common.cuh"
+#include "trace.h"
 
 namespace df {
 
@@ -477,6 +478,7 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
                   float* topk_val, int* status, cudaStream_t st, void* chunk_scratch) {
   const int K = B < V ? B : V;
   if (B > 0) {
+    DF_TRACE("topk", st);
     const int rows = b * D;
     if (chunk_scratch) {
       // chunked path: histogram, collect, final select (falls back per row when needed)
@@ -517,6 +519,7 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
       return DF_ERR_CUDA;
     configured = smem;
   }
+  DF_TRACE("ddtree_heap", st);
   ddtree_heap_kernel<<<b, 256, smem, st>>>(topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok, tok, parent, depth,
                                            score, anc, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;

@@ -23,6 +23,8 @@
 
 #include "common.cuh"
 #include "gemm.h"
+#include "partials.cuh"
+#include "trace.h"
 
 namespace df {
 
@@ -42,6 +44,11 @@ struct GemmParams {
   float* out;
   int ldo;
   unsigned long long* amax;  // argmax keys [M]
+  float* part;               // kGemmPartial: [G * max_seg][BN][128] fp32 slots
+  int* tile_cnt;             // kGemmPartial: [tiles] pieces per tile
+  int* tile_slot;            // kGemmPartial: [tiles][maxc] slots of each tile, in CTA order
+  int maxc;
+  int max_seg;
   float2* stats;             // kGemmStore: optional per (token, weight tile, warp) (max, sum exp(x - max))
   int n_stats;               // = 4 * number of weight tiles
   int* status;
@@ -111,6 +118,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   long long it0, it1;
   cta_range(p, it0, it1);
+  if (p.mode == kGemmPartial && threadIdx.x == 64 && it1 > it0) {
+    // Register this CTA's segments in the per-tile slot lists.  The CTA's place among a
+    // tile's contributors is its distance from the CTA that owns the tile's first k-step.
+    const long long G = gridDim.x, k = p.k_iters;
+    const long long t_first = it0 / k, t_last = (it1 - 1) / k;
+    for (long long t = t_first; t <= t_last; ++t) {
+      int pos = 0;
+      if (t * k < it0) {
+        long long cf = (t * k * G) / p.total_iters;  // CTA holding iteration t*k
+        while (cf + 1 < G && p.total_iters * (cf + 1) / G <= t * k) ++cf;
+        pos = (int)(blockIdx.x - cf);
+      }
+      p.tile_slot[t * p.maxc + pos] = (int)(blockIdx.x * p.max_seg + (t - t_first));
+      if ((t + 1) * k <= it1) p.tile_cnt[t] = pos + 1;  // this CTA holds the tile's last k-step
+    }
+  }
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -198,7 +221,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_ld16(taddr + c0, v);
         tmem_ld_wait();
         const int t0 = tt * BN + c0;
-        if (p.mode == kGemmAtomicAdd) {
+        if (p.mode == kGemmPartial) {
+          // this segment's accumulator -> its slot, [token][feature row], plain stores
+          float* dst = p.part + (((size_t)blockIdx.x * p.max_seg + si) * BN + c0) * 128 + q * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[j * 128] = v[j];
+        } else if (p.mode == kGemmAtomicAdd) {
           if (n_ok)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -326,6 +354,37 @@ int gemm_token_tile(int M) {
   return (bn + 15) / 16 * 16;
 }
 
+// Layout of a partial buffer: slots [grid * max_seg][BN][128] fp32, then tile_cnt[tiles],
+// then tile_slot[tiles][maxc].
+struct PartialLayout {
+  size_t slots_bytes, total_bytes;
+  long long tiles;
+  int max_seg, maxc;
+};
+static PartialLayout partial_layout(int M, int N, int K, long long grid) {
+  PartialLayout L;
+  const int BN = gemm_token_tile(M);
+  const long long n_tt = (M + BN - 1) / BN;
+  const long long k_iters = K / kBK;
+  L.tiles = (long long)((N + kBM - 1) / kBM) * n_tt;
+  const long long total = L.tiles * k_iters;
+  const long long range_max = (total + grid - 1) / grid, range_min = total / grid;
+  L.max_seg = (int)((range_max + k_iters - 1) / k_iters + 1);
+  L.maxc = (int)((k_iters + range_min - 1) / (range_min > 0 ? range_min : 1) + 2);
+  L.slots_bytes = (size_t)grid * L.max_seg * BN * 128 * 4;
+  L.total_bytes = L.slots_bytes + (size_t)L.tiles * 4 * (1 + L.maxc) + 64;
+  return L;
+}
+
+size_t gemm_partial_bytes(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const int BN = gemm_token_tile(M);
+  const long long total = (long long)((N + kBM - 1) / kBM) * ((M + BN - 1) / BN) * (K / kBK);
+  long long grid = num_sms();
+  if (grid > total) grid = total;
+  return partial_layout(M, N, K, grid).total_bytes;
+}
+
 int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return DF_OK;
   if (g.K % kBK != 0 || g.K <= 0) return DF_ERR_SHAPE;
@@ -353,7 +412,7 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   const long long tiles = (long long)((g.N + kBM - 1) / kBM) * p.n_ttiles;
   p.total_iters = tiles * p.k_iters;
   p.mode = g.mode;
-  p.whole_tiles = g.mode != kGemmAtomicAdd;
+  p.whole_tiles = g.mode == kGemmStore || g.mode == kGemmArgmax;
   p.out = g.out;
   p.ldo = g.ldo;
   p.amax = g.amax;
@@ -376,6 +435,24 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   const long long work = p.whole_tiles ? tiles : p.total_iters;
   if (grid > work) grid = work;
   if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;
+  if (g.mode == kGemmPartial) {
+    if (!g.part || !g.view) return DF_ERR_ARG;
+    const PartialLayout L = partial_layout(g.M, g.N, g.K, grid);
+    unsigned char* base = reinterpret_cast<unsigned char*>(g.part);
+    p.part = g.part;
+    p.max_seg = L.max_seg;
+    p.maxc = L.maxc;
+    p.tile_cnt = reinterpret_cast<int*>(base + L.slots_bytes);
+    p.tile_slot = p.tile_cnt + L.tiles;
+    PartialView& v = *g.view;
+    v.part = g.part;
+    v.tile_cnt = p.tile_cnt;
+    v.tile_slot = p.tile_slot;
+    v.maxc = L.maxc;
+    v.BN = BN;
+    v.n_ttiles = p.n_ttiles;
+  }
+  DF_TRACE(g.mode == kGemmArgmax ? "gemm_lmhead_argmax" : g.mode == kGemmStore ? "gemm_lmhead_logits" : "gemm", st);
   gemm_bf16_tc_kernel<<<(unsigned)grid, kGemmThreads, smem, st>>>(tw, tx, tx1, p);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

@@ -5,7 +5,9 @@
 
 namespace df {
 
-enum GemmMode { kGemmAtomicAdd = 0, kGemmStore = 1, kGemmArgmax = 2 };
+enum GemmMode { kGemmAtomicAdd = 0, kGemmStore = 1, kGemmArgmax = 2, kGemmPartial = 3 };
+
+struct PartialView;
 
 struct GemmDesc {
   const void* X;   // [M][K] bf16, row stride ldx elements
@@ -19,9 +21,13 @@ struct GemmDesc {
   float* stats;    // kGemmStore, optional: [M][4 * ceil(N/128)] float2 (max, sum exp(x - max)) partials
   int* status;
   int max_ctas;    // 0 = one CTA per SM
+  float* part;     // kGemmPartial: slot buffer (size from gemm_partial_bytes)
+  PartialView* view;  // kGemmPartial: filled with what consumers need to read the slots
 };
 
 int launch_gemm(const GemmDesc& g, cudaStream_t st);
+// Bytes of partial-tile slots a kGemmPartial launch of this shape writes.
+size_t gemm_partial_bytes(int M, int N, int K);
 int make_tmap_2d(struct CUtensorMap_st* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows);
 int num_sms();
 

@@ -12,6 +12,7 @@
 // come from the model config.
 #include "common.cuh"
 #include "layers.h"
+#include "trace.h"
 
 namespace df {
 
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(RmsNormArgs a) {
   }
 }
 
-// grid: rows; block 32 * warps; warp w handles heads w, w + warps, ... over Hq + 2 Hkv heads.
+// grid: (rows, ceil((Hq + 2 Hkv) / 8)); block 256: warp w handles head blockIdx.y * 8 + w.
 // Lane l owns elements l, l+32, l+64, l+96 of a 128-wide head, so both rotary pairs
 // (i, i+64) of the lane stay in the lane.
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
     return;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const float* row = a.qkv + (size_t)r * a.ld_qkv;
+  const float* row = a.qkv ? a.qkv + (size_t)r * a.ld_qkv : nullptr;
   // rotary angles of pairs (lane) and (lane + 32): pos * theta^(-2i/hd), reduced mod 2 pi
   // in fp64 so that large positions keep full fp32 accuracy in sincosf
   float c0, s0, c1, s1;
@@ -127,10 +128,17 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
     sincosf((float)a1, &s1, &c1);
   }
   const int nh = a.Hq + 2 * a.Hkv;
-  for (int h = warp; h < nh; h += nw) {
+  for (int h = blockIdx.y * nw + warp; h < nh && h < (int)(blockIdx.y + 1) * nw; h += nw) {
     if (!write_q && h < a.Hq) continue;
-    const float* x = row + h * HD;
-    float v0 = x[lane], v1 = x[lane + 32], v2 = x[lane + 64], v3 = x[lane + 96];
+    float v0, v1, v2, v3;
+    if (a.pv.part) {
+      float vv[4];
+      partial_sum_strided4(a.pv, h, r, lane, vv);
+      v0 = vv[0]; v1 = vv[1]; v2 = vv[2]; v3 = vv[3];
+    } else {
+      const float* x = row + h * HD;
+      v0 = x[lane]; v1 = x[lane + 32]; v2 = x[lane + 64]; v3 = x[lane + 96];
+    }
     if (h < a.Hq + a.Hkv) {
       const df_bf16* gain = h < a.Hq ? a.q_norm : a.k_norm;
       const float ms = warp_sum(v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3) / HD;
@@ -160,6 +168,74 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
       vt[(size_t)(lane + 96) * a.cap] = f_to_bf16(v3);
     }
   }
+}
+
+// grid: output rows; block min(d/4, 1024) threads (one float4 of the row each, two
+// passes for d > 4096).  d a multiple of 128 and at most 8192.
+__global__ void __launch_bounds__(1024) res_norm_kernel(ResNormArgs a) {
+  __shared__ float red[32];
+  const int o = blockIdx.x;
+  const int t = (o / a.group_out) * a.group_in + a.in_off + (o % a.group_out);
+  float4 v[2];
+  const int per = blockDim.x * 4;
+  float ss = 0.f;
+  float* hrow = a.h ? a.h + (size_t)t * a.d : nullptr;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int n = i * per + threadIdx.x * 4;
+    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n >= a.d) continue;
+    float4 y = partial_sum4(a.pv, n >> 7, t, n & 127);
+    if (hrow) {
+      const float4 hv = *reinterpret_cast<const float4*>(hrow + n);
+      y.x += hv.x; y.y += hv.y; y.z += hv.z; y.w += hv.w;
+      *reinterpret_cast<float4*>(hrow + n) = y;
+    }
+    v[i] = y;
+    ss += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+  }
+  ss = warp_sum(ss);
+  const int nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < nw; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / a.d + a.eps);
+  const uint2* g = reinterpret_cast<const uint2*>(a.gain);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int n = i * per + threadIdx.x * 4;
+    if (n >= a.d) continue;
+    const float4 y = v[i];
+    const uint2 gw = g[n / 4];
+    uint2 r;
+    r.x = (uint32_t)f_to_bf16(y.x * inv * bf16_to_f(gw.x & 0xFFFF)) |
+          ((uint32_t)f_to_bf16(y.y * inv * bf16_to_f(gw.x >> 16)) << 16);
+    r.y = (uint32_t)f_to_bf16(y.z * inv * bf16_to_f(gw.y & 0xFFFF)) |
+          ((uint32_t)f_to_bf16(y.w * inv * bf16_to_f(gw.y >> 16)) << 16);
+    *reinterpret_cast<uint2*>(a.out + (size_t)o * a.ld_out + n) = r;
+    if (a.capture) {
+      uint2 c;
+      c.x = (uint32_t)f_to_bf16(y.x) | ((uint32_t)f_to_bf16(y.y) << 16);
+      c.y = (uint32_t)f_to_bf16(y.z) | ((uint32_t)f_to_bf16(y.w) << 16);
+      *reinterpret_cast<uint2*>(a.capture + (size_t)t * a.ld_capture + n) = c;
+    }
+  }
+}
+
+// grid: (ceil(F / 1024), rows); block 256; 4 features per thread.
+__global__ void __launch_bounds__(256) swiglu_partial_kernel(SwigluArgs a) {
+  const int t = blockIdx.y;
+  const int f = (blockIdx.x * 256 + threadIdx.x) * 4;
+  if (f >= a.F) return;
+  const float4 g = partial_sum4(a.pv, f >> 7, t, f & 127);
+  const int fu = a.F + f;
+  const float4 u = partial_sum4(a.pv, fu >> 7, t, fu & 127);
+  auto sl = [](float x) { return x / (1.f + __expf(-x)); };
+  uint2 o;
+  o.x = (uint32_t)f_to_bf16(sl(g.x) * u.x) | ((uint32_t)f_to_bf16(sl(g.y) * u.y) << 16);
+  o.y = (uint32_t)f_to_bf16(sl(g.z) * u.z) | ((uint32_t)f_to_bf16(sl(g.w) * u.w) << 16);
+  *reinterpret_cast<uint2*>(a.act + (size_t)t * a.F + f) = o;
 }
 
 // act[r][f] = silu(gu[r][f]) * gu[r][F + f]
@@ -263,12 +339,14 @@ __global__ void add_lengths_kernel(int32_t* len, const int32_t* __restrict__ add
 // ----------------------------------------------------------------------------- launchers
 int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
                  float* h, int rows, int* status, cudaStream_t st) {
+  DF_TRACE("embed", st);
   embed_rows_kernel<<<rows, 256, 0, st>>>(E, d, V, tok, bonus, L, mask_id, h, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st) {
   int grid = a.rows;
   if (a.zero && a.zero_count && grid < 296) grid = 296;
+  DF_TRACE("rmsnorm", st);
   rmsnorm_kernel<<<grid, 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
@@ -277,7 +355,8 @@ int launch_qk_rope(const QkRopeArgs& a_in, cudaStream_t st) {
   if (rows == 0) return DF_OK;
   QkRopeArgs a = a_in;
   for (int i = 0; i < 64; ++i) a.inv_freq[i] = pow((double)a.theta, -2.0 * i / 128.0);
-  qk_norm_rope_kernel<<<rows, 256, 0, st>>>(a);
+  DF_TRACE("qk_norm_rope", st);
+  qk_norm_rope_kernel<<<dim3(rows, (a.Hq + 2 * a.Hkv + 7) / 8), 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st) {
@@ -288,17 +367,34 @@ int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t s
   swiglu_kernel<<<(unsigned)grid, 256, 0, st>>>(gu, rows, F, act);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
+int launch_res_norm(const ResNormArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return DF_OK;
+  if (a.d % 128 || a.d > 8192) return DF_ERR_SHAPE;
+  DF_TRACE("residual_norm", st);
+  int threads = a.d / 4 > 1024 ? 1024 : a.d / 4;
+  threads = (threads + 31) / 32 * 32;
+  res_norm_kernel<<<a.rows, threads, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_swiglu_partial(const SwigluArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return DF_OK;
+  DF_TRACE("swiglu", st);
+  swiglu_partial_kernel<<<dim3((a.F + 1023) / 1024, a.rows), 256, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
 int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st) {
   logsoftmax_rows_kernel<<<rows, 1024, 0, st>>>(x, V);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
                                  cudaStream_t st) {
+  DF_TRACE("logsoftmax", st);
   lse_from_stats_kernel<<<rows, 1024, 0, st>>>(reinterpret_cast<const float2*>(stats), n_stats, lse);
   sub_lse_kernel<<<dim3(32, rows), 256, 0, st>>>(x, V, lse);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st) {
+  DF_TRACE("argmax_finalize", st);
   argmax_finalize_kernel<<<(rows + 255) / 256, 256, 0, st>>>(amax, rows, out);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include "../../include/dflash.h"
+#include "partials.cuh"
 
 namespace df {
 
@@ -22,8 +23,32 @@ struct RmsNormArgs {
   int ld_capture;
 };
 
+// Consumer of a projection whose output is added to the residual stream (or, with
+// h == null, taken as is), followed by RMSNorm:  h[t] += y[t];  out[o] = RMSNorm(h[t]) * gain.
+struct ResNormArgs {
+  PartialView pv;         // partial tiles of y (d features)
+  float* h;               // residual rows [tokens][d], updated in place; null: no residual
+  int d;
+  const df_bf16* gain;
+  float eps;
+  df_bf16* out;           // bf16 rows, row stride ld_out
+  int ld_out;
+  int rows;               // output rows
+  int group_out, group_in, in_off;  // out row o <- token (o / group_out) * group_in + in_off + o % group_out
+  df_bf16* capture;       // optional bf16 copy of the new residual row, by token (row stride ld_capture)
+  int ld_capture;
+};
+
+// Consumer of the gate/up projection: act[t][f] = silu(y[t][f]) * y[t][F + f] (bf16).
+struct SwigluArgs {
+  PartialView pv;
+  int rows, F;
+  df_bf16* act;
+};
+
 struct QkRopeArgs {
-  const float* qkv;       // [rows][ld_qkv] fp32: q heads, k heads, v heads (hd 128)
+  const float* qkv;       // [rows][ld_qkv] fp32: q heads, k heads, v heads (hd 128); or
+  PartialView pv;         //   pv.part != null: read the projection's partial tiles (tile = head)
   int ld_qkv;
   int b, TA, TB;          // rows: b*TA "query" rows, then b*TB context rows
   const int32_t* base;    // [b] first slot (cache length before the step)
@@ -46,6 +71,8 @@ int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32
 int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st);
 int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st);
 int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st);
+int launch_res_norm(const ResNormArgs& a, cudaStream_t st);
+int launch_swiglu_partial(const SwigluArgs& a, cudaStream_t st);
 int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st);
 // In-place log-softmax of rows whose (max, sum exp) partials came from the LM-head GEMM.
 int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
