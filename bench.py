@@ -362,6 +362,52 @@ def run_gpu(a, rank, world, local_rank):
                 launches=launches, kernels=kern)
 
 
+def kernel_case(a):
+    """Small isolated launches of one kernel at the step's shapes (device footprint < 2 GB)."""
+    import numpy as np
+    import torch
+
+    import synth
+    from block_diffusion_draft_dflash_gb300 import _lib
+    from oracle import ddtree
+    dev = "cuda:0"
+    if a.kernel_case == "gemm":
+        # gate/up projection of one target layer: W 24576 x 4096 (201 MB > L2), 257 tree rows
+        W = synth.device_normal((24576, 4096), 0.02, 5, "case.W", dev)
+        X = synth.device_normal((a.batch * (a.budget + 1), 4096), 1.0, 5, "case.X", dev)
+        out = torch.zeros(X.shape[0], 24576, device=dev)
+        ws = _lib.Workspace(256, dev)
+        for _ in range(4):
+            _lib.linear(X, W, out, accumulate=True, ws=ws)
+    elif a.kernel_case == "attn":
+        b, T, N = a.batch, a.budget + 1, a.ctx
+        cap = (N + T + 127) // 128 * 128
+        q = synth.device_normal((b, T, 32, 128), 1.0, 5, "case.q", dev)
+        k = synth.device_normal((b, 8, cap, 128), 1.0, 5, "case.k", dev)
+        v = synth.device_normal((b, 8, 128, cap), 1.0, 5, "case.v", dev)
+        lp = ddtree.log_softmax(synth.ddtree_logits(1002, 1, 15, 2000)[0])
+        anc = ddtree.ancestor_mask(ddtree.build_tree(lp, T - 1)["parent"])
+        anc_t = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(anc, (b,) + anc.shape)).view(np.int32)).to(dev)
+        out = torch.zeros_like(q)
+        ws = _lib.Workspace(_lib.tree_verify_attention_workspace_size(b, T, 32, 8, 128, cap), dev)
+        clen = torch.full((b,), N, dtype=torch.int32, device=dev)
+        for _ in range(4):
+            _lib.tree_verify_attention(q, k, v, clen, anc_t, 1 / np.sqrt(128), out, ws)
+    elif a.kernel_case == "ddtree":
+        b = 64
+        lp = torch.from_numpy(ddtree.log_softmax(synth.ddtree_logits(1002, b, 15, 151936))).to(dev)
+        from block_diffusion_draft_dflash_gb300 import engine  # noqa: F401
+        T = a.budget + 1
+        W = (T + 31) // 32
+        z = lambda *sh, dt=torch.int32: torch.zeros(sh, dtype=dt, device=dev)
+        out = dict(tok=z(b, T), parent=z(b, T), depth=z(b, T), score=z(b, T, dt=torch.float32), anc=z(b, T, W))
+        ws = _lib.Workspace(_lib.ddtree_build_workspace_size(b, 15, 151936, a.budget), dev)
+        for _ in range(4):
+            _lib.ddtree_build(lp, a.budget, out, ws)
+    torch.cuda.synchronize()
+    print("kernel case", a.kernel_case, "done")
+
+
 def main():
     a = parse()
     if a.kernel_case:
