@@ -372,13 +372,16 @@ def kernel_case(a):
     from oracle import ddtree
     dev = "cuda:0"
     if a.kernel_case == "gemm":
-        # gate/up projection of one target layer: W 24576 x 4096 (201 MB > L2), 257 tree rows
-        W = synth.device_normal((24576, 4096), 0.02, 5, "case.W", dev)
-        X = synth.device_normal((a.batch * (a.budget + 1), 4096), 1.0, 5, "case.X", dev)
-        out = torch.zeros(X.shape[0], 24576, device=dev)
+        # one target projection (default gate/up: 24576 x 4096) on the 257 tree rows; enough
+        # distinct weight matrices are cycled that every launch streams its weights from HBM
+        N, K = a.case_n, a.case_k
+        n_w = max(1, -(-300_000_000 // (N * K * 2)))
+        Ws = [synth.device_normal((N, K), 0.02, 5, f"case.W{i}", dev) for i in range(n_w)]
+        X = synth.device_normal((a.batch * (a.budget + 1), K), 1.0, 5, "case.X", dev)
+        out = torch.zeros(X.shape[0], N, device=dev)
         ws = _lib.Workspace(256, dev)
-        for _ in range(4):
-            _lib.linear(X, W, out, accumulate=True, ws=ws)
+        for i in range(max(4, n_w)):
+            _lib.linear(X, Ws[i % n_w], out, accumulate=True, ws=ws)
     elif a.kernel_case == "attn":
         b, T, N = a.batch, a.budget + 1, a.ctx
         cap = (N + T + 127) // 128 * 128
