@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(32) accept_walk_kernel(int n_tree, int max_new
                                                          int cap, int32_t* n_new, int32_t* acc_tok, int32_t* n_acc,
                                                          int32_t* new_bonus, int32_t* src_slot,
                                                          AcceptScratch* scratch, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x, lane = threadIdx.x;
   const int32_t* ch = choice + (size_t)s * n_tree;
   const int32_t* tk = tok + (size_t)s * n_tree;
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(32) accept_walk_kernel(int n_tree, int max_new
 // grid: (n_layers * b * Hkv, 2): y = 0 moves K rows, y = 1 moves V columns.
 __global__ void __launch_bounds__(256) compact_kernel(df_bf16* k_cache, df_bf16* v_cache, int b, int Hkv, int cap,
                                                       const AcceptScratch* __restrict__ scratch) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int HD = 128;
   const int lhs = blockIdx.x;                 // ((layer * b) + s) * Hkv + h
   const int s = (lhs / Hkv) % b;
@@ -133,6 +137,8 @@ __global__ void __launch_bounds__(256) compact_kernel(df_bf16* k_cache, df_bf16*
 __global__ void __launch_bounds__(256) gather_feat_kernel(const df_bf16* __restrict__ tree_feat, int n_tree,
                                                           int feat_dim, df_bf16* __restrict__ new_feat, int max_new,
                                                           const AcceptScratch* __restrict__ scratch) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x, j = blockIdx.y;
   if (j > scratch[s].a) return;
   const int node = j == 0 ? 0 : scratch[s].path[j - 1];
@@ -150,12 +156,12 @@ int launch_accept(int b, int n_tree, const int32_t* choice, const int32_t* tok, 
                   int* status, cudaStream_t st) {
   DF_TRACE("accept_compact", st);
   AcceptScratch* sc = reinterpret_cast<AcceptScratch*>(scratch);
-  accept_walk_kernel<<<b, 32, 0, st>>>(n_tree, max_new, choice, tok, parent, cache_len, cap, n_new, acc_tok, n_acc,
+  launch_k(accept_walk_kernel, dim3(b), dim3(32), 0, st, n_tree, max_new, choice, tok, parent, cache_len, cap, n_new, acc_tok, n_acc,
                                        new_bonus, src_slot, sc, status);
   if (k_cache && v_cache && n_layers > 0)
-    compact_kernel<<<dim3(n_layers * b * Hkv, 2), 256, 0, st>>>(k_cache, v_cache, b, Hkv, cap, sc);
+    launch_k(compact_kernel, dim3(dim3(n_layers * b * Hkv, 2)), dim3(256), 0, st, k_cache, v_cache, b, Hkv, cap, sc);
   if (tree_feat && new_feat)
-    gather_feat_kernel<<<dim3(b, max_new), 256, 0, st>>>(tree_feat, n_tree, feat_dim, new_feat, max_new, sc);
+    launch_k(gather_feat_kernel, dim3(dim3(b, max_new)), dim3(256), 0, st, tree_feat, n_tree, feat_dim, new_feat, max_new, sc);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

@@ -200,10 +200,14 @@ size_t draft_ws(const df_model_cfg* c, int b, int max_new, void* base, DraftWs* 
 }
 
 __global__ void len_new_kernel(const int32_t* len, const int32_t* add, int32_t* out, int b) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < b) out[s] = len[s] + add[s];
 }
 __global__ void copy_len_kernel(const int32_t* src, int32_t* dst, int b) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < b) dst[s] = src[s];
 }
@@ -438,7 +442,7 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
   const int R = b * L, Rc = b * max_new;
   const size_t plane = (size_t)b * Hkv * cap * 128;
   if (max_new > 0) {
-    len_new_kernel<<<(b + 255) / 256, 256, 0, st>>>(ctx_len, n_new, W.len_new, b);
+    launch_k(len_new_kernel, dim3((b + 255) / 256), dim3(256), 0, st, ctx_len, n_new, W.len_new, b);
     // context fusion: c = RMSNorm(fc . f) into the context rows of x
     PartialView pv{};
     GemmDesc g{};
@@ -450,7 +454,7 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
     rn.ld_out = d; rn.rows = Rc; rn.group_out = 1; rn.group_in = 1; rn.in_off = 0;
     DF_TRY(launch_res_norm(rn, st));
   } else {
-    copy_len_kernel<<<(b + 255) / 256, 256, 0, st>>>(ctx_len, W.len_new, b);
+    launch_k(copy_len_kernel, dim3((b + 255) / 256), dim3(256), 0, st, ctx_len, W.len_new, b);
   }
   DF_TRY(launch_embed(w->embed, d, c->vocab, nullptr, bonus, L, c->mask_id, W.B.h, R, status, st));
   {
@@ -489,7 +493,7 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
   DF_TRY(launch_gemm(g, st));
   DF_TRY(launch_logsoftmax_from_stats(logprobs, b * (L - 1), c->vocab, W.stats, 4 * ((c->vocab + 127) / 128), W.lse,
                                       st));
-  copy_len_kernel<<<(b + 255) / 256, 256, 0, st>>>(W.len_new, ctx_len, b);
+  launch_k(copy_len_kernel, dim3((b + 255) / 256), dim3(256), 0, st, W.len_new, ctx_len, b);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

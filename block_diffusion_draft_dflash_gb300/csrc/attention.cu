@@ -80,19 +80,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ float red_sum[2][128];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work unit -> (sequence, kv head, query tile, split)
-  int u = blockIdx.x;
-  const int split = u % p.nsplit; u /= p.nsplit;
-  const int qt = u % p.n_qtiles; u /= p.n_qtiles;
-  const int kvh = u % p.Hkv;
-  const int s = u / p.Hkv;
-  const int G = p.Hq / p.Hkv, NPT = 128 / G;
-  const int dense_len = p.dense_len[s] + p.dense_add;
-  const int Lk = dense_len + p.tail_len;
-  const int nb = (Lk + kKB - 1) / kKB;
-  const int kb0 = (int)((long long)nb * split / p.nsplit), kb1 = (int)((long long)nb * (split + 1) / p.nsplit);
-  const int nblk = kb1 - kb0;
-
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kKVStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
@@ -105,6 +92,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // everything below reads what earlier kernels wrote (q, the caches, the lengths)
+  pdl_wait();
+  pdl_trigger();
+  // work unit -> (sequence, kv head, query tile, split)
+  int u = blockIdx.x;
+  const int split = u % p.nsplit; u /= p.nsplit;
+  const int qt = u % p.n_qtiles; u /= p.n_qtiles;
+  const int kvh = u % p.Hkv;
+  const int s = u / p.Hkv;
+  const int G = p.Hq / p.Hkv, NPT = 128 / G;
+  const int dense_len = p.dense_len[s] + p.dense_add;
+  const int Lk = dense_len + p.tail_len;
+  const int nb = (Lk + kKB - 1) / kKB;
+  const int kb0 = (int)((long long)nb * split / p.nsplit), kb1 = (int)((long long)nb * (split + 1) / p.nsplit);
+  const int nblk = kb1 - kb0;
   // TMEM: S/P of even blocks at cols 0-127, of odd blocks at 128-255, O at 256-383.  P
   // (bf16 pairs) overwrites its own S in place: half h at cols [64h, 64h+32).
   const uint32_t tmem = *tmem_slot;
@@ -190,9 +192,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float m_run = -INFINITY, l_part = 0.f;
     bool ok = true;
-    // Lazy rescaling: the running max m_run only moves when a block raises the row max
-    // by more than 8 (log2 units); P = 2^(s - m_run) then stays below 2^8, and O and the
-    // running sum are rescaled only on those rare moves.
+    // Lazy rescaling: the running max m_run (raw-score units) only moves when a block raises
+    // the row max by more than 8 in log2 units; P = 2^(scale2 (s - m_run)) then stays below
+    // 2^8, and O and the running sum are rescaled only on those rare moves.
     constexpr float kRescale = 8.f;
     for (int j = 0; j < nblk; ++j) {
       // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
@@ -205,21 +207,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; c += 16) tmem_ld16(sp + c, sv + c);
         tmem_ld_wait();
+        // Raw scores; the softmax scale is folded into the exponent below.  Only blocks
+        // that reach past the dense prefix need the admission mask.
         const int key0 = (kb0 + j) * kKB + half * 64;
-        uint32_t adm[2];
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const int j0 = key0 + 32 * g;
-          uint32_t bits = row_ok ? dense_bits32(j0, dense_len) : 0u;
-          if (anc_row) bits |= anc_bits32(anc_row, p.W, j0 - dense_len);
-          adm[g] = bits;
-        }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if ((kb0 + j + 1) * kKB > dense_len) {
+          uint32_t adm[2];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const bool a = (adm[c >> 5] >> (c & 31)) & 1u;
-          sv[c] = a ? sv[c] * scale2 : -INFINITY;
-          m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+          for (int g = 0; g < 2; ++g) {
+            const int j0 = key0 + 32 * g;
+            uint32_t bits = row_ok ? dense_bits32(j0, dense_len) : 0u;
+            if (anc_row) bits |= anc_bits32(anc_row, p.W, j0 - dense_len);
+            adm[g] = bits;
+          }
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            if (!((adm[c >> 5] >> (c & 31)) & 1u)) sv[c] = -INFINITY;
+            m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
         }
         mpart = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       } else {
@@ -228,20 +236,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       red_max[j & 1][half][r] = mpart;
       if (!group_and(w1 && ok)) { ok = false; break; }  // uniform across the 256 threads
-      const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);
+      const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);  // raw-score units
       float alpha = 1.f;
-      if (mx > m_run + kRescale) {  // also taken on the first admitted key (m_run = -inf)
-        alpha = exp2f(m_run - mx);   // 0 when m_run = -inf
+      if ((mx - m_run) * scale2 > kRescale) {  // also taken on the first admitted key (m_run = -inf)
+        alpha = ex2_approx((m_run - mx) * scale2);  // 0 when m_run = -inf
         m_run = mx;
       }
       uint32_t packed[32];
       if (warp_live && m_run != -INFINITY) {
+        const float mb = -m_run * scale2;
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = exp2f(sv[c] - m_run), p1 = exp2f(sv[c + 1] - m_run);
+          const float p0 = ex2_approx(fmaf(sv[c], scale2, mb)), p1 = ex2_approx(fmaf(sv[c + 1], scale2, mb));
           s4[(c >> 1) & 3] += p0 + p1;
-          packed[c >> 1] = (uint32_t)f_to_bf16(p0) | ((uint32_t)f_to_bf16(p1) << 16);
+          packed[c >> 1] = pack_bf16x2(p0, p1);
         }
         l_part = l_part * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       } else {
@@ -313,7 +322,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             *reinterpret_cast<float4*>(op + c + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
       }
       if (row_ok && half == 0) {
-        p.ml_part[((size_t)split * nrows + grow) * 2] = m_run;
+        p.ml_part[((size_t)split * nrows + grow) * 2] = m_run * scale2;  // log2 units for the combine
         p.ml_part[((size_t)split * nrows + grow) * 2 + 1] = l_run;
       }
     }
@@ -331,6 +340,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ o_part,
                                                            const float* __restrict__ ml_part, int nsplit,
                                                            long long nrows, df_bf16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= nrows) return;
@@ -440,13 +451,13 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
   const int grid = a.b * a.Hkv * n_qtiles * a.nsplit;
   {
     DF_TRACE(a.anc ? "attention_tree" : "attention_draft", st);
-    attn_tc_kernel<<<grid, kAttnThreads, smem, st>>>(tq, tk, tv, p);
+    launch_k(attn_tc_kernel, dim3(grid), dim3(kAttnThreads), smem, st, tq, tk, tv, p);
   }
   if (cudaGetLastError() != cudaSuccess) return DF_ERR_CUDA;
   if (a.nsplit > 1) {
     DF_TRACE("attention_combine", st);
     const long long nrows = (long long)a.b * a.T * a.Hq;
-    attn_combine_kernel<<<(unsigned)((nrows + 7) / 8), 256, 0, st>>>(a.o_part, a.ml_part, a.nsplit, nrows, a.out);
+    launch_k(attn_combine_kernel, dim3((unsigned)((nrows + 7) / 8)), dim3(256), 0, st, a.o_part, a.ml_part, a.nsplit, nrows, a.out);
     if (cudaGetLastError() != cudaSuccess) return DF_ERR_CUDA;
   }
   return DF_OK;

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dflash.h"
 
 #define DF_DEV __device__ __forceinline__
@@ -197,6 +199,32 @@ DF_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint3
 }
 DF_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// --------------------------------------------------------------------------- dependent launch
+// Every kernel of the library is launched with programmatic stream serialization: it may
+// start while its predecessor in the stream is still running.  pdl_wait() blocks until the
+// predecessor has completed and its memory is visible.  Each kernel calls pdl_trigger()
+// only after its own pdl_wait(), so a successor can launch only once this kernel's
+// predecessor is complete: code before pdl_wait() overlaps the immediate predecessor at
+// most, and must not touch memory that the predecessor reads or writes.
+DF_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DF_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // --------------------------------------------------------------------------- numerics
 // Order-preserving map of fp32 onto uint32 (larger float -> larger key; -0 < +0).
 DF_DEV uint32_t float_key(float f) {
@@ -217,6 +245,18 @@ DF_DEV float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// 2^x with the hardware approximation (flush-to-zero), one MUFU operation.
+DF_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Two floats -> packed bf16x2 (low = a), round to nearest even, one instruction.
+DF_DEV uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 DF_DEV float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }

@@ -203,6 +203,8 @@ template <bool kVec4>
 __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __restrict__ lp, int V, int K,
                                                                  int32_t* __restrict__ out_id,
                                                                  float* __restrict__ out_val, int* status) {
+  pdl_wait();
+  pdl_trigger();
   topk_row_full<kVec4>(lp, blockIdx.x, V, K, out_id, out_val, status);
 }
 
@@ -223,6 +225,8 @@ struct TopkScratch {     // per row
 
 __global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const float* __restrict__ lp, int V,
                                                                   uint32_t* __restrict__ ghist, int* status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t hist[4096];
   __shared__ uint32_t sh_nan;
   const size_t row = blockIdx.y;
@@ -251,6 +255,8 @@ __global__ void __launch_bounds__(kChunkThreads) topk_collect_kernel(const float
                                                                      TopkScratch* __restrict__ sc,
                                                                      unsigned long long* __restrict__ hi,
                                                                      unsigned long long* __restrict__ eq) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t warp_tmp[32];
   __shared__ uint32_t sh_bin, sh_above;
   const size_t row = blockIdx.y;
@@ -331,6 +337,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(const float* _
                                                                   const unsigned long long* __restrict__ eq,
                                                                   int32_t* __restrict__ out_id,
                                                                   float* __restrict__ out_val, int* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned long long cand[];  // [kCapEq] then [kMaxK]
   const size_t row = blockIdx.x;
   if (status && *(volatile int*)status == DF_ERR_NAN) return;
@@ -378,6 +386,8 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
                                                           int32_t* __restrict__ tok, int32_t* __restrict__ parent,
                                                           int32_t* __restrict__ depth, float* __restrict__ score,
                                                           uint32_t* __restrict__ anc, const int* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char smem[];
   const int s = blockIdx.x, tid = threadIdx.x;
   const int n = B + 1;
@@ -470,6 +480,8 @@ size_t ddtree_heap_smem(int D, int K, int B) {
 }
 
 __global__ void zero_u32_kernel(uint32_t* p, size_t n) {
+  pdl_wait();
+  pdl_trigger();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = 0;
 }
 
@@ -489,11 +501,11 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
           (reinterpret_cast<uintptr_t>(sc + rows) + 255) & ~uintptr_t(255));
       unsigned long long* eq = hi + (size_t)rows * kMaxK;
       const size_t nzero = (size_t)rows * 4096 + (size_t)rows * (sizeof(TopkScratch) / 4);
-      zero_u32_kernel<<<(unsigned)((nzero + 1023) / 1024 < 1024 ? (nzero + 1023) / 1024 : 1024), 1024, 0, st>>>(
+      launch_k(zero_u32_kernel, dim3((unsigned)((nzero + 1023) / 1024 < 1024 ? (nzero + 1023) / 1024 : 1024)), dim3(1024), 0, st, 
           ghist, nzero);
       const dim3 grid((V + kChunk - 1) / kChunk, rows);
-      topk_hist_kernel<<<grid, kChunkThreads, 0, st>>>(lp, V, ghist, status);
-      topk_collect_kernel<<<grid, kChunkThreads, 0, st>>>(lp, V, K, ghist, sc, hi, eq);
+      launch_k(topk_hist_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, ghist, status);
+      launch_k(topk_collect_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, K, ghist, sc, hi, eq);
       const size_t smem = (size_t)(kCapEq + kMaxK) * 8;
       static bool attr = false;
       if (!attr) {
@@ -502,13 +514,13 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
         attr = true;
       }
       if ((V & 3) == 0)
-        topk_final_kernel<true><<<rows, kTopkThreads, smem, st>>>(lp, V, K, sc, hi, eq, topk_id, topk_val, status);
+        launch_k(topk_final_kernel<true>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, hi, eq, topk_id, topk_val, status);
       else
-        topk_final_kernel<false><<<rows, kTopkThreads, smem, st>>>(lp, V, K, sc, hi, eq, topk_id, topk_val, status);
+        launch_k(topk_final_kernel<false>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, hi, eq, topk_id, topk_val, status);
     } else if ((V & 3) == 0) {
-      topk_rows_kernel<true><<<rows, kTopkThreads, 0, st>>>(lp, V, K, topk_id, topk_val, status);
+      launch_k(topk_rows_kernel<true>, dim3(rows), dim3(kTopkThreads), 0, st, lp, V, K, topk_id, topk_val, status);
     } else {
-      topk_rows_kernel<false><<<rows, kTopkThreads, 0, st>>>(lp, V, K, topk_id, topk_val, status);
+      launch_k(topk_rows_kernel<false>, dim3(rows), dim3(kTopkThreads), 0, st, lp, V, K, topk_id, topk_val, status);
     }
   }
   const size_t smem = ddtree_heap_smem(D, K > 0 ? K : 1, B);
@@ -520,7 +532,7 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
     configured = smem;
   }
   DF_TRACE("ddtree_heap", st);
-  ddtree_heap_kernel<<<b, 256, smem, st>>>(topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok, tok, parent, depth,
+  launch_k(ddtree_heap_kernel, dim3(b), dim3(256), smem, st, topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok, tok, parent, depth,
                                            score, anc, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

@@ -118,44 +118,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   long long it0, it1;
   cta_range(p, it0, it1);
-  if (p.mode == kGemmPartial && threadIdx.x == 64 && it1 > it0) {
-    // Register this CTA's segments in the per-tile slot lists.  The CTA's place among a
-    // tile's contributors is its distance from the CTA that owns the tile's first k-step.
-    const long long G = gridDim.x, k = p.k_iters;
-    const long long t_first = it0 / k, t_last = (it1 - 1) / k;
-    for (long long t = t_first; t <= t_last; ++t) {
-      int pos = 0;
-      if (t * k < it0) {
-        long long cf = (t * k * G) / p.total_iters;  // CTA holding iteration t*k
-        while (cf + 1 < G && p.total_iters * (cf + 1) / G <= t * k) ++cf;
-        pos = (int)(blockIdx.x - cf);
-      }
-      p.tile_slot[t * p.maxc + pos] = (int)(blockIdx.x * p.max_seg + (t - t_first));
-      if ((t + 1) * k <= it1) p.tile_cnt[t] = pos + 1;  // this CTA holds the tile's last k-step
-    }
-  }
-
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
     const uint64_t pol_w = p.w_keep ? policy_evict_last() : policy_evict_first(), pol_x = policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    long long it = it0;
-    Segment sg;
+    const long long n = it1 - it0;
+    auto coords = [&](long long it, int& wt, int& tt, int& k) {
+      const long long tile = it / p.k_iters;
+      k = (int)(it - tile * p.k_iters);
+      wt = (int)(tile / p.n_ttiles);
+      tt = (int)(tile % p.n_ttiles);
+    };
+    auto load_x = [&](int st, int tt, int k) {
+      unsigned char* xb = smem + (size_t)st * stage_bytes + w_bytes;
+      tma_load_2d(xb, &tmX, &full[st], k * kBK, tt * BN, pol_x);
+      if (p.sub1) tma_load_2d(xb + p.sub0 * 128, &tmX1, &full[st], k * kBK, tt * BN + p.sub0, pol_x);
+    };
+    // Weights are constant: the first ring's worth of weight tiles is requested before the
+    // previous kernel has finished.  Each stage's transaction count covers both halves, so
+    // it completes only once its token rows (loaded after the wait) have arrived too.
+    const int npre = (int)(n < S ? n : S);
+    for (int i = 0; i < npre; ++i) {
+      int wt, tt, k;
+      coords(it0 + i, wt, tt, k);
+      mbar_arrive_expect_tx(&full[i], stage_bytes);
+      tma_load_2d(smem + (size_t)i * stage_bytes, &tmW, &full[i], k * kBK, wt * kBM, pol_w);
+    }
+    pdl_wait();  // token rows are the previous kernel's output
+    for (int i = 0; i < npre; ++i) {
+      int wt, tt, k;
+      coords(it0 + i, wt, tt, k);
+      load_x(i, tt, k);
+    }
+    int stage = npre % S;
+    uint32_t phase = npre == S ? 1u : 0u;
     bool ok = true;
-    long long issued = 0;
-    while (ok && next_segment(p, it, it1, sg)) {
-      const int wt = (int)(sg.tile / p.n_ttiles), tt = (int)(sg.tile % p.n_ttiles);
-      for (int k = sg.k0; k < sg.k1; ++k) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 1)) { ok = false; break; }
-        unsigned char* sb = smem + (size_t)stage * stage_bytes;
-        mbar_arrive_expect_tx(&full[stage], stage_bytes);
-        tma_load_2d(sb, &tmW, &full[stage], k * kBK, wt * kBM, pol_w);
-        tma_load_2d(sb + w_bytes, &tmX, &full[stage], k * kBK, tt * BN, pol_x);
-        if (p.sub1) tma_load_2d(sb + w_bytes + p.sub0 * 128, &tmX1, &full[stage], k * kBK, tt * BN + p.sub0, pol_x);
-        ++issued;
-        if (++stage == S) { stage = 0; phase ^= 1; }
-      }
+    long long issued = npre;
+    for (long long i = npre; i < n; ++i) {
+      if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 1)) { ok = false; break; }
+      int wt, tt, k;
+      coords(it0 + i, wt, tt, k);
+      mbar_arrive_expect_tx(&full[stage], stage_bytes);
+      tma_load_2d(smem + (size_t)stage * stage_bytes, &tmW, &full[stage], k * kBK, wt * kBM, pol_w);
+      load_x(stage, tt, k);
+      ++issued;
+      if (++stage == S) { stage = 0; phase ^= 1; }
     }
     if (!ok) {
       // Drain: wait (bounded) for the loads still in flight before the CTA may exit.
@@ -203,6 +209,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue
+    // Partial slots and outputs may still be read by the previous kernel: wait for it.
+    pdl_wait();
+    pdl_trigger();
+    if (p.mode == kGemmPartial && threadIdx.x == 64 && it1 > it0) {
+      // Register this CTA's segments in the per-tile slot lists.  The CTA's place among a
+      // tile's contributors is its distance from the CTA that owns the tile's first k-step.
+      const long long G = gridDim.x, k = p.k_iters;
+      const long long t_first = it0 / k, t_last = (it1 - 1) / k;
+      for (long long t = t_first; t <= t_last; ++t) {
+        int pos = 0;
+        if (t * k < it0) {
+          long long cf = (t * k * G) / p.total_iters;  // CTA holding iteration t*k
+          while (cf + 1 < G && p.total_iters * (cf + 1) / G <= t * k) ++cf;
+          pos = (int)(blockIdx.x - cf);
+        }
+        p.tile_slot[t * p.maxc + pos] = (int)(blockIdx.x * p.max_seg + (t - t_first));
+        if ((t + 1) * k <= it1) p.tile_cnt[t] = pos + 1;  // this CTA holds the tile's last k-step
+      }
+    }
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     long long it = it0;
     Segment sg;
@@ -453,7 +478,7 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
     v.n_ttiles = p.n_ttiles;
   }
   DF_TRACE(g.mode == kGemmArgmax ? "gemm_lmhead_argmax" : g.mode == kGemmStore ? "gemm_lmhead_logits" : "gemm", st);
-  gemm_bf16_tc_kernel<<<(unsigned)grid, kGemmThreads, smem, st>>>(tw, tx, tx1, p);
+  launch_k(gemm_bf16_tc_kernel, dim3((unsigned)grid), dim3(kGemmThreads), smem, st, tw, tx, tx1, p);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

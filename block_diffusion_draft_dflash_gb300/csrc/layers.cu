@@ -20,6 +20,8 @@ namespace df {
 __global__ void __launch_bounds__(256) embed_rows_kernel(const df_bf16* __restrict__ E, int d, int V,
                                                          const int32_t* __restrict__ tok, const int32_t* __restrict__ bonus,
                                                          int L, int mask_id, float* __restrict__ h, int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   int t;
   if (bonus) {
@@ -42,6 +44,8 @@ __global__ void __launch_bounds__(256) embed_rows_kernel(const df_bf16* __restri
 
 // grid: out rows (+ extra blocks that only zero); block 256.  d multiple of 4.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(RmsNormArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8];
   const int o = blockIdx.x;
   // zeroing of the next accumulator, spread over all blocks
@@ -90,6 +94,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(RmsNormArgs a) {
 // Lane l owns elements l, l+32, l+64, l+96 of a 128-wide head, so both rotary pairs
 // (i, i+64) of the lane stay in the lane.
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int HD = 128;
   const int r = blockIdx.x;
   const int nA = a.b * a.TA;
@@ -173,6 +179,8 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
 // grid: output rows; block min(d/4, 1024) threads (one float4 of the row each, two
 // passes for d > 4096).  d a multiple of 128 and at most 8192.
 __global__ void __launch_bounds__(1024) res_norm_kernel(ResNormArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   const int o = blockIdx.x;
   const int t = (o / a.group_out) * a.group_in + a.in_off + (o % a.group_out);
@@ -225,6 +233,8 @@ __global__ void __launch_bounds__(1024) res_norm_kernel(ResNormArgs a) {
 
 // grid: (ceil(F / 1024), rows); block 256; 4 features per thread.
 __global__ void __launch_bounds__(256) swiglu_partial_kernel(SwigluArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
   const int f = (blockIdx.x * 256 + threadIdx.x) * 4;
   if (f >= a.F) return;
@@ -241,6 +251,8 @@ __global__ void __launch_bounds__(256) swiglu_partial_kernel(SwigluArgs a) {
 // act[r][f] = silu(gu[r][f]) * gu[r][F + f]
 __global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ gu, int rows, int F,
                                                      df_bf16* __restrict__ act) {
+  pdl_wait();
+  pdl_trigger();
   const long long n4 = (long long)rows * F / 4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
     const long long e = i * 4;
@@ -258,6 +270,8 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ g
 
 // grid: rows; block 1024.  Two passes: online max/sum, then x - (max + log(sum)).
 __global__ void __launch_bounds__(1024) logsoftmax_rows_kernel(float* __restrict__ x, int V) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sm[32], ss[32];
   float* row = x + (size_t)blockIdx.x * V;
   float m = -INFINITY, s = 0.f;
@@ -288,6 +302,8 @@ __global__ void __launch_bounds__(1024) logsoftmax_rows_kernel(float* __restrict
 // lse[r] from the GEMM epilogue's (max, sum exp) partials of row r.
 __global__ void __launch_bounds__(1024) lse_from_stats_kernel(const float2* __restrict__ stats, int n_stats,
                                                               float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sm[32], ss[32];
   const float2* st = stats + (size_t)blockIdx.x * n_stats;
   float m = -INFINITY, s = 0.f;
@@ -318,6 +334,8 @@ __global__ void __launch_bounds__(1024) lse_from_stats_kernel(const float2* __re
 
 // x[r][i] -= lse[r] over a grid of (row, chunk) blocks.
 __global__ void __launch_bounds__(256) sub_lse_kernel(float* __restrict__ x, int V, const float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   const float l = lse[r];
   float* row = x + (size_t)r * V;
@@ -327,11 +345,15 @@ __global__ void __launch_bounds__(256) sub_lse_kernel(float* __restrict__ x, int
 }
 
 __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ amax, int rows, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < rows) out[r] = (int32_t)(~(uint32_t)(amax[r] & 0xFFFFFFFFull));
 }
 
 __global__ void add_lengths_kernel(int32_t* len, const int32_t* __restrict__ add, int b) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < b) len[s] += add[s];
 }
@@ -340,14 +362,14 @@ __global__ void add_lengths_kernel(int32_t* len, const int32_t* __restrict__ add
 int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
                  float* h, int rows, int* status, cudaStream_t st) {
   DF_TRACE("embed", st);
-  embed_rows_kernel<<<rows, 256, 0, st>>>(E, d, V, tok, bonus, L, mask_id, h, status);
+  launch_k(embed_rows_kernel, dim3(rows), dim3(256), 0, st, E, d, V, tok, bonus, L, mask_id, h, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st) {
   int grid = a.rows;
   if (a.zero && a.zero_count && grid < 296) grid = 296;
   DF_TRACE("rmsnorm", st);
-  rmsnorm_kernel<<<grid, 256, 0, st>>>(a);
+  launch_k(rmsnorm_kernel, dim3(grid), dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_qk_rope(const QkRopeArgs& a_in, cudaStream_t st) {
@@ -356,7 +378,7 @@ int launch_qk_rope(const QkRopeArgs& a_in, cudaStream_t st) {
   QkRopeArgs a = a_in;
   for (int i = 0; i < 64; ++i) a.inv_freq[i] = pow((double)a.theta, -2.0 * i / 128.0);
   DF_TRACE("qk_norm_rope", st);
-  qk_norm_rope_kernel<<<dim3(rows, (a.Hq + 2 * a.Hkv + 7) / 8), 256, 0, st>>>(a);
+  launch_k(qk_norm_rope_kernel, dim3(dim3(rows, (a.Hq + 2 * a.Hkv + 7) / 8)), dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st) {
@@ -364,7 +386,7 @@ int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t s
   long long grid = (n4 + 255) / 256;
   if (grid > 4 * 152) grid = 4 * 152;
   if (grid < 1) grid = 1;
-  swiglu_kernel<<<(unsigned)grid, 256, 0, st>>>(gu, rows, F, act);
+  launch_k(swiglu_kernel, dim3((unsigned)grid), dim3(256), 0, st, gu, rows, F, act);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_res_norm(const ResNormArgs& a, cudaStream_t st) {
@@ -373,33 +395,33 @@ int launch_res_norm(const ResNormArgs& a, cudaStream_t st) {
   DF_TRACE("residual_norm", st);
   int threads = a.d / 4 > 1024 ? 1024 : a.d / 4;
   threads = (threads + 31) / 32 * 32;
-  res_norm_kernel<<<a.rows, threads, 0, st>>>(a);
+  launch_k(res_norm_kernel, dim3(a.rows), dim3(threads), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_swiglu_partial(const SwigluArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return DF_OK;
   DF_TRACE("swiglu", st);
-  swiglu_partial_kernel<<<dim3((a.F + 1023) / 1024, a.rows), 256, 0, st>>>(a);
+  launch_k(swiglu_partial_kernel, dim3(dim3((a.F + 1023) / 1024, a.rows)), dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st) {
-  logsoftmax_rows_kernel<<<rows, 1024, 0, st>>>(x, V);
+  launch_k(logsoftmax_rows_kernel, dim3(rows), dim3(1024), 0, st, x, V);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
                                  cudaStream_t st) {
   DF_TRACE("logsoftmax", st);
-  lse_from_stats_kernel<<<rows, 1024, 0, st>>>(reinterpret_cast<const float2*>(stats), n_stats, lse);
-  sub_lse_kernel<<<dim3(32, rows), 256, 0, st>>>(x, V, lse);
+  launch_k(lse_from_stats_kernel, dim3(rows), dim3(1024), 0, st, reinterpret_cast<const float2*>(stats), n_stats, lse);
+  launch_k(sub_lse_kernel, dim3(dim3(32, rows)), dim3(256), 0, st, x, V, lse);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st) {
   DF_TRACE("argmax_finalize", st);
-  argmax_finalize_kernel<<<(rows + 255) / 256, 256, 0, st>>>(amax, rows, out);
+  launch_k(argmax_finalize_kernel, dim3((rows + 255) / 256), dim3(256), 0, st, amax, rows, out);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_add_lengths(int32_t* len, const int32_t* add, int b, cudaStream_t st) {
-  add_lengths_kernel<<<(b + 255) / 256, 256, 0, st>>>(len, add, b);
+  launch_k(add_lengths_kernel, dim3((b + 255) / 256), dim3(256), 0, st, len, add, b);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
