@@ -39,7 +39,7 @@ def parse():
     ap.add_argument("--ctx", type=int, default=4096)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree"],
+    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree", "layer"],
                     help="run one small isolated case of a kernel a few times (for ncu captures), no JSON")
     ap.add_argument("--case-n", type=int, default=24576, help="gemm case: weight rows (output features)")
     ap.add_argument("--case-k", type=int, default=4096, help="gemm case: reduction length")
@@ -220,8 +220,16 @@ def traced_breakdown(dec, n_steps):
     torch.cuda.synchronize()
     rec = _lib.trace_read()
     _lib.trace_enable(False)
-    return {k: {"ms_per_step": round(ms / n_steps, 4), "launches_per_step": cnt / n_steps}
-            for k, (ms, cnt) in sorted(rec.items(), key=lambda kv: -kv[1][0])}
+    cls, shapes = {}, {}
+    for tag, (ms, cnt) in rec.items():
+        c = cls.setdefault(tag.split(" ")[0], [0.0, 0])
+        c[0] += ms
+        c[1] += cnt
+        if " " in tag:
+            shapes[tag] = (ms, cnt)
+    per = lambda d: {k: {"ms_per_step": round(ms / n_steps, 4), "launches_per_step": cnt / n_steps}
+                     for k, (ms, cnt) in sorted(d.items(), key=lambda kv: -kv[1][0])}
+    return per(cls), per(shapes)
 
 
 def step_roofline_ms(b, B, N, hbm_gbs, tc_tflops):
@@ -344,7 +352,7 @@ def run_gpu(a, rank, world, local_rank):
         e2e_s = float(t.item())
 
     # live per-kernel breakdown (CUDA events around every library launch, eager steps)
-    kern = traced_breakdown(dec, 3)
+    kern, kern_shapes = traced_breakdown(dec, 3)
     g_ms = kern["gemm"]["ms_per_step"]
     g_bytes, g_flops = gemm_algorithmic(b, B)
     achieved = g_bytes / (g_ms * 1e-3) / 1e9
@@ -359,7 +367,7 @@ def run_gpu(a, rank, world, local_rank):
     launches = sum(v["launches_per_step"] * KERNELS_PER_CALL.get(k, 1) for k, v in kern.items())
     return dict(ms=ms, e2e_s=e2e_s, emitted=emitted, roof=roof, t_star_ms=t_star_ms, step_bytes=step_bytes,
                 clocks=clk, peak_src=peak_src, hbm=hbm, tc=tc_sust, tau=emitted / (a.steps * b),
-                launches=launches, kernels=kern)
+                launches=launches, kernels=kern, kernel_shapes=kern_shapes)
 
 
 def kernel_case(a):
@@ -407,6 +415,33 @@ def kernel_case(a):
         ws = _lib.Workspace(_lib.ddtree_build_workspace_size(b, 15, 151936, a.budget), dev)
         for _ in range(4):
             _lib.ddtree_build(lp, a.budget, out, ws)
+    elif a.kernel_case == "layer":
+        # the target tree forward at Qwen3-8B width but 2 layers deep (about 2.5 GB on the
+        # device): every projection GEMM in its fused partial-tile mode, 9 GEMM launches a call
+        import dataclasses
+        from block_diffusion_draft_dflash_gb300 import engine
+        TS = dataclasses.replace(synth.QWEN3_8B_TARGET, n_layers=2, feat_layers=(1, 2))
+        tm = engine.DeviceModel.random(TS, 5, "target", dev)
+        b, T, N = a.batch, a.budget + 1, a.ctx
+        cap = (N + T + 127) // 128 * 128
+        k = synth.device_normal((2, b, 8, cap, 128), 1.0, 5, "case.k", dev)
+        v = synth.device_normal((2, b, 8, 128, cap), 1.0, 5, "case.v", dev)
+        lp = ddtree.log_softmax(synth.ddtree_logits(1002, 1, 15, 2000)[0])
+        tr = ddtree.build_tree(lp, T - 1)
+        rep = lambda x: torch.from_numpy(np.ascontiguousarray(np.broadcast_to(x, (b,) + x.shape))).to(dev)
+        tt = tr["tok"].astype(np.int32)
+        tt[0] = 1  # the root carries the last accepted token
+        tok = rep(tt)
+        depth = rep(tr["depth"].astype(np.int32))
+        anc = rep(ddtree.ancestor_mask(tr["parent"]).view(np.int32))
+        clen = torch.full((b,), N, dtype=torch.int32, device=dev)
+        choice = torch.zeros(b, T, dtype=torch.int32, device=dev)
+        feat = torch.zeros(b, T, 2 * TS.d_model, dtype=torch.bfloat16, device=dev)
+        ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T), dev)
+        for _ in range(4):
+            _lib.target_tree_forward(tm.cfg, tm.weights, tok, depth, anc, k, v, clen, choice, feat, ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
     torch.cuda.synchronize()
     print("kernel case", a.kernel_case, "done")
 
@@ -465,6 +500,7 @@ def main():
         "tokens_per_step": round(r["tau"], 3),
         "gpu_launches": int(round(r["launches"] * a.steps)),
         "kernels": r["kernels"],
+        "gemm_shapes": r["kernel_shapes"],
         "clocks": r["clocks"],
     }
     print(json.dumps(line))

@@ -239,16 +239,17 @@ def trace_enable(on=True):
     load().dflash_trace_enable(int(on))
 
 
-def trace_read(max_entries=64):
-    """{kernel class: (total ms, launches)} since the last read (synchronises)."""
-    names = C.create_string_buffer(32 * max_entries)
+def trace_read(max_entries=128):
+    """{tag: (total ms, launches)} since the last read (synchronises).  A tag is the kernel
+    class, optionally followed by a space and the launch shape."""
+    names = C.create_string_buffer(64 * max_entries)
     ms = (C.c_double * max_entries)()
     cnt = (C.c_int * max_entries)()
     n = load().dflash_trace_read(max_entries, names, ms, cnt)
     if n < 0:
         raise StatusError("dflash_trace_read", n)
     raw = names.raw
-    return {raw[32 * i:32 * i + 32].split(b"\0")[0].decode(): (ms[i], cnt[i]) for i in range(n)}
+    return {raw[64 * i:64 * i + 64].split(b"\0")[0].decode(): (ms[i], cnt[i]) for i in range(n)}
 
 
 def exported_symbols():

@@ -18,6 +18,8 @@
 //   * epilogues: fp32 reduction-add, fp32 store (whole tiles), or fused argmax over the
 //     output features (whole tiles; the target LM head writes no logits).
 // Every mbarrier wait is bounded (common.cuh); a timeout is recorded in the status word.
+#include <stdio.h>
+
 #include <mutex>
 #include <unordered_map>
 
@@ -40,7 +42,6 @@ struct GemmParams {
   int w_keep;       // 1: weights are re-read by later token tiles (keep them in L2)
   long long total_iters;
   int whole_tiles;  // 1: each CTA owns whole tiles (store / argmax epilogues)
-  int mode;
   float* out;
   int ldo;
   unsigned long long* amax;  // argmax keys [M]
@@ -83,6 +84,9 @@ DF_DEV bool next_segment(const GemmParams& p, long long& it, long long it1, Segm
   return true;
 }
 
+// MODE is the epilogue (GemmMode): one instantiation per epilogue keeps each kernel's code
+// small and free of per-element mode branches.
+template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmX1, const GemmParams p) {
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Partial slots and outputs may still be read by the previous kernel: wait for it.
     pdl_wait();
     pdl_trigger();
-    if (p.mode == kGemmPartial && threadIdx.x == 64 && it1 > it0) {
+    if (MODE == kGemmPartial && threadIdx.x == 64 && it1 > it0) {
       // Register this CTA's segments in the per-tile slot lists.  The CTA's place among a
       // tile's contributors is its distance from the CTA that owns the tile's first k-step.
       const long long G = gridDim.x, k = p.k_iters;
@@ -246,17 +250,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_ld16(taddr + c0, v);
         tmem_ld_wait();
         const int t0 = tt * BN + c0;
-        if (p.mode == kGemmPartial) {
+        if constexpr (MODE == kGemmPartial) {
           // this segment's accumulator -> its slot, [token][feature row], plain stores
           float* dst = p.part + (((size_t)blockIdx.x * p.max_seg + si) * BN + c0) * 128 + q * 32 + lane;
 #pragma unroll
           for (int j = 0; j < 16; ++j) dst[j * 128] = v[j];
-        } else if (p.mode == kGemmAtomicAdd) {
+        } else if constexpr (MODE == kGemmAtomicAdd) {
           if (n_ok)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (t0 + j < p.M) atomicAdd(p.out + (size_t)(t0 + j) * p.ldo + n, v[j]);
-        } else if (p.mode == kGemmStore) {
+        } else if constexpr (MODE == kGemmStore) {
           if (n_ok)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -436,7 +440,6 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   p.k_iters = g.K / kBK;
   const long long tiles = (long long)((g.N + kBM - 1) / kBM) * p.n_ttiles;
   p.total_iters = tiles * p.k_iters;
-  p.mode = g.mode;
   p.whole_tiles = g.mode == kGemmStore || g.mode == kGemmArgmax;
   p.out = g.out;
   p.ldo = g.ldo;
@@ -453,7 +456,11 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    for (auto k : {gemm_bf16_tc_kernel<kGemmPartial>, gemm_bf16_tc_kernel<kGemmAtomicAdd>,
+                   gemm_bf16_tc_kernel<kGemmStore>, gemm_bf16_tc_kernel<kGemmArgmax>}) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e != cudaSuccess) attr_err = e;
+    }
   });
   if (attr_err != cudaSuccess) return DF_ERR_CUDA;
   long long grid = num_sms();
@@ -477,8 +484,21 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
     v.BN = BN;
     v.n_ttiles = p.n_ttiles;
   }
-  DF_TRACE(g.mode == kGemmArgmax ? "gemm_lmhead_argmax" : g.mode == kGemmStore ? "gemm_lmhead_logits" : "gemm", st);
-  launch_k(gemm_bf16_tc_kernel, dim3((unsigned)grid), dim3(kGemmThreads), smem, st, tw, tx, tx1, p);
+  // trace tag: the kernel class, then the launch shape (M x N x K)
+  char tag[48] = {0};
+  if (trace_on())
+    snprintf(tag, sizeof tag, "%s %dx%dx%d", g.mode == kGemmArgmax ? "gemm_lmhead_argmax"
+                                             : g.mode == kGemmStore ? "gemm_lmhead_logits" : "gemm",
+             g.M, g.N, g.K);
+  DF_TRACE(tag, st);
+  const dim3 gd((unsigned)grid), bd(kGemmThreads);
+  switch (g.mode) {
+    case kGemmPartial: launch_k(gemm_bf16_tc_kernel<kGemmPartial>, gd, bd, smem, st, tw, tx, tx1, p); break;
+    case kGemmAtomicAdd: launch_k(gemm_bf16_tc_kernel<kGemmAtomicAdd>, gd, bd, smem, st, tw, tx, tx1, p); break;
+    case kGemmStore: launch_k(gemm_bf16_tc_kernel<kGemmStore>, gd, bd, smem, st, tw, tx, tx1, p); break;
+    case kGemmArgmax: launch_k(gemm_bf16_tc_kernel<kGemmArgmax>, gd, bd, smem, st, tw, tx, tx1, p); break;
+    default: return DF_ERR_ARG;
+  }
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

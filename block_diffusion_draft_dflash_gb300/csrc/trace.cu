@@ -76,8 +76,8 @@ extern "C" int dflash_trace_read(int max_entries, char* names, double* total_ms,
   for (auto& kv : agg) {
     if (n >= max_entries) break;
     if (names) {
-      strncpy(names + 32 * n, kv.first.c_str(), 31);
-      names[32 * n + 31] = 0;
+      strncpy(names + 64 * n, kv.first.c_str(), 63);
+      names[64 * n + 63] = 0;
     }
     if (total_ms) total_ms[n] = kv.second.first;
     if (count) count[n] = kv.second.second;

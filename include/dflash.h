@@ -279,9 +279,10 @@ int dflash_linear(const df_bf16* X, const df_bf16* W, int M, int N, int K, float
  * ------------------------------------------------------------------------------------ */
 /* Launch tracing, off by default.  While on, every kernel launch of the library (outside
  * stream capture) is bracketed by a pair of CUDA events on its stream.
- * dflash_trace_read synchronises on those events, writes up to max_entries per-kernel-class
- * totals (names: max_entries x 32 chars; total_ms; count), clears the record and returns
- * the number of classes written. */
+ * dflash_trace_read synchronises on those events, writes up to max_entries per-tag totals
+ * (names: max_entries x 64 chars, NUL-terminated; total_ms; count), clears the record and
+ * returns the number of tags written.  A tag is the kernel class, optionally followed by a
+ * space and the launch's shape (GEMMs: "M x N x K"). */
 int dflash_trace_enable(int on);
 int dflash_trace_read(int max_entries, char* names, double* total_ms, int* count);
 /* Reads and clears the device status word of a workspace (synchronises `stream`).

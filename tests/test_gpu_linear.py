@@ -11,7 +11,7 @@ from gpu_util import bf16_dev, rel_close
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (16, 256, 512), (33, 200, 192), (257, 1000, 1024),
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (16, 256, 512), (33, 200, 192), (257, 1000, 1024), (260, 256, 64), (264, 520, 320), (265, 300, 128),
                                    (300, 384, 4096), (600, 130, 256), (1028, 512, 128), (16, 4096, 4096)])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_linear_matches_float64(M, N, K, accumulate):
