@@ -66,6 +66,7 @@ struct LayerBufs {
   float* part;      // GEMM partial-tile slots, reused by every projection
   float* o_part;    // attention split-KV partials
   float* ml_part;
+  float2* rope;     // [Rx][64] rotary (cos, sin) of every q/k/v row, filled once per forward
 };
 
 int nsplit_for(int b, int T, int Hq, int Hkv, int max_keys) {
@@ -111,6 +112,7 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
   DF_TRY(launch_gemm(g, st));
   QkRopeArgs qk = L.qk;
   qk.qkv = nullptr; qk.pv = pv; qk.ld_qkv = nqkv; qk.q_norm = L.w->q_norm; qk.k_norm = L.w->k_norm; qk.q_out = B.q;
+  qk.rope = B.rope;
   DF_TRY(launch_qk_rope(qk, st));
   AttnArgs at = L.at;
   at.q = B.q; at.k_plane = qk.k_plane; at.v_plane = qk.v_plane; at.out = B.attn;
@@ -158,6 +160,7 @@ size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs*
   w.B.act = cv.take<df_bf16>(R * F);
   w.B.part = cv.take<float>(layer_partial_bytes(c, (int)R, (int)R) / 4 + 1);
   w.amax = cv.take<unsigned long long>(R);
+  w.B.rope = cv.take<float2>(R * 64);
   // split-KV partials sized for the largest split this call could choose (cache up to 2^20 keys)
   const int ns = nsplit_for(b, n_tree, Hq, Hkv, 1 << 20);
   const size_t pb = attn_partial_bytes(b, n_tree, Hq, ns);
@@ -191,6 +194,7 @@ size_t draft_ws(const df_model_cfg* c, int b, int max_new, void* base, DraftWs* 
   w.len_new = cv.take<int32_t>(b);
   w.stats = cv.take<float>((size_t)b * (L - 1) * 4 * ((c->vocab + 127) / 128) * 2);
   w.lse = cv.take<float>((size_t)b * (L - 1));
+  w.B.rope = cv.take<float2>((R + Rc) * 64);
   const int ns = nsplit_for(b, L, Hq, Hkv, 1 << 20);
   const size_t pb = attn_partial_bytes(b, L, Hq, ns);
   w.B.o_part = cv.take<float>(pb / 4);
@@ -396,6 +400,7 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
     qk.Hq = c->n_q_heads; qk.Hkv = Hkv; qk.eps = c->rms_eps; qk.theta = c->rope_theta;
     qk.k_plane = k_cache + (size_t)li * plane; qk.v_plane = v_cache + (size_t)li * plane; qk.cap = cap;
     qk.status = status;
+    if (li == 0) DF_TRY(launch_rope_table(qk, W.B.rope, st));
     AttnArgs& at = L.at;
     at.b = b; at.T = n_tree; at.Hq = c->n_q_heads; at.Hkv = Hkv; at.cap = cap;
     at.dense_len = cache_len; at.dense_add = 0; at.tail_len = n_tree; at.anc = anc;
@@ -472,6 +477,7 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
     qk.Hq = c->n_q_heads; qk.Hkv = Hkv; qk.eps = c->rms_eps; qk.theta = c->rope_theta;
     qk.k_plane = ctx_k + (size_t)li * plane; qk.v_plane = ctx_v + (size_t)li * plane; qk.cap = cap;
     qk.status = status;
+    if (li == 0) DF_TRY(launch_rope_table(qk, W.B.rope, st));
     AttnArgs& at = Lr.at;
     at.b = b; at.T = L; at.Hq = c->n_q_heads; at.Hkv = Hkv; at.cap = cap;
     at.dense_len = W.len_new; at.dense_add = L; at.tail_len = 0; at.anc = nullptr;

@@ -30,7 +30,8 @@ namespace df {
 
 constexpr int kAttnThreads = 320;  // 8 softmax warps, 1 TMA warp, 1 MMA warp
 constexpr int kKB = 128;     // keys per block
-constexpr int kKVStages = 2;
+constexpr int kKStages = 3;  // K tiles are free again once S = Q K^T has run
+constexpr int kVStages = 2;  // V tiles are free again once O += P V has run
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128x128 bf16 tile = 2 swizzled slabs
 
 DF_DEV int floordiv32(int t) { return t >= 0 ? (t >> 5) : -((-t + 31) >> 5); }
@@ -67,12 +68,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* q_smem = smem;                                  // 32 KB
-  unsigned char* kv_smem = smem + kTileBytes;                    // stages x (K 32 KB + V 32 KB)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + kKVStages * 2 * kTileBytes);
+  unsigned char* k_smem = smem + kTileBytes;                     // kKStages x 32 KB
+  unsigned char* v_smem = k_smem + kKStages * kTileBytes;        // kVStages x 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(v_smem + kVStages * kTileBytes);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + kKVStages;
-  uint64_t* s_full = kv_empty + kKVStages;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + kKStages;
+  uint64_t* v_full = k_empty + kKStages;
+  uint64_t* v_empty = v_full + kVStages;
+  uint64_t* s_full = v_empty + kVStages;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
@@ -82,7 +86,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kKVStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+    for (int i = 0; i < kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+    for (int i = 0; i < kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
     for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     mbar_init(p_full, 256);
     mbar_init(o_done, 1);
@@ -120,22 +125,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_load_3d(q_smem, &tmQ, q_full, 0, kvh * G, qz, pol_q);
       tma_load_3d(q_smem + kTileBytes / 2, &tmQ, q_full, 64, kvh * G, qz, pol_q);
       const int plane = s * p.Hkv + kvh;
-      bool ok = true;
-      for (int j = 0; j < nblk && ok; ++j) {
-        const int st = j % kKVStages;
-        if (!mbar_wait(&kv_empty[st], ((j / kKVStages) & 1) ^ 1, p.status, 11)) { ok = false; break; }
-        unsigned char* kb = kv_smem + st * 2 * kTileBytes;
-        unsigned char* vb = kb + kTileBytes;
+      // Loads in the order the MMAs need them: K_0, then (K_{j+1}, V_j) for every block j.
+      auto load_k = [&](int j) -> bool {
+        const int st = j % kKStages;
+        if (!mbar_wait(&k_empty[st], ((j / kKStages) & 1) ^ 1, p.status, 11)) return false;
+        unsigned char* kb = k_smem + st * kTileBytes;
         const int key0 = (kb0 + j) * kKB;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
-        tma_load_2d(kb, &tmK, &kv_full[st], 0, plane * p.cap + key0, pol_kv);
-        tma_load_2d(kb + kTileBytes / 2, &tmK, &kv_full[st], 64, plane * p.cap + key0, pol_kv);
-        tma_load_2d(vb, &tmV, &kv_full[st], key0, plane * 128, pol_kv);
-        tma_load_2d(vb + kTileBytes / 2, &tmV, &kv_full[st], key0 + 64, plane * 128, pol_kv);
+        mbar_arrive_expect_tx(&k_full[st], kTileBytes);
+        tma_load_2d(kb, &tmK, &k_full[st], 0, plane * p.cap + key0, pol_kv);
+        tma_load_2d(kb + kTileBytes / 2, &tmK, &k_full[st], 64, plane * p.cap + key0, pol_kv);
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int st = j % kVStages;
+        if (!mbar_wait(&v_empty[st], ((j / kVStages) & 1) ^ 1, p.status, 15)) return false;
+        unsigned char* vb = v_smem + st * kTileBytes;
+        const int key0 = (kb0 + j) * kKB;
+        mbar_arrive_expect_tx(&v_full[st], kTileBytes);
+        tma_load_2d(vb, &tmV, &v_full[st], key0, plane * 128, pol_kv);
+        tma_load_2d(vb + kTileBytes / 2, &tmV, &v_full[st], key0 + 64, plane * 128, pol_kv);
+        return true;
+      };
+      int nk = 0, nv = 0;  // tiles issued
+      bool ok = load_k(0);
+      if (ok) nk = 1;
+      for (int j = 0; j < nblk && ok; ++j) {
+        if (j + 1 < nblk) {
+          if (!load_k(j + 1)) { ok = false; break; }
+          ++nk;
+        }
+        if (!load_v(j)) { ok = false; break; }
+        ++nv;
       }
       if (!ok) {
+        // wait (bounded) for every load still in flight before the CTA may exit
         mbar_wait(q_full, 0, nullptr, 0);
-        for (int st = 0; st < kKVStages; ++st) mbar_wait(&kv_full[st], 0, nullptr, 0);
+        for (int j = nk - kKStages > 0 ? nk - kKStages : 0; j < nk; ++j)
+          mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1, nullptr, 0);
+        for (int j = nv - kVStages > 0 ? nv - kVStages : 0; j < nv; ++j)
+          mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, nullptr, 0);
       }
     }
   } else if (warp == 9) {
@@ -147,8 +175,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       auto issue_pv = [&](int j) -> bool {
         if (!mbar_wait(p_full, j & 1, p.status, 13)) return false;
+        if (!mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, p.status, 19)) return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(kv_smem + (j % kKVStages) * 2 * kTileBytes + kTileBytes);
+        const uint32_t vb = smem_u32(v_smem + (j % kVStages) * kTileBytes);
         const uint32_t pt = tmem + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: P columns (kk/4)*64 + (kk%4)*8
@@ -157,16 +186,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                       (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(o_done);
-        mma_commit(&kv_empty[j % kKVStages]);
+        mma_commit(&v_empty[j % kVStages]);
         return true;
       };
       // S_{j+1} is always issued after PV_{j-1}, and the tensor core runs one CTA's MMAs in
       // issue order, so an S region is rewritten only after the PV that read its P.
       for (int j = 0; j < nblk && ok; ++j) {
-        const int st = j % kKVStages;
-        if (!mbar_wait(&kv_full[st], (j / kKVStages) & 1, p.status, 14)) { ok = false; break; }
+        const int st = j % kKStages;
+        if (!mbar_wait(&k_full[st], (j / kKStages) & 1, p.status, 14)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = smem_u32(kv_smem + st * 2 * kTileBytes);
+        const uint32_t kb = smem_u32(k_smem + st * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
@@ -174,6 +203,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                    kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[j & 1]);
+        mma_commit(&k_empty[st]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(nblk - 1);
@@ -441,7 +471,7 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
   p.nsplit = a.nsplit;
   p.out = a.out; p.o_part = a.o_part; p.ml_part = a.ml_part;
   p.status = a.status;
-  const size_t smem = 1024 + kTileBytes * (1 + 2 * kKVStages) + 256;
+  const size_t smem = 1024 + kTileBytes * (1 + kKStages + kVStages) + 256;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

@@ -46,9 +46,8 @@ struct GemmParams {
   int ldo;
   unsigned long long* amax;  // argmax keys [M]
   float* part;               // kGemmPartial: [G * max_seg][BN][128] fp32 slots
-  int* tile_cnt;             // kGemmPartial: [tiles] pieces per tile
-  int* tile_slot;            // kGemmPartial: [tiles][maxc] slots of each tile, in CTA order
-  int maxc;
+  int* meta;                 // kGemmPartial: [tiles][meta_stride] piece count, then slots in CTA order
+  int meta_stride;
   int max_seg;
   float2* stats;             // kGemmStore: optional per (token, weight tile, warp) (max, sum exp(x - max))
   int n_stats;               // = 4 * number of weight tiles
@@ -228,8 +227,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           while (cf + 1 < G && p.total_iters * (cf + 1) / G <= t * k) ++cf;
           pos = (int)(blockIdx.x - cf);
         }
-        p.tile_slot[t * p.maxc + pos] = (int)(blockIdx.x * p.max_seg + (t - t_first));
-        if ((t + 1) * k <= it1) p.tile_cnt[t] = pos + 1;  // this CTA holds the tile's last k-step
+        p.meta[t * p.meta_stride + 1 + pos] = (int)(blockIdx.x * p.max_seg + (t - t_first));
+        if ((t + 1) * k <= it1) p.meta[t * p.meta_stride] = pos + 1;  // this CTA holds the tile's last k-step
       }
     }
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -383,12 +382,12 @@ int gemm_token_tile(int M) {
   return (bn + 15) / 16 * 16;
 }
 
-// Layout of a partial buffer: slots [grid * max_seg][BN][128] fp32, then tile_cnt[tiles],
-// then tile_slot[tiles][maxc].
+// Layout of a partial buffer: slots [grid * max_seg][BN][128] fp32, then per tile its piece
+// count and slot list, meta[tiles][meta_stride] (meta_stride >= maxc + 1, a multiple of 4).
 struct PartialLayout {
   size_t slots_bytes, total_bytes;
   long long tiles;
-  int max_seg, maxc;
+  int max_seg, maxc, meta_stride;
 };
 static PartialLayout partial_layout(int M, int N, int K, long long grid) {
   PartialLayout L;
@@ -401,7 +400,8 @@ static PartialLayout partial_layout(int M, int N, int K, long long grid) {
   L.max_seg = (int)((range_max + k_iters - 1) / k_iters + 1);
   L.maxc = (int)((k_iters + range_min - 1) / (range_min > 0 ? range_min : 1) + 2);
   L.slots_bytes = (size_t)grid * L.max_seg * BN * 128 * 4;
-  L.total_bytes = L.slots_bytes + (size_t)L.tiles * 4 * (1 + L.maxc) + 64;
+  L.meta_stride = (L.maxc + 1 + 3) / 4 * 4;
+  L.total_bytes = L.slots_bytes + (size_t)L.tiles * 4 * L.meta_stride + 64;
   return L;
 }
 
@@ -473,14 +473,12 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
     unsigned char* base = reinterpret_cast<unsigned char*>(g.part);
     p.part = g.part;
     p.max_seg = L.max_seg;
-    p.maxc = L.maxc;
-    p.tile_cnt = reinterpret_cast<int*>(base + L.slots_bytes);
-    p.tile_slot = p.tile_cnt + L.tiles;
+    p.meta = reinterpret_cast<int*>(base + L.slots_bytes);
+    p.meta_stride = L.meta_stride;
     PartialView& v = *g.view;
     v.part = g.part;
-    v.tile_cnt = p.tile_cnt;
-    v.tile_slot = p.tile_slot;
-    v.maxc = L.maxc;
+    v.meta = p.meta;
+    v.meta_stride = L.meta_stride;
     v.BN = BN;
     v.n_ttiles = p.n_ttiles;
   }

@@ -3,6 +3,7 @@
 //   rmsnorm_kernel         bf16 GEMM input <- RMSNorm(fp32 residual) * gain; can also
 //                          zero the next GEMM's fp32 accumulator and capture the residual
 //                          rows as bf16 feature rows (the drafter's context features)
+//   rope_table_kernel      (cos, sin) of every row's rotary angles, once per forward
 //   qk_norm_rope_kernel    per-head RMSNorm of q and k, rotary embedding, q to its buffer,
 //                          k and v into their cache slots (v transposed)
 //   swiglu_kernel          bf16 act <- silu(gate) * up from the fp32 gate/up accumulator
@@ -90,6 +91,47 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(RmsNormArgs a) {
   }
 }
 
+// Row r of a q/k/v projection: its sequence, cache slot and rotary position.  Rows
+// 0 .. b*TA-1 are query rows (slot after the sequence's new context rows, position offset by
+// depth); the b*TB context rows follow.  Returns false for a context row beyond its
+// sequence's count (nothing to write).
+DF_DEV bool qk_row(const QkRopeArgs& a, int r, int& s, int& slot, int& pos, bool& write_q) {
+  const int nA = a.b * a.TA;
+  if (r < nA) {
+    s = r / a.TA;
+    const int i = r % a.TA;
+    const int base = a.base[s] + (a.nnew ? a.nnew[s] : 0);
+    slot = base + i;
+    pos = base + (a.depth ? a.depth[r] : i);
+    write_q = true;
+    return true;
+  }
+  const int rr = r - nA;
+  s = rr / a.TB;
+  const int j = rr % a.TB;
+  slot = pos = a.base[s] + j;
+  write_q = false;
+  return j < a.nnew[s];
+}
+
+// grid: rows; block 64: (cos, sin) of pos * theta^(-2i/128) for pair i = threadIdx.x.
+// The angle is reduced mod 2 pi in fp64 so that large positions keep full fp32 accuracy
+// in sincosf.
+__global__ void __launch_bounds__(64) rope_table_kernel(QkRopeArgs a, float2* __restrict__ table) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x, i = threadIdx.x;
+  int s, slot, pos;
+  bool write_q;
+  if (!qk_row(a, r, s, slot, pos, write_q)) return;
+  const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
+  double ang = (double)pos * a.inv_freq[i];
+  ang -= twopi * rint(ang * inv_twopi);
+  float sn, cs;
+  sincosf((float)ang, &sn, &cs);
+  table[(size_t)r * 64 + i] = make_float2(cs, sn);
+}
+
 // grid: (rows, ceil((Hq + 2 Hkv) / 8)); block 256: warp w handles head blockIdx.y * 8 + w.
 // Lane l owns elements l, l+32, l+64, l+96 of a 128-wide head, so both rotary pairs
 // (i, i+64) of the lane stay in the lane.
@@ -98,41 +140,17 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
   pdl_trigger();
   constexpr int HD = 128;
   const int r = blockIdx.x;
-  const int nA = a.b * a.TA;
   int s, slot, pos;
   bool write_q;
-  if (r < nA) {
-    s = r / a.TA;
-    const int i = r % a.TA;
-    const int base = a.base[s] + (a.nnew ? a.nnew[s] : 0);
-    slot = base + i;
-    pos = base + (a.depth ? a.depth[r] : i);
-    write_q = true;
-  } else {
-    const int rr = r - nA;
-    s = rr / a.TB;
-    const int j = rr % a.TB;
-    if (j >= a.nnew[s]) return;
-    slot = pos = a.base[s] + j;
-    write_q = false;
-  }
+  if (!qk_row(a, r, s, slot, pos, write_q)) return;
   if (slot >= a.cap) {
     if (threadIdx.x == 0) set_status(a.status, DF_ERR_CAPACITY, r);
     return;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const float* row = a.qkv ? a.qkv + (size_t)r * a.ld_qkv : nullptr;
-  // rotary angles of pairs (lane) and (lane + 32): pos * theta^(-2i/hd), reduced mod 2 pi
-  // in fp64 so that large positions keep full fp32 accuracy in sincosf
-  float c0, s0, c1, s1;
-  {
-    const double twopi = 6.283185307179586476925286766559, inv_twopi = 0.15915494309189533576888376337251;
-    double a0 = (double)pos * a.inv_freq[lane], a1 = (double)pos * a.inv_freq[lane + 32];
-    a0 -= twopi * rint(a0 * inv_twopi);
-    a1 -= twopi * rint(a1 * inv_twopi);
-    sincosf((float)a0, &s0, &c0);
-    sincosf((float)a1, &s1, &c1);
-  }
+  const float2 cs0 = a.rope[(size_t)r * 64 + lane], cs1 = a.rope[(size_t)r * 64 + lane + 32];
+  const float c0 = cs0.x, s0 = cs0.y, c1 = cs1.x, s1 = cs1.y;
   const int nh = a.Hq + 2 * a.Hkv;
   for (int h = blockIdx.y * nw + warp; h < nh && h < (int)(blockIdx.y + 1) * nw; h += nw) {
     if (!write_q && h < a.Hq) continue;
@@ -372,11 +390,19 @@ int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st) {
   launch_k(rmsnorm_kernel, dim3(grid), dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
-int launch_qk_rope(const QkRopeArgs& a_in, cudaStream_t st) {
+int launch_rope_table(const QkRopeArgs& a_in, float2* table, cudaStream_t st) {
   const int rows = a_in.b * (a_in.TA + a_in.TB);
   if (rows == 0) return DF_OK;
   QkRopeArgs a = a_in;
   for (int i = 0; i < 64; ++i) a.inv_freq[i] = pow((double)a.theta, -2.0 * i / 128.0);
+  DF_TRACE("rope_table", st);
+  launch_k(rope_table_kernel, dim3(rows), dim3(64), 0, st, a, table);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st) {
+  const int rows = a.b * (a.TA + a.TB);
+  if (rows == 0) return DF_OK;
+  if (!a.rope) return DF_ERR_ARG;
   DF_TRACE("qk_norm_rope", st);
   launch_k(qk_norm_rope_kernel, dim3(dim3(rows, (a.Hq + 2 * a.Hkv + 7) / 8)), dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;

@@ -63,12 +63,15 @@ struct QkRopeArgs {
   df_bf16* v_plane;       // [b][Hkv][128][cap]
   int cap;
   int* status;
-  double inv_freq[64];    // theta^(-2i/128), filled by launch_qk_rope
+  const float2* rope;     // [rows][64] (cos, sin) of pair i at the row's position (launch_rope_table)
+  double inv_freq[64];    // theta^(-2i/128), filled by launch_rope_table
 };
 
 int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
                  float* h, int rows, int* status, cudaStream_t st);
 int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st);
+// Rotary table of every row of a forward (the positions are the same in every layer).
+int launch_rope_table(const QkRopeArgs& a, float2* table, cudaStream_t st);
 int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st);
 int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st);
 int launch_res_norm(const ResNormArgs& a, cudaStream_t st);
