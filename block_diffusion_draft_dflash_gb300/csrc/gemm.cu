@@ -33,6 +33,7 @@ namespace df {
 constexpr int kGemmThreads = 192;
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // k per stage (one 128-byte swizzle row)
+constexpr int kArgChunks = 16;  // argmax epilogue: running maxima of up to 16 x 32 token columns
 
 struct GemmParams {
   int M, N, K;
@@ -83,6 +84,52 @@ DF_DEV bool next_segment(const GemmParams& p, long long& it, long long it1, Segm
   return true;
 }
 
+// Argmax epilogue.  Keys are (order-preserving float bits << 32) | ~row, so the maximum
+// key is the largest value and, among equal values, the lowest row (token id).
+//
+// argmax_tile: for every token column of the tile, the maximum key over this warp's 32
+// rows, folded into the warp's running maxima (shared memory, run[chunk * 32 + lane]).
+// 32 columns at a time: a transposing butterfly (offsets 16, 8, 4, 2, 1) halves the
+// columns each lane holds while taking maxima, so lane L ends with column L after 31
+// exchanges instead of 5 per column.
+DF_DEV void argmax_tile(uint32_t taddr, int BN, int n, bool n_ok, unsigned long long* run, int lane) {
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+    tmem_ld16(taddr + c0, v);
+    const bool two = c0 + 16 < BN;  // BN is a multiple of 16; never read past the tile
+    if (two) tmem_ld16(taddr + c0 + 16, v + 16);
+    tmem_ld_wait();
+    unsigned long long k[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      k[j] = (n_ok && (j < 16 || two)) ? (((unsigned long long)float_key(v[j]) << 32) | (uint32_t)(~(uint32_t)n)) : 0ull;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const bool hi = (lane & off) != 0;  // keep the upper half of the current columns
+#pragma unroll
+      for (int i = 0; i < off; ++i) {
+        const unsigned long long keep = hi ? k[i + off] : k[i];
+        const unsigned long long send = hi ? k[i] : k[i + off];
+        const unsigned long long got = __shfl_xor_sync(0xffffffffu, send, off);
+        k[i] = keep > got ? keep : got;
+      }
+    }
+    unsigned long long& r = run[(c0 >> 5) * 32 + lane];
+    if (k[0] > r) r = k[0];
+  }
+}
+
+// Publishes the running maxima of token tile tt (one atomic per column) and clears them.
+template <class P>
+DF_DEV void argmax_flush(const P& p, unsigned long long* run, int tt, int lane) {
+  for (int c = 0; c * 32 < p.BN; ++c) {
+    const int col = c * 32 + lane, t = tt * p.BN + col;
+    unsigned long long& r = run[c * 32 + lane];
+    if (col < p.BN && t < p.M && r) atomicMax(p.amax + t, r);
+    r = 0ull;
+  }
+}
+
 // MODE is the epilogue (GemmMode): one instantiation per epilogue keeps each kernel's code
 // small and free of per-element mode branches.
 template <int MODE>
@@ -100,6 +147,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = bars + 2 * S;
   uint64_t* tempty = bars + 2 * S + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  // argmax epilogue: per warp, per 32-column chunk, per lane (= column) running maximum key
+  unsigned long long* run_max = reinterpret_cast<unsigned long long*>(bars + 2 * S + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int acc_cols = p.nbuf * BN;
@@ -232,6 +281,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    unsigned long long* run = run_max + (size_t)(warp - 2) * kArgChunks * 32;
+    int run_tt = 0;
+    if constexpr (MODE == kGemmArgmax) {
+      for (int i = lane; i < kArgChunks * 32; i += 32) run[i] = 0ull;
+      __syncwarp();
+    }
     long long it = it0;
     Segment sg;
     int si = 0;
@@ -244,6 +299,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int n = wt * kBM + q * 32 + lane;
       const bool n_ok = n < p.N;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      if constexpr (MODE == kGemmArgmax) {
+        if (tt != run_tt) {  // a new token tile: publish the finished one's maxima
+          argmax_flush(p, run, run_tt, lane);
+          run_tt = tt;
+        }
+        argmax_tile(taddr, BN, n, n_ok, run, lane);
+      } else
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
         tmem_ld16(taddr + c0, v);
@@ -275,24 +337,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 p.stats[(size_t)(t0 + j) * p.n_stats + wt * 4 + q] = make_float2(m, e);
             }
           }
-        } else {  // kGemmArgmax: max over this warp's 32 rows, per token column
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            unsigned long long key =
-                n_ok ? (((unsigned long long)float_key(v[j]) << 32) | (uint32_t)(~(uint32_t)n)) : 0ull;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-              key = other > key ? other : key;
-            }
-            if (lane == j && t0 + j < p.M) atomicMax(p.amax + t0 + j, key);
-          }
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       ++si;
     }
+    if constexpr (MODE == kGemmArgmax) argmax_flush(p, run, run_tt, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -452,7 +503,8 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   if (stages > 8) stages = 8;
   if (stages < 2) stages = 2;
   p.stages = stages;
-  const size_t smem = 1024 + (size_t)stages * stage_bytes + (2 * stages + 4) * 8 + 16;
+  const size_t smem = 1024 + (size_t)stages * stage_bytes + (2 * stages + 6) * 8 +
+                      (g.mode == kGemmArgmax ? 4 * kArgChunks * 32 * 8 : 0);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
