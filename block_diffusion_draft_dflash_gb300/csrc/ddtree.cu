@@ -11,11 +11,12 @@
 //   warp-aggregated shared-memory histograms) finds the K-th largest key T.  A gather
 //   pass takes every key > T and the lowest-id keys == T, and a bitonic sort orders the
 //   K survivors by (log-prob desc, token id asc).
-// Kernel 2 (ddtree_heap_kernel): one CTA per sequence.  One thread runs the heap: each
-//   entry is a single 64-bit key whose integer order is the tree's total order
-//   (score desc, depth asc, parent index asc, rank asc), so every heap comparison is one
-//   integer compare.  The CTA then writes the node arrays and the ancestor bitsets
-//   (one warp per row; each lane owns a 32-bit word).
+// Kernel 2 (ddtree_heap_kernel): one CTA per sequence.  One warp runs the best-first
+//   selection: each candidate is a single 64-bit key whose integer order is the tree's
+//   total order (score desc, depth asc, parent index asc, rank asc), the live candidates
+//   are held in the warp's registers and every pop is a warp-wide maximum.  The CTA then
+//   writes the node arrays and the ancestor bitsets (one warp per row; each lane owns a
+//   32-bit word).
 #include "common.cuh"
 #include "trace.h"
 
@@ -380,6 +381,12 @@ DF_DEV unsigned long long heap_key(float s, int depth, int parent, int rank) {
          ((uint32_t)(2047 - parent) << 16) | ((uint32_t)(2047 - rank) << 5);
 }
 
+// One CTA per sequence; warp 0 runs the best-first selection.  The live candidates (at most
+// B + 1) sit in the warp's registers, NREG per lane, densely packed: candidate c lives in
+// lane c % 32, register c / 32.  Each pop takes the lane maxima, a 5-step shuffle maximum
+// and a ballot for the owner; the last candidate fills the hole; the successors (first
+// child, next sibling) are appended.  Keys are unique, so the maximum is unique.
+template <int NREG>
 __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restrict__ topk_id,
                                                           const float* __restrict__ topk_val, int D, int K, int B,
                                                           const int32_t* __restrict__ root_tok,
@@ -393,8 +400,7 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
   const int n = B + 1;
   const int W = (n + 31) / 32;
   float* val = reinterpret_cast<float*>(smem);                                       // [D][K]
-  unsigned long long* heap = reinterpret_cast<unsigned long long*>(val + ((D * K + 1) & ~1));  // [B+2]
-  int32_t* n_par = reinterpret_cast<int32_t*>(heap + (B + 2));                       // [n]
+  int32_t* n_par = reinterpret_cast<int32_t*>(val + ((D * K + 1) & ~1));             // [n]
   int32_t* n_dep = n_par + n;                                                        // [n]
   int32_t* n_rank = n_dep + n;                                                       // [n]
   float* n_score = reinterpret_cast<float*>(n_rank + n);                             // [n]
@@ -404,46 +410,58 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
   for (int i = tid; i < D * K; i += blockDim.x) val[i] = gval[i];
   __syncthreads();
 
-  if (tid == 0) {
-    n_par[0] = -1; n_dep[0] = 0; n_rank[0] = -1; n_score[0] = 0.f;
-    int hn = 0;
-    auto push = [&](unsigned long long key) {
-      int i = hn++;
-      while (i > 0) {
-        const int p = (i - 1) >> 1;
-        const unsigned long long hp = heap[p];
-        if (hp >= key) break;
-        heap[i] = hp;
-        i = p;
-      }
-      heap[i] = key;
+  if (tid < 32) {
+    const int lane = tid;
+    unsigned long long cand[NREG];
+#pragma unroll
+    for (int i = 0; i < NREG; ++i) cand[i] = 0ull;  // 0 = empty (no key is 0)
+    int cnt = 0;
+    auto append = [&](unsigned long long key) {  // warp-uniform
+      const int li = cnt & 31, ri = cnt >> 5;
+#pragma unroll
+      for (int i = 0; i < NREG; ++i)
+        if (i == ri && lane == li) cand[i] = key;
+      ++cnt;
     };
-    if (B > 0) push(heap_key(0.f + val[0], 1, 0, 0));
+    // every lane writes the node arrays (same value), so every lane reads its own writes
+    n_par[0] = -1; n_dep[0] = 0; n_rank[0] = -1; n_score[0] = 0.f;
+    if (B > 0) append(heap_key(0.f + val[0], 1, 0, 0));
     for (int idx = 1; idx <= B; ++idx) {
-      const unsigned long long top = heap[0];
-      const unsigned long long last = heap[--hn];
-      int i = 0;
-      while (true) {  // sift `last` down from the root
-        int c = 2 * i + 1;
-        if (c >= hn) break;
-        unsigned long long hc = heap[c];
-        if (c + 1 < hn) {
-          const unsigned long long h2 = heap[c + 1];
-          if (h2 > hc) { hc = h2; ++c; }
-        }
-        if (hc <= last) break;
-        heap[i] = hc;
-        i = c;
+      unsigned long long best = cand[0];
+      int bi = 0;
+#pragma unroll
+      for (int i = 1; i < NREG; ++i)
+        if (cand[i] > best) { best = cand[i]; bi = i; }
+      unsigned long long top = best;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xffffffffu, top, o);
+        top = x > top ? x : top;
       }
-      if (hn > 0) heap[i] = last;
+      const int owner = __ffs(__ballot_sync(0xffffffffu, best == top)) - 1;
+      const int hole = __shfl_sync(0xffffffffu, bi, owner);
+      // the last candidate moves into the hole (or the hole is the last one)
+      const int last = cnt - 1, ll = last & 31, lr = last >> 5;
+      unsigned long long lv = 0ull;
+#pragma unroll
+      for (int i = 0; i < NREG; ++i)
+        if (i == lr) lv = cand[i];
+      lv = __shfl_sync(0xffffffffu, lv, ll);
+#pragma unroll
+      for (int i = 0; i < NREG; ++i)
+        if (lane == owner && i == hole) cand[i] = lv;
+#pragma unroll
+      for (int i = 0; i < NREG; ++i)
+        if (lane == ll && i == lr) cand[i] = 0ull;
+      --cnt;
       const uint32_t lo = (uint32_t)top;
       const int dep = 31 - (int)(lo >> 27);
       const int par = 2047 - (int)((lo >> 16) & 0x7FF);
       const int r = 2047 - (int)((lo >> 5) & 0x7FF);
       const float sc = key_float((uint32_t)(top >> 32));
       n_par[idx] = par; n_dep[idx] = dep; n_rank[idx] = r; n_score[idx] = sc;
-      if (dep < D) push(heap_key(sc + val[dep * K], dep + 1, idx, 0));
-      if (r + 1 < K) push(heap_key(n_score[par] + val[(dep - 1) * K + r + 1], dep, par, r + 1));
+      if (dep < D) append(heap_key(sc + val[dep * K], dep + 1, idx, 0));
+      if (r + 1 < K) append(heap_key(n_score[par] + val[(dep - 1) * K + r + 1], dep, par, r + 1));
     }
   }
   __syncthreads();
@@ -476,7 +494,7 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
 namespace df {
 size_t ddtree_heap_smem(int D, int K, int B) {
   const int n = B + 1;
-  return (size_t)((D * K + 1) & ~1) * 4 + (size_t)(B + 2) * 8 + (size_t)n * 16;
+  return (size_t)((D * K + 1) & ~1) * 4 + (size_t)n * 16;
 }
 
 __global__ void zero_u32_kernel(uint32_t* p, size_t n) {
@@ -524,16 +542,29 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
     }
   }
   const size_t smem = ddtree_heap_smem(D, K > 0 ? K : 1, B);
-  static thread_local size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    if (cudaFuncSetAttribute(ddtree_heap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return DF_ERR_CUDA;
-    configured = smem;
-  }
-  DF_TRACE("ddtree_heap", st);
-  launch_k(ddtree_heap_kernel, dim3(b), dim3(256), smem, st, topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok, tok, parent, depth,
-                                           score, anc, status);
-  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  // registers per lane for the live candidates (at most B + 1)
+  const int nreg = (B + 1 + 31) / 32;
+  auto launch = [&](auto kern) -> int {
+    static thread_local size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+      for (auto k : {ddtree_heap_kernel<1>, ddtree_heap_kernel<2>, ddtree_heap_kernel<4>, ddtree_heap_kernel<9>,
+                     ddtree_heap_kernel<17>, ddtree_heap_kernel<33>, ddtree_heap_kernel<65>})
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+          return DF_ERR_CUDA;
+      configured = smem;
+    }
+    DF_TRACE("ddtree_heap", st);
+    launch_k(kern, dim3(b), dim3(256), smem, st, topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok, tok, parent, depth,
+             score, anc, status);
+    return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  };
+  if (nreg <= 1) return launch(ddtree_heap_kernel<1>);
+  if (nreg <= 2) return launch(ddtree_heap_kernel<2>);
+  if (nreg <= 4) return launch(ddtree_heap_kernel<4>);
+  if (nreg <= 9) return launch(ddtree_heap_kernel<9>);
+  if (nreg <= 17) return launch(ddtree_heap_kernel<17>);
+  if (nreg <= 33) return launch(ddtree_heap_kernel<33>);
+  if (nreg <= 65) return launch(ddtree_heap_kernel<65>);
+  return DF_ERR_SHAPE;
 }
 }  // namespace df
