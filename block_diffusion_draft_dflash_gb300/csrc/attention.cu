@@ -12,14 +12,14 @@
 //
 // Tile: 128 query rows = (128 / G) consecutive tree nodes x the G query heads that share
 // one kv head (GQA), so one K/V tile feeds all 128 rows.  Per 128-key block:
-//   S = Q K^T   (tcgen05.mma, M=128 N=128 K=128, accumulator in TMEM, double-buffered)
+//   S = Q K^T   (tcgen05.mma, M=128 N=128 K=128, accumulator in TMEM, triple-buffered)
 //   softmax     (one TMEM lane = one query row, exp2 domain, running max / sum; the
 //                ancestor mask is applied as 32-bit words per key group)
 //   O += P V    (P written bf16 to shared memory in the 128-byte-swizzled K-major layout,
 //                V stored transposed in the cache so that its tile is K-major too)
-// Warp roles: warps 0-7 softmax/epilogue (two warps per row group, one per 64-column
-// half, exchanging row maxima through shared memory), warp 8 TMA producer, warp 9 TMEM
-// owner + MMA issuer.
+// Warp roles: warps 0 .. 4 kCG - 1 softmax/epilogue (kCG warps per 32-row group, one per
+// 128/kCG-column group, exchanging row maxima through shared memory), then a Q/K TMA
+// producer warp, the TMEM owner + MMA issuer warp and a V TMA producer warp.
 // The key range of a sequence is split over CTAs (split-KV) when the grid would
 // otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
 #include "attention.h"
@@ -28,8 +28,14 @@
 
 namespace df {
 
-constexpr int kAttnThreads = 320;  // 8 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kCG = 2;                       // column groups per query row (one warp each)
+constexpr int kCols = 128 / kCG;             // S columns (keys) and O columns (head dims) per thread
+constexpr int kSoftThreads = 128 * kCG;      // softmax / epilogue threads
+constexpr int kTmaWarp = 4 * kCG, kMmaWarp = 4 * kCG + 1, kVWarp = 4 * kCG + 2;
+constexpr int kAttnThreads = kSoftThreads + 96;  // + Q/K TMA warp, MMA warp, V TMA warp
 constexpr int kKB = 128;     // keys per block
+constexpr int kSBufs = 3;                    // S/P buffers in TMEM (128 columns each)
+constexpr uint32_t kOCol = kSBufs * 128;     // O accumulator columns [384, 512)
 constexpr int kKStages = 3;  // K tiles are free again once S = Q K^T has run
 constexpr int kVStages = 2;  // V tiles are free again once O += P V has run
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128x128 bf16 tile = 2 swizzled slabs
@@ -51,16 +57,16 @@ DF_DEV uint32_t dense_bits32(int j0, int dense_len) {
   return n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
 }
 
-// Named-barrier AND over the 256 softmax threads (barrier 1): every thread gets the same
+// Named-barrier AND over the softmax threads (barrier 1): every thread gets the same
 // answer, so the group leaves its loop together.
 DF_DEV bool group_and(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r) : "r"((uint32_t)v) : "memory");
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r) : "r"((uint32_t)v), "r"(kSoftThreads) : "memory");
   return r != 0;
 }
-DF_DEV void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+DF_DEV void group_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kSoftThreads) : "memory"); }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -77,23 +83,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* v_full = k_empty + kKStages;
   uint64_t* v_empty = v_full + kVStages;
   uint64_t* s_full = v_empty + kVStages;
-  uint64_t* p_full = s_full + 2;
+  uint64_t* p_full = s_full + kSBufs;
   uint64_t* o_done = p_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
-  __shared__ float red_max[2][2][128];  // [block parity][column half][row]
-  __shared__ float red_sum[2][128];
+  __shared__ float red_max[2][kCG][128];  // [block parity][column group][row]
+  __shared__ float red_sum[kCG][128];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
-    mbar_init(p_full, 256);
+    for (int i = 0; i < kSBufs; ++i) mbar_init(&s_full[i], 1);
+    mbar_init(p_full, kSoftThreads);
     mbar_init(o_done, 1);
     fence_barrier_init();
   }
-  if (warp == 9) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  if (warp == kMmaWarp) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -112,61 +118,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int nb = (Lk + kKB - 1) / kKB;
   const int kb0 = (int)((long long)nb * split / p.nsplit), kb1 = (int)((long long)nb * (split + 1) / p.nsplit);
   const int nblk = kb1 - kb0;
-  // TMEM: S/P of even blocks at cols 0-127, of odd blocks at 128-255, O at 256-383.  P
-  // (bf16 pairs) overwrites its own S in place: half h at cols [64h, 64h+32).
+  // TMEM: S/P of block j at cols 128 (j % 3) .. +127, O at 384-511.  P
+  // (bf16 pairs) overwrites its own S in place: column group g at cols [g kCols, g kCols + kCols/2).
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kTmaWarp || warp == kVWarp) {
+    // ------------------------------------------------------------ TMA producers
+    // One warp loads Q and the K tiles, another the V tiles: a wait for a free K slot never
+    // holds up a V load, or the other way round.
     if (lane == 0 && nblk > 0) {
-      // ------------------------------------------------------------ TMA producer
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      const int qz = s * p.T + qt * NPT;
-      tma_load_3d(q_smem, &tmQ, q_full, 0, kvh * G, qz, pol_q);
-      tma_load_3d(q_smem + kTileBytes / 2, &tmQ, q_full, 64, kvh * G, qz, pol_q);
       const int plane = s * p.Hkv + kvh;
-      // Loads in the order the MMAs need them: K_0, then (K_{j+1}, V_j) for every block j.
-      auto load_k = [&](int j) -> bool {
-        const int st = j % kKStages;
-        if (!mbar_wait(&k_empty[st], ((j / kKStages) & 1) ^ 1, p.status, 11)) return false;
-        unsigned char* kb = k_smem + st * kTileBytes;
+      const bool is_k = warp == kTmaWarp;
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        const int qz = s * p.T + qt * NPT;
+        tma_load_3d(q_smem, &tmQ, q_full, 0, kvh * G, qz, pol_q);
+        tma_load_3d(q_smem + kTileBytes / 2, &tmQ, q_full, 64, kvh * G, qz, pol_q);
+      }
+      const int NS = is_k ? kKStages : kVStages;
+      uint64_t* fullb = is_k ? k_full : v_full;
+      uint64_t* emptyb = is_k ? k_empty : v_empty;
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nblk; ++j) {
+        const int st = j % NS;
+        if (!mbar_wait(&emptyb[st], ((j / NS) & 1) ^ 1, p.status, is_k ? 11 : 15)) { ok = false; break; }
         const int key0 = (kb0 + j) * kKB;
-        mbar_arrive_expect_tx(&k_full[st], kTileBytes);
-        tma_load_2d(kb, &tmK, &k_full[st], 0, plane * p.cap + key0, pol_kv);
-        tma_load_2d(kb + kTileBytes / 2, &tmK, &k_full[st], 64, plane * p.cap + key0, pol_kv);
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        const int st = j % kVStages;
-        if (!mbar_wait(&v_empty[st], ((j / kVStages) & 1) ^ 1, p.status, 15)) return false;
-        unsigned char* vb = v_smem + st * kTileBytes;
-        const int key0 = (kb0 + j) * kKB;
-        mbar_arrive_expect_tx(&v_full[st], kTileBytes);
-        tma_load_2d(vb, &tmV, &v_full[st], key0, plane * 128, pol_kv);
-        tma_load_2d(vb + kTileBytes / 2, &tmV, &v_full[st], key0 + 64, plane * 128, pol_kv);
-        return true;
-      };
-      int nk = 0, nv = 0;  // tiles issued
-      bool ok = load_k(0);
-      if (ok) nk = 1;
-      for (int j = 0; j < nblk && ok; ++j) {
-        if (j + 1 < nblk) {
-          if (!load_k(j + 1)) { ok = false; break; }
-          ++nk;
+        mbar_arrive_expect_tx(&fullb[st], kTileBytes);
+        if (is_k) {
+          unsigned char* kb = k_smem + st * kTileBytes;
+          tma_load_2d(kb, &tmK, &fullb[st], 0, plane * p.cap + key0, pol_kv);
+          tma_load_2d(kb + kTileBytes / 2, &tmK, &fullb[st], 64, plane * p.cap + key0, pol_kv);
+        } else {
+          unsigned char* vb = v_smem + st * kTileBytes;
+          tma_load_2d(vb, &tmV, &fullb[st], key0, plane * 128, pol_kv);
+          tma_load_2d(vb + kTileBytes / 2, &tmV, &fullb[st], key0 + 64, plane * 128, pol_kv);
         }
-        if (!load_v(j)) { ok = false; break; }
-        ++nv;
+        ++issued;
       }
       if (!ok) {
         // wait (bounded) for every load still in flight before the CTA may exit
-        mbar_wait(q_full, 0, nullptr, 0);
-        for (int j = nk - kKStages > 0 ? nk - kKStages : 0; j < nk; ++j)
-          mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1, nullptr, 0);
-        for (int j = nv - kVStages > 0 ? nv - kVStages : 0; j < nv; ++j)
-          mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, nullptr, 0);
+        if (is_k) mbar_wait(q_full, 0, nullptr, 0);
+        for (int j = issued - NS > 0 ? issued - NS : 0; j < issued; ++j)
+          mbar_wait(&fullb[j % NS], (j / NS) & 1, nullptr, 0);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0 && nblk > 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc = idesc_bf16_f32(128, 128);
@@ -178,41 +176,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, p.status, 19)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(v_smem + (j % kVStages) * kTileBytes);
-        const uint32_t pt = tmem + (j & 1) * 128;
+        const uint32_t pt = tmem + (j % kSBufs) * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: P columns (kk/4)*64 + (kk%4)*8
+        for (int kk = 0; kk < 8; ++kk) {  // keys 16kk..16kk+15: P of column group 16kk / kCols
+          constexpr int kPer = kCols / 16;  // 16-key steps per column group
           const uint32_t boff = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          mma_bf16_ts(tmem + 256, pt + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_kmajor_sw128(vb + boff), idesc,
+          mma_bf16_ts(tmem + kOCol, pt + (kk / kPer) * kCols + (kk % kPer) * 8, sdesc_kmajor_sw128(vb + boff), idesc,
                       (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(o_done);
         mma_commit(&v_empty[j % kVStages]);
         return true;
       };
-      // S_{j+1} is always issued after PV_{j-1}, and the tensor core runs one CTA's MMAs in
-      // issue order, so an S region is rewritten only after the PV that read its P.
-      for (int j = 0; j < nblk && ok; ++j) {
+      auto issue_s = [&](int j) -> bool {
         const int st = j % kKStages;
-        if (!mbar_wait(&k_full[st], (j / kKStages) & 1, p.status, 14)) { ok = false; break; }
+        if (!mbar_wait(&k_full[st], (j / kKStages) & 1, p.status, 14)) return false;
         tc_fence_after();
         const uint32_t kb = smem_u32(k_smem + st * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          mma_bf16(tmem + (j & 1) * 128, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off), idesc,
+          mma_bf16(tmem + (j % kSBufs) * 128, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off), idesc,
                    kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[j & 1]);
+        mma_commit(&s_full[j % kSBufs]);
         mma_commit(&k_empty[st]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        return true;
+      };
+      // Issue order S_0, S_1, then (PV_j, S_{j+2}) for every block j: S_{j+1} runs while the
+      // softmax of block j does, so the softmax warps never wait for scores.  S_{j+2}
+      // reuses the buffer of block j-1, whose PV was issued before it, and the tensor core
+      // runs one CTA's MMAs in issue order, so a buffer is rewritten only after its P is read.
+      ok = ok && issue_s(0) && (nblk < 2 || issue_s(1));
+      for (int j = 0; j < nblk && ok; ++j) {
+        if (!issue_pv(j)) { ok = false; break; }
+        if (j + 2 < nblk && !issue_s(j + 2)) { ok = false; break; }
       }
-      if (ok) issue_pv(nblk - 1);
     }
   } else {
-    // ------------------------------------------------ softmax / epilogue (warps 0-7)
-    // Warp w owns TMEM lanes 32*(w%4)..+31 (one query row per thread) and column half
-    // w/4: S columns [64h, 64h+64) (keys) and O columns [64h, 64h+64) (head dims).
-    const int half = warp >> 2;
+    // ------------------------------------------------ softmax / epilogue (warps 0 .. 4 kCG - 1)
+    // Warp w owns TMEM lanes 32*(w%4)..+31 (one query row per thread) and column group
+    // g = w/4: S columns [g kCols, (g+1) kCols) (keys) and the same O columns (head dims).
+    const int grp = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // query row == TMEM lane
     const int node = qt * NPT + r / G, head = kvh * G + r % G;
     const bool row_ok = node < p.T;
@@ -228,56 +233,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     constexpr float kRescale = 8.f;
     for (int j = 0; j < nblk; ++j) {
       // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
-      const bool w1 = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.status, 16));
-      float sv[64];
+      const bool w1 = __all_sync(0xffffffffu, mbar_wait(&s_full[j % kSBufs], (j / kSBufs) & 1, p.status, 16));
+      float sv[kCols];
       float mpart = -INFINITY;
-      const uint32_t sp = tmem + lane_base + (j & 1) * 128 + half * 64;  // this half's S (then P)
+      const uint32_t sp = tmem + lane_base + (j % kSBufs) * 128 + grp * kCols;  // this group's S (then P)
       if (w1) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) tmem_ld16(sp + c, sv + c);
+        for (int c = 0; c < kCols; c += 16) tmem_ld16(sp + c, sv + c);
         tmem_ld_wait();
         // Raw scores; the softmax scale is folded into the exponent below.  Only blocks
         // that reach past the dense prefix need the admission mask.
-        const int key0 = (kb0 + j) * kKB + half * 64;
+        const int key0 = (kb0 + j) * kKB + grp * kCols;
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if ((kb0 + j + 1) * kKB > dense_len) {
-          uint32_t adm[2];
+          uint32_t adm[kCols / 32];
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
+          for (int g = 0; g < kCols / 32; ++g) {
             const int j0 = key0 + 32 * g;
             uint32_t bits = row_ok ? dense_bits32(j0, dense_len) : 0u;
             if (anc_row) bits |= anc_bits32(anc_row, p.W, j0 - dense_len);
             adm[g] = bits;
           }
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < kCols; ++c) {
             if (!((adm[c >> 5] >> (c & 31)) & 1u)) sv[c] = -INFINITY;
             m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
+          for (int c = 0; c < kCols; ++c) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
         }
         mpart = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sv[c] = -INFINITY;
+        for (int c = 0; c < kCols; ++c) sv[c] = -INFINITY;
       }
-      red_max[j & 1][half][r] = mpart;
-      if (!group_and(w1 && ok)) { ok = false; break; }  // uniform across the 256 threads
-      const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);  // raw-score units
+      red_max[j & 1][grp][r] = mpart;
+      if (!group_and(w1 && ok)) { ok = false; break; }  // uniform across the softmax threads
+      float mx = red_max[j & 1][0][r];  // raw-score units
+#pragma unroll
+      for (int g = 1; g < kCG; ++g) mx = fmaxf(mx, red_max[j & 1][g][r]);
       float alpha = 1.f;
       if ((mx - m_run) * scale2 > kRescale) {  // also taken on the first admitted key (m_run = -inf)
         alpha = ex2_approx((m_run - mx) * scale2);  // 0 when m_run = -inf
         m_run = mx;
       }
-      uint32_t packed[32];
+      uint32_t packed[kCols / 2];
       if (warp_live && m_run != -INFINITY) {
         const float mb = -m_run * scale2;
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < kCols; c += 2) {
           const float p0 = ex2_approx(fmaf(sv[c], scale2, mb)), p1 = ex2_approx(fmaf(sv[c + 1], scale2, mb));
           s4[(c >> 1) & 3] += p0 + p1;
           packed[c >> 1] = pack_bf16x2(p0, p1);
@@ -285,15 +292,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l_part = l_part * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) packed[c] = 0u;
+        for (int c = 0; c < kCols / 2; ++c) packed[c] = 0u;
       }
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O must hold PV of every earlier block before it is rescaled
         ok = mbar_wait(o_done, (j - 1) & 1, p.status, 17) && ok;
         tc_fence_after();
-        const uint32_t oaddr = tmem + lane_base + 256 + half * 64;
+        const uint32_t oaddr = tmem + lane_base + kOCol + grp * kCols;
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < kCols; c += 16) {
           float o[16];
           tmem_ld16(oaddr + c, o);
           tmem_ld_wait();
@@ -302,7 +309,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tmem_st16(oaddr + c, o);
         }
       }
-      tmem_st32(sp, packed);  // P over this half's (already loaded) S columns
+      // P over this group's (already loaded) S columns
+      static_assert(kCols == 32 || kCols == 64, "column groups of 32 or 64");
+      if constexpr (kCols == 64) {
+        tmem_st32(sp, packed);
+      } else {
+        float pf[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pf[i] = __uint_as_float(packed[i]);
+        tmem_st16(sp, pf);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -310,16 +326,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ---------------------------------------------------------------- epilogue
     if (ok && nblk > 0) ok = mbar_wait(o_done, (nblk - 1) & 1, p.status, 18);
     tc_fence_after();
-    red_sum[half][r] = l_part;
+    red_sum[grp][r] = l_part;
     group_sync();
-    const float l_run = red_sum[0][r] + red_sum[1][r];
+    float l_run = red_sum[0][r];
+#pragma unroll
+    for (int g = 1; g < kCG; ++g) l_run += red_sum[g][r];
     const size_t grow = ((size_t)s * p.T + node) * p.Hq + head;  // global query row
-    const uint32_t oaddr = tmem + lane_base + 256 + half * 64;
+    const uint32_t oaddr = tmem + lane_base + kOCol + grp * kCols;
     if (p.nsplit == 1) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + grow * 128 + half * 64);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + grow * 128 + grp * kCols);
 #pragma unroll
-      for (int c = 0; c < 64; c += 16) {
+      for (int c = 0; c < kCols; c += 16) {
         float o[16];
         if (nblk > 0) { tmem_ld16(oaddr + c, o); tmem_ld_wait(); }
         else {
@@ -337,9 +355,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     } else {
       const size_t nrows = (size_t)p.b * p.T * p.Hq;
-      float* op = p.o_part + ((size_t)split * nrows + grow) * 128 + half * 64;
+      float* op = p.o_part + ((size_t)split * nrows + grow) * 128 + grp * kCols;
 #pragma unroll
-      for (int c = 0; c < 64; c += 16) {
+      for (int c = 0; c < kCols; c += 16) {
         float o[16];
         if (nblk > 0) { tmem_ld16(oaddr + c, o); tmem_ld_wait(); }
         else {
@@ -351,7 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int i = 0; i < 16; i += 4)
             *reinterpret_cast<float4*>(op + c + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
       }
-      if (row_ok && half == 0) {
+      if (row_ok && grp == 0) {
         p.ml_part[((size_t)split * nrows + grow) * 2] = m_run * scale2;  // log2 units for the combine
         p.ml_part[((size_t)split * nrows + grow) * 2 + 1] = l_run;
       }
@@ -360,7 +378,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
