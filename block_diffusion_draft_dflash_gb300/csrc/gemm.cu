@@ -305,18 +305,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           run_tt = tt;
         }
         argmax_tile(taddr, BN, n, n_ok, run, lane);
+      } else if constexpr (MODE == kGemmPartial) {
+        // this segment's accumulator -> its slot, [token][feature row], plain stores; 64
+        // columns per TMEM round trip, then 16 at a time for the rest
+        float* dst = p.part + ((size_t)blockIdx.x * p.max_seg + si) * BN * 128 + q * 32 + lane;
+        int c0 = 0;
+        for (; c0 + 64 <= BN; c0 += 64) {
+          float v[64];
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) tmem_ld16(taddr + c0 + c, v + c);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 64; ++j) dst[(size_t)(c0 + j) * 128] = v[j];
+        }
+        for (; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[(size_t)(c0 + j) * 128] = v[j];
+        }
       } else
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
         tmem_ld16(taddr + c0, v);
         tmem_ld_wait();
         const int t0 = tt * BN + c0;
-        if constexpr (MODE == kGemmPartial) {
-          // this segment's accumulator -> its slot, [token][feature row], plain stores
-          float* dst = p.part + (((size_t)blockIdx.x * p.max_seg + si) * BN + c0) * 128 + q * 32 + lane;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) dst[j * 128] = v[j];
-        } else if constexpr (MODE == kGemmAtomicAdd) {
+        if constexpr (MODE == kGemmAtomicAdd) {
           if (n_ok)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
