@@ -83,9 +83,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* v_full = k_empty + kKStages;
   uint64_t* v_empty = v_full + kVStages;
   uint64_t* s_full = v_empty + kVStages;
+  // One P barrier and one PV barrier per S buffer: each is reused only every third block,
+  // which no waiter can fall a whole phase behind (a parity wait cannot tell phases two
+  // apart).  Softmax of block j runs only after S_j, and S_j follows PV_{j-2} on the tensor
+  // core, so at most PV_{j-1} is still pending when block j's softmax looks at O.
   uint64_t* p_full = s_full + kSBufs;
-  uint64_t* o_done = p_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  uint64_t* o_done = p_full + kSBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + kSBufs);
   __shared__ float red_max[2][kCG][128];  // [block parity][column group][row]
   __shared__ float red_sum[kCG][128];
 
@@ -95,8 +99,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = 0; i < kKStages; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
     for (int i = 0; i < kSBufs; ++i) mbar_init(&s_full[i], 1);
-    mbar_init(p_full, kSoftThreads);
-    mbar_init(o_done, 1);
+    for (int i = 0; i < kSBufs; ++i) { mbar_init(&p_full[i], kSoftThreads); mbar_init(&o_done[i], 1); }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = mbar_wait(q_full, 0, p.status, 12);
       tc_fence_after();
       auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(p_full, j & 1, p.status, 13)) return false;
+        if (!mbar_wait(&p_full[j % kSBufs], (j / kSBufs) & 1, p.status, 13)) return false;
         if (!mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, p.status, 19)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(v_smem + (j % kVStages) * kTileBytes);
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mma_bf16_ts(tmem + kOCol, pt + (kk / kPer) * kCols + (kk % kPer) * 8, sdesc_kmajor_sw128(vb + boff), idesc,
                       (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(o_done);
+        mma_commit(&o_done[j % kSBufs]);
         mma_commit(&v_empty[j % kVStages]);
         return true;
       };
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O must hold PV of every earlier block before it is rescaled
-        ok = mbar_wait(o_done, (j - 1) & 1, p.status, 17) && ok;
+        ok = mbar_wait(&o_done[(j - 1) % kSBufs], ((j - 1) / kSBufs) & 1, p.status, 17) && ok;
         tc_fence_after();
         const uint32_t oaddr = tmem + lane_base + kOCol + grp * kCols;
 #pragma unroll
@@ -321,10 +324,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[j % kSBufs]);
     }
     // ---------------------------------------------------------------- epilogue
-    if (ok && nblk > 0) ok = mbar_wait(o_done, (nblk - 1) & 1, p.status, 18);
+    if (ok && nblk > 0) ok = mbar_wait(&o_done[(nblk - 1) % kSBufs], ((nblk - 1) / kSBufs) & 1, p.status, 18);
     tc_fence_after();
     red_sum[grp][r] = l_part;
     group_sync();

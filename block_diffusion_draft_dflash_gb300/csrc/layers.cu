@@ -249,12 +249,13 @@ __global__ void __launch_bounds__(1024) res_norm_kernel(ResNormArgs a) {
   }
 }
 
-// grid: (ceil(F / 1024), rows); block 256; 4 features per thread.
+// grid: (rows, ceil(F / 1024)) (rows in x: y is limited to 65535); block 256; 4 features
+// per thread.
 __global__ void __launch_bounds__(256) swiglu_partial_kernel(SwigluArgs a) {
   pdl_wait();
   pdl_trigger();
-  const int t = blockIdx.y;
-  const int f = (blockIdx.x * 256 + threadIdx.x) * 4;
+  const int t = blockIdx.x;
+  const int f = (blockIdx.y * 256 + threadIdx.x) * 4;
   if (f >= a.F) return;
   const float4 g = partial_sum4(a.pv, f >> 7, t, f & 127);
   const int fu = a.F + f;
@@ -350,15 +351,15 @@ __global__ void __launch_bounds__(1024) lse_from_stats_kernel(const float2* __re
   }
 }
 
-// x[r][i] -= lse[r] over a grid of (row, chunk) blocks.
+// x[r][i] -= lse[r] over a grid of (row, chunk) blocks (rows in x).
 __global__ void __launch_bounds__(256) sub_lse_kernel(float* __restrict__ x, int V, const float* __restrict__ lse) {
   pdl_wait();
   pdl_trigger();
-  const int r = blockIdx.y;
+  const int r = blockIdx.x;
   const float l = lse[r];
   float* row = x + (size_t)r * V;
-  const int chunk = (V + gridDim.x - 1) / gridDim.x;
-  const int i0 = blockIdx.x * chunk, i1 = min(V, i0 + chunk);
+  const int chunk = (V + gridDim.y - 1) / gridDim.y;
+  const int i0 = blockIdx.y * chunk, i1 = min(V, i0 + chunk);
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) row[i] -= l;
 }
 
@@ -427,7 +428,7 @@ int launch_res_norm(const ResNormArgs& a, cudaStream_t st) {
 int launch_swiglu_partial(const SwigluArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return DF_OK;
   DF_TRACE("swiglu", st);
-  launch_k(swiglu_partial_kernel, dim3(dim3((a.F + 1023) / 1024, a.rows)), dim3(256), 0, st, a);
+  launch_k(swiglu_partial_kernel, dim3(dim3(a.rows, (a.F + 1023) / 1024)), dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st) {
@@ -438,7 +439,7 @@ int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, 
                                  cudaStream_t st) {
   DF_TRACE("logsoftmax", st);
   launch_k(lse_from_stats_kernel, dim3(rows), dim3(1024), 0, st, reinterpret_cast<const float2*>(stats), n_stats, lse);
-  launch_k(sub_lse_kernel, dim3(dim3(32, rows)), dim3(256), 0, st, x, V, lse);
+  launch_k(sub_lse_kernel, dim3(dim3(rows, 32)), dim3(256), 0, st, x, V, lse);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st) {

@@ -89,3 +89,15 @@ def test_chain_tree_equals_causal_block():
             ref = model.attend(q[0, i, h], k[0, h // 4, :N + i + 1].astype(np.float64),
                                v[0, h // 4, :N + i + 1].astype(np.float64), 1 / np.sqrt(128))
             assert np.abs(got[0, i, h] - ref).max() <= 2e-2 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("b", [16])
+def test_tree_attention_many_waves(b):
+    # b*Hkv*ceil(T/32) = 1152 CTAs: several waves of CTAs per SM, no split of the key range
+    T, Hq, Hkv, cap = 257, 32, 8, 2048
+    N = [900 + 37 * s for s in range(b)]
+    q, k, v, trees, anc = _case(13, b, T, N, Hq, Hkv, cap, D=15, V=200)
+    got = _run_gpu(q, k, v, N, anc)
+    for s in (0, b // 2, b - 1):
+        rows = [0, 1, 128, 200, T - 1]
+        rel_close(got[s, rows], _oracle(q, k, v, N, trees[s], s, rows))
