@@ -420,7 +420,10 @@ int launch_res_norm(const ResNormArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return DF_OK;
   if (a.d % 128 || a.d > 8192) return DF_ERR_SHAPE;
   DF_TRACE("residual_norm", st);
-  int threads = a.d / 4 > 1024 ? 1024 : a.d / 4;
+  // two float4 per thread when the row is long enough: 512-thread blocks leave room for two
+  // of them beside a GEMM CTA, so every row's block is resident before the GEMM ends
+  int threads = a.d >= 2048 ? a.d / 8 : a.d / 4;
+  if (threads > 1024) threads = 1024;
   threads = (threads + 31) / 32 * 32;
   launch_k(res_norm_kernel, dim3(a.rows), dim3(threads), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
