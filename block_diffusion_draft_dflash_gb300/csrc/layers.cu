@@ -132,9 +132,12 @@ __global__ void __launch_bounds__(64) rope_table_kernel(QkRopeArgs a, float2* __
   table[(size_t)r * 64 + i] = make_float2(cs, sn);
 }
 
-// grid: (rows, ceil((Hq + 2 Hkv) / 8)); block 256: warp w handles head blockIdx.y * 8 + w.
+// grid: (rows, ceil((Hq + 2 Hkv) / (8 KH))); block 256: warp w handles heads
+// blockIdx.y * 8 KH + w + 8 i, i < KH.
 // Lane l owns elements l, l+32, l+64, l+96 of a 128-wide head, so both rotary pairs
 // (i, i+64) of the lane stay in the lane.
+constexpr int kQkHeads = 3;
+template <int KH>  // heads per warp
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -152,17 +155,26 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(QkRopeArgs a) {
   const float2 cs0 = a.rope[(size_t)r * 64 + lane], cs1 = a.rope[(size_t)r * 64 + lane + 32];
   const float c0 = cs0.x, s0 = cs0.y, c1 = cs1.x, s1 = cs1.y;
   const int nh = a.Hq + 2 * a.Hkv;
-  for (int h = blockIdx.y * nw + warp; h < nh && h < (int)(blockIdx.y + 1) * nw; h += nw) {
-    if (!write_q && h < a.Hq) continue;
-    float v0, v1, v2, v3;
+  // this warp's heads: h0 + i * nw, i < KH; every head's loads are issued before any is used
+  const int h0 = blockIdx.y * nw * KH + warp;
+  float v[KH][4];
+#pragma unroll
+  for (int i = 0; i < KH; ++i) {
+    const int h = h0 + i * nw;
+    v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+    if (h >= nh || (!write_q && h < a.Hq)) continue;
     if (a.pv.part) {
-      float vv[4];
-      partial_sum_strided4(a.pv, h, r, lane, vv);
-      v0 = vv[0]; v1 = vv[1]; v2 = vv[2]; v3 = vv[3];
+      partial_sum_strided4(a.pv, h, r, lane, v[i]);
     } else {
       const float* x = row + h * HD;
-      v0 = x[lane]; v1 = x[lane + 32]; v2 = x[lane + 64]; v3 = x[lane + 96];
+      v[i][0] = x[lane]; v[i][1] = x[lane + 32]; v[i][2] = x[lane + 64]; v[i][3] = x[lane + 96];
     }
+  }
+#pragma unroll
+  for (int i = 0; i < KH; ++i) {
+    const int h = h0 + i * nw;
+    if (h >= nh || (!write_q && h < a.Hq)) continue;
+    float v0 = v[i][0], v1 = v[i][1], v2 = v[i][2], v3 = v[i][3];
     if (h < a.Hq + a.Hkv) {
       const df_bf16* gain = h < a.Hq ? a.q_norm : a.k_norm;
       const float ms = warp_sum(v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3) / HD;
@@ -405,7 +417,10 @@ int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st) {
   if (rows == 0) return DF_OK;
   if (!a.rope) return DF_ERR_ARG;
   DF_TRACE("qk_norm_rope", st);
-  launch_k(qk_norm_rope_kernel, dim3(dim3(rows, (a.Hq + 2 * a.Hkv + 7) / 8)), dim3(256), 0, st, a);
+  // kQkHeads heads per warp: one row's 48 heads in 2 blocks of 8 warps, so the whole grid is
+  // resident beside the q/k/v GEMM
+  launch_k(qk_norm_rope_kernel<kQkHeads>, dim3(dim3(rows, (a.Hq + 2 * a.Hkv + 8 * kQkHeads - 1) / (8 * kQkHeads))),
+           dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st) {
