@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // One warp per query row: out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
+constexpr int kCombineFast = 4;  // splits merged from one round of loads
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ o_part,
                                                            const float* __restrict__ ml_part, int nsplit,
                                                            long long nrows, df_bf16* __restrict__ out) {
@@ -396,17 +397,40 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= nrows) return;
-  float M = -INFINITY;
-  for (int j = 0; j < nsplit; ++j) M = fmaxf(M, ml_part[((size_t)j * nrows + row) * 2]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  for (int j = 0; j < nsplit; ++j) {
-    const float m = ml_part[((size_t)j * nrows + row) * 2];
-    if (m == -INFINITY) continue;
-    const float w = exp2f(m - M);
-    L += w * ml_part[((size_t)j * nrows + row) * 2 + 1];
-    const float4 o = reinterpret_cast<const float4*>(o_part + ((size_t)j * nrows + row) * 128)[lane];
-    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+  if (nsplit <= kCombineFast) {
+    // every split's (max, sum) and O slice in one round of (predicated) loads
+    float m[kCombineFast], l[kCombineFast];
+    float4 o[kCombineFast];
+#pragma unroll
+    for (int j = 0; j < kCombineFast; ++j) {
+      const bool on = j < nsplit;
+      const size_t at = (size_t)j * nrows + row;
+      m[j] = on ? ml_part[at * 2] : -INFINITY;
+      l[j] = on ? ml_part[at * 2 + 1] : 0.f;
+      o[j] = on ? reinterpret_cast<const float4*>(o_part + at * 128)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float M = m[0];
+#pragma unroll
+    for (int j = 1; j < kCombineFast; ++j) M = fmaxf(M, m[j]);
+#pragma unroll
+    for (int j = 0; j < kCombineFast; ++j) {
+      const float w = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M);
+      L += w * l[j];
+      acc.x += w * o[j].x; acc.y += w * o[j].y; acc.z += w * o[j].z; acc.w += w * o[j].w;
+    }
+  } else {
+    float M = -INFINITY;
+    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, ml_part[((size_t)j * nrows + row) * 2]);
+    for (int j = 0; j < nsplit; ++j) {
+      const float m = ml_part[((size_t)j * nrows + row) * 2];
+      if (m == -INFINITY) continue;
+      const float w = exp2f(m - M);
+      L += w * ml_part[((size_t)j * nrows + row) * 2 + 1];
+      const float4 o = reinterpret_cast<const float4*>(o_part + ((size_t)j * nrows + row) * 128)[lane];
+      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   uint2 r;
