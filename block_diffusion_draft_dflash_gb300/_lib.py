@@ -62,6 +62,9 @@ _SIGS = {
     "dflash_target_tree_forward": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int] + [C.c_void_p] * 5 +
                                    [C.c_int] + [C.c_void_p] * 4 + [C.c_size_t, C.c_void_p]),
     "dflash_linear_workspace_size": (C.c_size_t, []),
+    "dflash_linear_argmax_workspace_size": (C.c_size_t, [C.c_int]),
+    "dflash_linear_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                       C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_linear": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int,
                       C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_draft_block_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
@@ -232,6 +235,19 @@ def linear(X, W, out, accumulate=False, ws: Workspace = None):
     N = W.shape[0]
     _check("dflash_linear", load().dflash_linear(_p(X), _p(W), M, N, K, _p(out), int(accumulate), ws.ptr,
                                                  ws.nbytes, _stream()))
+    return ws
+
+
+def linear_argmax(X, W, out, ws: Workspace = None):
+    """out[t] = argmax_n (X W^T)[t][n] (lowest n on ties); X [M][K] bf16, W [N][K] bf16, out [M] int32."""
+    _dev(X, torch.bfloat16, "X")
+    _dev(W, torch.bfloat16, "W")
+    _dev(out, torch.int32, "out")
+    M, K = X.shape
+    N = W.shape[0]
+    ws = ws or Workspace(load().dflash_linear_argmax_workspace_size(M), X.device)
+    _check("dflash_linear_argmax", load().dflash_linear_argmax(_p(X), _p(W), M, N, K, _p(out), ws.ptr, ws.nbytes,
+                                                               _stream()))
     return ws
 
 

@@ -508,6 +508,31 @@ int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, 
 extern "C" {
 size_t dflash_linear_workspace_size(void) { return 256; }
 
+size_t dflash_linear_argmax_workspace_size(int M) {
+  Carver cv(nullptr);
+  cv.take<unsigned long long>(M > 0 ? (size_t)M : 1);
+  return cv.off;
+}
+
+int dflash_linear_argmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, int32_t* out, void* ws,
+                         size_t ws_bytes, df_stream stream) {
+  if (M < 0 || N <= 0 || K <= 0) return DF_ERR_ARG;
+  if (K % 64) return DF_ERR_SHAPE;
+  if (M == 0) return DF_OK;
+  if (!X || !W || !out) return DF_ERR_ARG;
+  if (!al16(X) || !al16(W)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < dflash_linear_argmax_workspace_size(M)) return DF_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  Carver cv(ws);
+  unsigned long long* keys = cv.take<unsigned long long>((size_t)M);
+  if (cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * M, st) != cudaSuccess) return DF_ERR_CUDA;
+  GemmDesc g{};
+  g.X = X; g.W = W; g.M = M; g.N = N; g.K = K; g.ldx = K; g.ldw = K;
+  g.mode = kGemmArgmax; g.amax = keys; g.status = status_of(ws);
+  DF_TRY(launch_gemm(g, st));
+  return launch_argmax_finalize(keys, M, out, st);
+}
+
 int dflash_linear(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out, int accumulate, void* ws,
                   size_t ws_bytes, df_stream stream) {
   if (M < 0 || N < 0 || K <= 0) return DF_ERR_ARG;

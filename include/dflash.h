@@ -274,6 +274,14 @@ size_t dflash_linear_workspace_size(void);
 int dflash_linear(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out, int accumulate,
                   void* ws, size_t ws_bytes, df_stream stream);
 
+/* dflash_linear_argmax -- out[t] = argmax_n (X W^T)[t][n], lowest n among equal maxima: the
+ * target's LM head of dflash_target_tree_forward (the logits are never written).
+ *   X [M][K] bf16, W [N][K] bf16, K a multiple of 64, out [M] int32.
+ *   Workspace: dflash_linear_argmax_workspace_size(M) bytes (per-row keys + status). */
+size_t dflash_linear_argmax_workspace_size(int M);
+int dflash_linear_argmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, int32_t* out,
+                         void* ws, size_t ws_bytes, df_stream stream);
+
 /* ------------------------------------------------------------------------------------
  * Status and device queries.
  * ------------------------------------------------------------------------------------ */

@@ -156,3 +156,34 @@ def test_speculative_loop_is_lossless(models):
         clear = (top2[:, 1] - top2[:, 0]) > 0.02 * np.abs(ologits).max()
         bad = np.nonzero(clear & (pred != got))[0]
         assert len(bad) == 0, (s, bad, pred[bad], got[bad])
+
+
+def test_target_tree_forward_wide_rows():
+    # d = 2048: the residual + RMSNorm consumer runs two float4 per thread (the d = 4096 layout)
+    shape = synth.ModelShape(1, 2048, 16, 4, 128, 2048, 1024, feat_layers=(1,), block_size=4)
+    tw = synth.target_weights(shape, 2003)
+    tm = engine.DeviceModel.from_host(tw)
+    b, B, N, cap = 1, 12, [45], 128
+    rng = np.random.default_rng(3)
+    kc = synth.normal(7, "wk", (1, b, 4, cap, 128))
+    vc = synth.normal(7, "wv", (1, b, 4, cap, 128))
+    kc[:, 0, :, N[0]:] = 0
+    vc[:, 0, :, N[0]:] = 0
+    t = ddtree.build_tree(ddtree.log_softmax(rng.normal(0, 2, size=(3, shape.vocab))), B)
+    t["tok"][0] = 5
+    T = B + 1
+    k = bf16_dev(kc)
+    v = bf16_dev(vc).transpose(-1, -2).contiguous()
+    st = lambda key: torch.from_numpy(t[key][None].astype(np.int32)).cuda()
+    anc = torch.from_numpy(ddtree.ancestor_mask(t["parent"])[None].view(np.int32)).cuda()
+    clen = torch.tensor(N, dtype=torch.int32, device="cuda")
+    choice = torch.zeros(b, T, dtype=torch.int32, device="cuda")
+    feat = torch.zeros(b, T, shape.d_model, dtype=torch.bfloat16, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T))
+    _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k, v, clen, choice, feat, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    cache = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), 0)
+    och, ofeat, ologits = step.target_tree_forward(tw, t["tok"], t["parent"], t["depth"], cache, N[0])
+    rel_close(to_np(feat[0]), ofeat)
+    _clear_choice(choice[0].cpu().numpy(), och, ologits)
