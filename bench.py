@@ -390,8 +390,15 @@ def run_gpu(a, rank, world, local_rank):
         traffic = round(GEMM_TRAFFIC["bytes_per_layer"] / 4)  # per launch, averaged over the four shapes
     g_ms = kern["gemm"]["ms_per_step"]
     g_bytes, g_flops = gemm_algorithmic(b, B)
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": traffic,
+    # the binding resource: HBM while the weights dominate (b = 1: 257 flop per byte, just
+    # under the ridge), the tensor cores once b * 257 token rows share each weight byte
+    tensor_bound = t_flops / (tc_sust * 1e12) > t_bytes / (hbm * 1e9)
+    if tensor_bound:
+        achieved = t_flops / (t_ms * 1e-3) / 1e12 if t_ms else 0.0
+    peak_r = tc_sust if tensor_bound else hbm
+    roof = {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(achieved, 1), "peak": peak_r,
+            "unit": "TFLOP/s" if tensor_bound else "GB/s",
+            "frac": round(achieved / peak_r, 4), "traffic": traffic,
             "kernel": "gemm_bf16_tc_kernel (partial-tile epilogue): the 4 projection launches of each of the "
                       "36 target layers",
             "algorithmic_bytes_per_launch": round(t_bytes / t_launch) if t_launch else None,
