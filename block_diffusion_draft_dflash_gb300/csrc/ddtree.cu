@@ -383,7 +383,7 @@ DF_DEV unsigned long long heap_key(float s, int depth, int parent, int rank) {
 
 // One CTA per sequence; warp 0 runs the best-first selection.  The live candidates (at most
 // B + 1) sit in the warp's registers, NREG per lane, densely packed: candidate c lives in
-// lane c % 32, register c / 32.  Each pop takes the lane maxima, a 5-step shuffle maximum
+// lane c % 32, register c / 32.  Each pop takes the lane maxima, a warp maximum (two redux steps)
 // and a ballot for the owner; the last candidate fills the hole; the successors (first
 // child, next sibling) are appended.  Keys are unique, so the maximum is unique.
 template <int NREG>
@@ -432,12 +432,12 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
 #pragma unroll
       for (int i = 1; i < NREG; ++i)
         if (cand[i] > best) { best = cand[i]; bi = i; }
-      unsigned long long top = best;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long x = __shfl_xor_sync(0xffffffffu, top, o);
-        top = x > top ? x : top;
-      }
+      // warp maximum of the 64-bit lane maxima: the high words with one redux, then the low
+      // words among the lanes that hold the top high word
+      const uint32_t top_hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+      const bool at_hi = (uint32_t)(best >> 32) == top_hi;
+      const uint32_t top_lo = __reduce_max_sync(0xffffffffu, at_hi ? (uint32_t)best : 0u);
+      const unsigned long long top = ((unsigned long long)top_hi << 32) | top_lo;
       const int owner = __ffs(__ballot_sync(0xffffffffu, best == top)) - 1;
       const int hole = __shfl_sync(0xffffffffu, bi, owner);
       // the last candidate moves into the hole (or the hole is the last one)
