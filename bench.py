@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import tempfile
 import subprocess
 import sys
 import time
@@ -325,8 +326,8 @@ def run_gpu(a, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = Clocks(os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp",
-                                 f"clocks_rank{rank}.csv"))
+    # the nvidia-smi samples go to $BENCH_OUT_DIR (default: the temp directory)
+    clocks = Clocks(os.path.join(os.environ.get("BENCH_OUT_DIR", tempfile.gettempdir()), f"clocks_rank{rank}.csv"))
     n_acc_before = None
     with clocks:
         time.sleep(0.3)
