@@ -113,10 +113,11 @@ def test_draft_block_matches_oracle(models, b, ctx0, n_new):
                 rel_close(gv[l], ctx.v[l][ctx0[s]:n1].transpose(1, 2, 0))
 
 
-def test_speculative_loop_is_lossless(models):
+@pytest.mark.parametrize("B", [16, DS.block_size - 1])  # a tree, and a budget of D nodes (the DFlash chain size)
+def test_speculative_loop_is_lossless(models, B):
     """Spec output equals the target's greedy choice at every position whose margin is clear."""
     tw, dw, tm, dm = models
-    b, P, B, n_gen, cap = 2, 40, 16, 48, 512
+    b, P, n_gen, cap = 2, 40, 48, 512
     prompt = synth.uniform_ints(2001, "prompt", (b, P), 0, TS.vocab)
     ref = [step.greedy_generate(tw, prompt[s], n_gen + 16, cap) for s in range(b)]
     dec = engine.SpecDecoder(tm, dm, b, B, cap, prompt_len=P)
