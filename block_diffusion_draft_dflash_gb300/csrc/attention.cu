@@ -36,8 +36,8 @@ constexpr int kAttnThreads = kSoftThreads + 96;  // + Q/K TMA warp, MMA warp, V 
 constexpr int kKB = 128;     // keys per block
 constexpr int kSBufs = 3;                    // S/P buffers in TMEM (128 columns each)
 constexpr uint32_t kOCol = kSBufs * 128;     // O accumulator columns [384, 512)
-constexpr int kKStages = 3;  // K tiles are free again once S = Q K^T has run
-constexpr int kVStages = 2;  // V tiles are free again once O += P V has run
+constexpr int kKStages = 2;  // K tiles are free again once S = Q K^T has run
+constexpr int kVStages = 3;  // V tiles are free again once O += P V has run (the longer wait)
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128x128 bf16 tile = 2 swizzled slabs
 
 DF_DEV int floordiv32(int t) { return t >= 0 ? (t >> 5) : -((-t + 31) >> 5); }
