@@ -226,6 +226,21 @@ def gemm_src_hash():
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(x, world, device="cpu"):
+    """The slowest rank's time (all ranks take part; a no-op for one process)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, b, ms_per_step):
+    """Whole-job spec steps/s: every rank runs b sequences (weak scaling, replicas)."""
+    return world * b * 1000.0 / ms_per_step
+
+
 def traced_breakdown(dec, n_steps):
     """Per-class device time of eager steps, from the library's CUDA-event tracing."""
     import torch
@@ -336,11 +351,7 @@ def run_gpu(a, rank, world, local_rank):
             g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / a.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / a.steps, world, dev)
     st = dec.status()
     assert st == 0, f"device status {st}"
 
@@ -364,11 +375,7 @@ def run_gpu(a, rank, world, local_rank):
         torch.cuda.current_stream().synchronize()
         emitted += int(h_n.sum()) + b
         h_in.copy_(h_tok[torch.arange(b), h_n.long()])
-    e2e_s = (time.perf_counter() - t0) / a.steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / a.steps, world, dev)
 
     # live per-kernel breakdown (CUDA events around every library launch, eager steps)
     kern, kern_shapes = traced_breakdown(dec, 3)
@@ -525,7 +532,7 @@ def main():
     if rank != 0:
         return
     b = a.batch
-    value = world * b * 1000.0 / r["ms"]
+    value = job_value(world, b, r["ms"])
     e2e = world * b / r["e2e_s"]
     cpu = None
     if not a.no_cpu_baseline and world == 1:
