@@ -174,9 +174,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t qa = smem_u32(q_smem);
       bool ok = mbar_wait(q_full, 0, p.status, 12);
       tc_fence_after();
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(&p_full[j % kSBufs], (j / kSBufs) & 1, p.status, 13)) return false;
-        if (!mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, p.status, 19)) return false;
+      // operands already present: issue only
+      auto issue_pv = [&](int j) {
         tc_fence_after();
         const uint32_t vb = smem_u32(v_smem + (j % kVStages) * kTileBytes);
         const uint32_t pt = tmem + (j % kSBufs) * 128;
@@ -189,12 +188,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit(&o_done[j % kSBufs]);
         mma_commit(&v_empty[j % kVStages]);
-        return true;
       };
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kKStages;
-        if (!mbar_wait(&k_full[st], (j / kKStages) & 1, p.status, 14)) return false;
+      auto issue_s = [&](int j) {
         tc_fence_after();
+        const int st = j % kKStages;
         const uint32_t kb = smem_u32(k_smem + st * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -204,16 +201,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit(&s_full[j % kSBufs]);
         mma_commit(&k_empty[st]);
-        return true;
       };
-      // Issue order S_0, S_1, then (PV_j, S_{j+2}) for every block j: S_{j+1} runs while the
-      // softmax of block j does, so the softmax warps never wait for scores.  S_{j+2}
-      // reuses the buffer of block j-1, whose PV was issued before it, and the tensor core
-      // runs one CTA's MMAs in issue order, so a buffer is rewritten only after its P is read.
-      ok = ok && issue_s(0) && (nblk < 2 || issue_s(1));
-      for (int j = 0; j < nblk && ok; ++j) {
-        if (!issue_pv(j)) { ok = false; break; }
-        if (j + 2 < nblk && !issue_s(j + 2)) { ok = false; break; }
+      // Whichever product has its operands goes next, S first (its scores gate the next
+      // softmax block), so a late K tile never holds up a ready PV or the other way round.
+      // S_k reuses the buffer of block k - 3, so it waits until PV_{k-3} has been issued:
+      // the tensor core runs one CTA's MMAs in issue order, so a buffer is rewritten only
+      // after its P was read, and S_k complete implies every PV up to k - 3 complete.
+      int s_next = 0, pv_next = 0, idle = 0;
+      uint64_t t_last = globaltimer();
+      while (ok && pv_next < nblk) {
+        if (s_next < nblk && s_next - pv_next < kSBufs &&
+            mbar_test_wait(&k_full[s_next % kKStages], (s_next / kKStages) & 1)) {
+          issue_s(s_next++);
+        } else if (pv_next < s_next && mbar_test_wait(&p_full[pv_next % kSBufs], (pv_next / kSBufs) & 1) &&
+                   mbar_test_wait(&v_full[pv_next % kVStages], (pv_next / kVStages) & 1)) {
+          issue_pv(pv_next++);
+        } else {
+          if ((++idle & 1023) == 0) {  // bounded: give up after kWaitLimitNs without progress
+            if (globaltimer() - t_last > kWaitLimitNs) { set_status(p.status, DF_ERR_TIMEOUT, 13); ok = false; }
+            else if (*(volatile int*)p.status == DF_ERR_TIMEOUT) ok = false;
+          }
+          continue;
+        }
+        idle = 0;
+        t_last = globaltimer();
       }
     }
   } else {

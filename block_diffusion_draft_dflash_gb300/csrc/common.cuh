@@ -60,6 +60,14 @@ DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
+// Non-blocking probe of the same phase (try_wait may suspend the thread for a while).
+DF_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
 // Bounded wait for phase `parity` of `bar` to complete.  Returns false (and records a
 // timeout) if it does not complete within kWaitLimitNs.
 DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int where) {
