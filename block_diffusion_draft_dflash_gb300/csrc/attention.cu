@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         } else {
           if ((++idle & 1023) == 0) {  // bounded: give up after kWaitLimitNs without progress
             if (globaltimer() - t_last > kWaitLimitNs) { set_status(p.status, DF_ERR_TIMEOUT, 13); ok = false; }
-            else if (*(volatile int*)p.status == DF_ERR_TIMEOUT) ok = false;
+            else if (p.status && *(volatile int*)p.status == DF_ERR_TIMEOUT) ok = false;
           }
           continue;
         }
