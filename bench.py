@@ -212,7 +212,7 @@ def gemm_algorithmic(b, B, nd_ctx_rows=16):
 # target tree forward (B=256): the four projection launches of one layer read + wrote
 # 54.01 (q/k/v), 35.81 (o), 211.55 (gate/up) and 111.42 (down) MB.  Valid only for the GEMM
 # sources it was taken on (their hash below); any other build reports traffic null.
-GEMM_TRAFFIC = {"src_sha256_16": "e90101e02dc99c38", "bytes_per_layer": 412795904,
+GEMM_TRAFFIC = {"src_sha256_16": "a064e4de381fa665", "bytes_per_layer": 412926720,
                 "capture": "profiles/gemm_attention_ncu_full_qwen3_8b_2layer_B256.md"}
 GEMM_SOURCES = ("gemm.cu", "common.cuh", "partials.cuh")
 
