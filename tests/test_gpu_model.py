@@ -188,3 +188,41 @@ def test_target_tree_forward_wide_rows():
     och, ofeat, ologits = step.target_tree_forward(tw, t["tok"], t["parent"], t["depth"], cache, N[0])
     rel_close(to_np(feat[0]), ofeat)
     _clear_choice(choice[0].cpu().numpy(), och, ologits)
+
+
+def test_target_tree_forward_qwen3_width():
+    # One target layer at Qwen3-8B width over a 256-node tree: the four projection GEMMs run
+    # at exactly the shapes and launch configuration of the benchmarked step (257 rows;
+    # N x K = 6144 x 4096, 4096 x 4096, 24576 x 4096, 4096 x 12288; one CTA per SM,
+    # stream-K partial tiles), and their consumers sum those partials.  Small vocabulary and
+    # context keep the oracle to seconds.
+    shape = synth.ModelShape(1, 4096, 32, 8, 128, 12288, 2048, feat_layers=(1,), block_size=16)
+    tw = synth.target_weights(shape, 2005)
+    tm = engine.DeviceModel.from_host(tw)
+    b, B, N, cap = 1, 256, [64], 384
+    rng = np.random.default_rng(5)
+    t = ddtree.build_tree(ddtree.log_softmax(rng.normal(0, 2, size=(shape.block_size - 1, shape.vocab))), B)
+    t["tok"][0] = 5
+    T = B + 1
+    kc = synth.normal(7, "fk", (1, b, shape.n_kv_heads, cap, 128))
+    vc = synth.normal(7, "fv", (1, b, shape.n_kv_heads, cap, 128))
+    kc[:, 0, :, N[0]:] = 0
+    vc[:, 0, :, N[0]:] = 0
+    k = bf16_dev(kc)
+    v = bf16_dev(vc).transpose(-1, -2).contiguous()
+    st = lambda key: torch.from_numpy(t[key][None].astype(np.int32)).cuda()
+    anc = torch.from_numpy(ddtree.ancestor_mask(t["parent"])[None].view(np.int32)).cuda()
+    clen = torch.tensor(N, dtype=torch.int32, device="cuda")
+    choice = torch.zeros(b, T, dtype=torch.int32, device="cuda")
+    feat = torch.zeros(b, T, shape.d_model, dtype=torch.bfloat16, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T))
+    _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k, v, clen, choice, feat, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    cache = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), 0)
+    och, ofeat, ologits = step.target_tree_forward(tw, t["tok"], t["parent"], t["depth"], cache, N[0])
+    rel_close(to_np(feat[0]), ofeat)
+    _clear_choice(choice[0].cpu().numpy(), och, ologits)
+    # the tree rows' K/V went to slots N .. N + B of the cache
+    ok = to_np(k)[0, 0][:, N[0]:N[0] + T].transpose(1, 0, 2)
+    rel_close(ok, cache.k[0][N[0]:N[0] + T])
