@@ -36,7 +36,7 @@ def _clear_choice(gpu_choice, o_choice, o_logits, frac=0.02):
 
 
 @pytest.mark.parametrize("b,B,Ns", [(2, 20, [37, 150]), (1, 64, [300]), (3, 0, [5, 0, 77]),
-                                    (1, 256, [200]), (2, 131, [37, 350])])
+                                    (1, 256, [200]), (2, 131, [37, 350]), (2, 134, [60, 300])])
 def test_target_tree_forward_matches_oracle(models, b, B, Ns):
     tw, _, tm, _ = models
     T, cap = B + 1, 512
