@@ -200,3 +200,64 @@ def test_target_forward_matches_torch_library_formulation():
     np.testing.assert_allclose(feats, rf, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(logits, rl, rtol=1e-10, atol=1e-12)
     np.testing.assert_array_equal(ch, np.argmax(rl, -1))
+
+
+def _torch_reference_draft(dw, feat, bonus):
+    """The drafter block from torch library routines, all context rows at once (positions
+    0 .. n-1, block rows n .. n+L-1): F.rms_norm, complex-valued rotation at explicit
+    positions, F.scaled_dot_product_attention without a mask over [context ++ block] keys
+    (grouped-query), F.log_softmax.  float64, CPU."""
+    import torch
+    import torch.nn.functional as F
+    sh = dw.shape
+    d, hd, Hq, Hkv, L = sh.d_model, sh.head_dim, sh.n_q_heads, sh.n_kv_heads, sh.block_size
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    half = hd // 2
+    freq = sh.rope_theta ** (-torch.arange(half, dtype=torch.float64) * 2 / hd)
+
+    def rotate(x, pos):  # x [T, H, hd], pos [T]
+        rot = torch.polar(torch.ones(len(pos), half, dtype=torch.float64), pos[:, None].double() * freq)
+        z = torch.complex(x[..., :half], x[..., half:]) * rot[:, None, :]
+        return torch.cat([z.real, z.imag], -1)
+
+    n = feat.shape[0]
+    c = F.rms_norm(t(feat) @ t(dw.fc).T, (d,), t(dw.fc_norm), sh.rms_eps)
+    pos_c, pos_b = torch.arange(n), torch.arange(n, n + L)
+    block = torch.as_tensor([bonus] + [sh.mask_token] * (L - 1))
+    h = t(dw.embed)[block]
+    for ly in dw.layers:
+        Wq, Wk, Wv = (t(ly.w_qkv)[:Hq * hd], t(ly.w_qkv)[Hq * hd:(Hq + Hkv) * hd], t(ly.w_qkv)[(Hq + Hkv) * hd:])
+        kc = rotate(F.rms_norm((c @ Wk.T).view(n, Hkv, hd), (hd,), t(ly.k_norm), sh.rms_eps), pos_c)
+        vc = (c @ Wv.T).view(n, Hkv, hd)
+        x = F.rms_norm(h, (d,), t(ly.attn_norm), sh.rms_eps)
+        q = rotate(F.rms_norm((x @ Wq.T).view(L, Hq, hd), (hd,), t(ly.q_norm), sh.rms_eps), pos_b)
+        kb = rotate(F.rms_norm((x @ Wk.T).view(L, Hkv, hd), (hd,), t(ly.k_norm), sh.rms_eps), pos_b)
+        vb = (x @ Wv.T).view(L, Hkv, hd)
+        K, V = torch.cat([kc, kb]), torch.cat([vc, vb])
+        o = F.scaled_dot_product_attention(q.transpose(0, 1), K.transpose(0, 1), V.transpose(0, 1), enable_gqa=True)
+        h = h + o.transpose(0, 1).reshape(L, Hq * hd) @ t(ly.w_o).T
+        x = F.rms_norm(h, (d,), t(ly.mlp_norm), sh.rms_eps)
+        gu = x @ t(ly.w_gate_up).T
+        h = h + (F.silu(gu[:, :sh.d_ff]) * gu[:, sh.d_ff:]) @ t(ly.w_down).T
+    logits = F.rms_norm(h[1:], (d,), t(dw.final_norm), sh.rms_eps) @ t(dw.embed).T
+    return F.log_softmax(logits, -1).numpy(), logits.numpy()
+
+
+def test_drafter_block_matches_torch_library_formulation():
+    # context fusion, per-layer K/V injection at the context positions, and the block's
+    # unmasked attention over context ++ block, against an independent formulation
+    tw, dw = _toy_models()
+    n_feat = synth.TOY_TARGET.n_feat
+    feat = synth.normal(6, "feat", (5, n_feat * dw.shape.d_model))
+    ctx = step.KVCache.empty(dw.shape, 32)
+    lp, n, logits = step.draft_block(dw, feat, ctx, 0, 23)
+    rlp, rlogits = _torch_reference_draft(dw, feat, 23)
+    assert n == 5
+    np.testing.assert_allclose(logits, rlogits, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lp, rlp, rtol=1e-6, atol=1e-6)  # oracle log-probs are stored as fp32
+    # the same context committed in two calls (3 rows, then 2) gives the same block
+    ctx2 = step.KVCache.empty(dw.shape, 32)
+    _, n2, _ = step.draft_block(dw, feat[:3], ctx2, 0, 7)
+    lp2, n2, logits2 = step.draft_block(dw, feat[3:], ctx2, n2, 23)
+    assert n2 == 5
+    np.testing.assert_allclose(logits2, rlogits, rtol=1e-10, atol=1e-12)
