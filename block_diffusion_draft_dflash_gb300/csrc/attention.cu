@@ -15,11 +15,14 @@
 //   S = Q K^T   (tcgen05.mma, M=128 N=128 K=128, accumulator in TMEM, triple-buffered)
 //   softmax     (one TMEM lane = one query row, exp2 domain, running max / sum; the
 //                ancestor mask is applied as 32-bit words per key group)
-//   O += P V    (P written bf16 to shared memory in the 128-byte-swizzled K-major layout,
-//                V stored transposed in the cache so that its tile is K-major too)
+//   O += P V    (P written bf16 into TMEM over its own S, the MMA reading A from TMEM;
+//                V stored transposed in the cache so that its tile is K-major)
 // Warp roles: warps 0 .. 4 kCG - 1 softmax/epilogue (kCG warps per 32-row group, one per
 // 128/kCG-column group, exchanging row maxima through shared memory), then a Q/K TMA
-// producer warp, the TMEM owner + MMA issuer warp and a V TMA producer warp.
+// producer warp, the TMEM owner + MMA issuer warp and a V TMA producer warp.  The single
+// MMA thread issues whichever product has its operands (S of a later block, or PV of the
+// oldest block whose P is written), S first, so neither a late K nor a late V tile holds
+// up the other product.
 // The key range of a sequence is split over CTAs (split-KV) when the grid would
 // otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
 #include "attention.h"
