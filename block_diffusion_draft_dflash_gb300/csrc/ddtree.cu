@@ -6,11 +6,15 @@
 // tree is the set of B prefixes with the highest prefix probability under the factorized
 // per-position distribution, found by a best-first max-heap in O(B log B).
 //
-// Kernel 1 (topk_rows_kernel): one CTA per (sequence, position) row of V log-probs.
-//   Radix select on order-preserving 32-bit keys (12 + 12 + 8 bit digits, MSB first,
-//   warp-aggregated shared-memory histograms) finds the K-th largest key T.  A gather
-//   pass takes every key > T and the lowest-id keys == T, and a bitonic sort orders the
-//   K survivors by (log-prob desc, token id asc).
+// Top-K, per (sequence, position) row of V log-probs, on order-preserving 32-bit keys:
+//   * with scratch in the workspace (ddtree_build), three passes over 8192-key chunks
+//     spread over the whole GPU: a histogram of the top 12 key bits, a collect pass that
+//     keeps every key above the K-th key's bin and the candidates inside it, and a final
+//     per-row select + bitonic sort by (log-prob desc, token id asc);
+//   * otherwise, or when a row's candidates overflow, topk_rows_kernel: one CTA per row,
+//     radix select (12 + 12 + 8 bit digits, MSB first, warp-aggregated shared-memory
+//     histograms) for the K-th largest key T, a gather of every key > T and the lowest-id
+//     keys == T, and the same sort.
 // Kernel 2 (ddtree_heap_kernel): one CTA per sequence.  One warp runs the best-first
 //   selection: each candidate is a single 64-bit key whose integer order is the tree's
 //   total order (score desc, depth asc, parent index asc, rank asc), the live candidates
