@@ -10,13 +10,15 @@
 //     runs full-width tensor instructions;
 //   * persistent CTAs (one per SM) split the (tile, k-block) iteration space evenly
 //     ("stream-K"), so the grid stays full however few 128-row weight tiles there are;
-//     partial tiles are summed with fp32 reductions into the output (which, for the
-//     o- and down-projections, is the fp32 residual stream itself);
-//   * warp roles: warp 0 issues TMA loads into a multi-stage shared-memory ring,
-//     warp 1 owns the TMEM allocation and one lane issues tcgen05.mma, warps 2-5 drain
-//     double-buffered TMEM accumulators (tcgen05.ld) and write the epilogue;
-//   * epilogues: fp32 reduction-add, fp32 store (whole tiles), or fused argmax over the
-//     output features (whole tiles; the target LM head writes no logits).
+//   * warp roles: warp 0 issues TMA loads into a multi-stage shared-memory ring (a stage
+//     = one 128 x 64 weight tile + the token rows' 64-wide k-slice), warp 1 owns the TMEM
+//     allocation and one lane issues tcgen05.mma, warps 2-5 drain the TMEM accumulators
+//     (double-buffered when two fit in 512 columns) and write the epilogue;
+//   * epilogues: partial slots (each CTA stores every tile piece it computed to a slot of
+//     its own and lists it for the tile; the next kernel sums a tile's pieces in a fixed
+//     order, so results are deterministic with no atomics; see partials.cuh), fp32
+//     reduction-add or store (whole tiles), or fused argmax over the output features
+//     (whole tiles; the target LM head writes no logits).
 // Every mbarrier wait is bounded (common.cuh); a timeout is recorded in the status word.
 #include <stdio.h>
 
