@@ -25,6 +25,8 @@
 // up the other product.
 // The key range of a sequence is split over CTAs (split-KV) when the grid would
 // otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
+#include <mutex>
+
 #include "attention.h"
 #include "common.cuh"
 #include "trace.h"
@@ -531,12 +533,12 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
   p.out = a.out; p.o_part = a.o_part; p.ml_part = a.ml_part;
   p.status = a.status;
   const size_t smem = 1024 + kTileBytes * (1 + kKStages + kVStages) + 256;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return DF_ERR_CUDA;
-    attr = true;
-  }
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [smem] {
+    attr_err = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (attr_err != cudaSuccess) return DF_ERR_CUDA;
   const int grid = a.b * a.Hkv * n_qtiles * a.nsplit;
   {
     DF_TRACE(a.anc ? "attention_tree" : "attention_draft", st);

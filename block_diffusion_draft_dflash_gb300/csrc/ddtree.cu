@@ -21,6 +21,8 @@
 //   are held in the warp's registers and every pop is a warp-wide maximum.  The CTA then
 //   writes the node arrays and the ancestor bitsets (one warp per row; each lane owns a
 //   32-bit word).
+#include <mutex>
+
 #include "common.cuh"
 #include "trace.h"
 
@@ -529,12 +531,14 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
       launch_k(topk_hist_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, ghist, status);
       launch_k(topk_collect_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, K, ghist, sc, hi, eq);
       const size_t smem = (size_t)(kCapEq + kMaxK) * 8;
-      static bool attr = false;
-      if (!attr) {
-        cudaFuncSetAttribute(topk_final_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(topk_final_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-      }
+      static std::once_flag once;
+      static cudaError_t attr_err = cudaSuccess;
+      std::call_once(once, [smem] {
+        attr_err = cudaFuncSetAttribute(topk_final_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const cudaError_t e = cudaFuncSetAttribute(topk_final_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (attr_err == cudaSuccess) attr_err = e;
+      });
+      if (attr_err != cudaSuccess) return DF_ERR_CUDA;
       if ((V & 3) == 0)
         launch_k(topk_final_kernel<true>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, hi, eq, topk_id, topk_val, status);
       else
