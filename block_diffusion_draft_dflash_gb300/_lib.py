@@ -67,6 +67,10 @@ _SIGS = {
                                        C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_linear": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int,
                       C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dflash_linear_logsoftmax_workspace_size": (C.c_size_t, [C.c_int, C.c_int]),
+    "dflash_linear_logsoftmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                           C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dflash_workspace_configure": (C.c_int, [C.c_void_p, C.c_ulonglong, C.c_int, C.c_void_p]),
     "dflash_draft_block_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
     "dflash_draft_block": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_int] + [C.c_void_p] * 4 +
                            [C.c_int] + [C.c_void_p] * 3 + [C.c_size_t, C.c_void_p]),
@@ -137,6 +141,11 @@ class Workspace:
     def status(self) -> int:
         return load().dflash_workspace_status(self.ptr, _stream())
 
+    def configure(self, wait_limit_ns: int = 0, hold: bool = False):
+        """Failure-path settings (see dflash_workspace_configure)."""
+        _check("dflash_workspace_configure",
+               load().dflash_workspace_configure(self.ptr, int(wait_limit_ns), int(hold), _stream()))
+
 
 # ----------------------------------------------------------------------------- calls
 def ddtree_build_workspace_size(b, D, V, B):
@@ -151,6 +160,7 @@ def ddtree_build(logprobs, B, out, ws: Workspace, root_tok=None):
         _dev(out[k], torch.int32, k)
     _dev(out["score"], torch.float32, "score")
     _dev(out["anc"], torch.int32, "anc")
+    _dev(root_tok, torch.int32, "root_tok")
     _check("ddtree_build", load().ddtree_build(
         _p(logprobs), b, D, V, B, _p(root_tok), _p(out["tok"]), _p(out["parent"]), _p(out["depth"]),
         _p(out["score"]), _p(out["anc"]), ws.ptr, ws.nbytes, _stream()))
@@ -160,6 +170,11 @@ def ddtree_build_static(logprobs, B, out, root_tok=None):
     """ddtree_build without a workspace (the library's fixed device scratch; see dflash.h)."""
     b, D, V = logprobs.shape
     _dev(logprobs, torch.float32, "logprobs")
+    for k in ("tok", "parent", "depth"):
+        _dev(out[k], torch.int32, k)
+    _dev(out["score"], torch.float32, "score")
+    _dev(out["anc"], torch.int32, "anc")
+    _dev(root_tok, torch.int32, "root_tok")
     _check("ddtree_build_static", load().ddtree_build_static(
         _p(logprobs), b, D, V, B, _p(root_tok), _p(out["tok"]), _p(out["parent"]), _p(out["depth"]),
         _p(out["score"]), _p(out["anc"]), _stream()))
@@ -248,6 +263,19 @@ def linear_argmax(X, W, out, ws: Workspace = None):
     ws = ws or Workspace(load().dflash_linear_argmax_workspace_size(M), X.device)
     _check("dflash_linear_argmax", load().dflash_linear_argmax(_p(X), _p(W), M, N, K, _p(out), ws.ptr, ws.nbytes,
                                                                _stream()))
+    return ws
+
+
+def linear_logsoftmax(X, W, out, ws: Workspace = None):
+    """out[t] = log_softmax(X W^T)[t] (fp32); X [M][K] bf16, W [N][K] bf16, out [M][N] fp32."""
+    _dev(X, torch.bfloat16, "X")
+    _dev(W, torch.bfloat16, "W")
+    _dev(out, torch.float32, "out")
+    M, K = X.shape
+    N = W.shape[0]
+    ws = ws or Workspace(load().dflash_linear_logsoftmax_workspace_size(M, N), X.device)
+    _check("dflash_linear_logsoftmax", load().dflash_linear_logsoftmax(_p(X), _p(W), M, N, K, _p(out), ws.ptr,
+                                                                       ws.nbytes, _stream()))
     return ws
 
 

@@ -533,6 +533,52 @@ int dflash_linear_argmax(const df_bf16* X, const df_bf16* W, int M, int N, int K
   return launch_argmax_finalize(keys, M, out, st);
 }
 
+size_t dflash_linear_logsoftmax_workspace_size(int M, int N) {
+  Carver cv(nullptr);
+  const size_t rows = M > 0 ? (size_t)M : 1, tiles = N > 0 ? (size_t)(N + 127) / 128 : 1;
+  cv.take<float>(rows * 4 * tiles * 2);  // per (row, weight tile, warp) (max, sum exp) pairs
+  cv.take<float>(rows);                  // log-sum-exp per row
+  return cv.off;
+}
+
+int dflash_linear_logsoftmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out, void* ws,
+                             size_t ws_bytes, df_stream stream) {
+  if (M < 0 || N <= 0 || K <= 0) return DF_ERR_ARG;
+  if (K % 64) return DF_ERR_SHAPE;
+  if (M == 0) return DF_OK;
+  if (!X || !W || !out) return DF_ERR_ARG;
+  if (!al16(X) || !al16(W) || !al16(out)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < dflash_linear_logsoftmax_workspace_size(M, N)) return DF_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  Carver cv(ws);
+  const int n_stats = 4 * ((N + 127) / 128);
+  float* stats = cv.take<float>((size_t)M * n_stats * 2);
+  float* lse = cv.take<float>((size_t)M);
+  // exactly the drafter's LM-head sequence: logits + softmax partials, then x - lse
+  GemmDesc g{};
+  g.X = X; g.W = W; g.M = M; g.N = N; g.K = K; g.ldx = K; g.ldw = K;
+  g.mode = kGemmStore; g.out = out; g.ldo = N; g.status = status_of(ws); g.stats = stats;
+  DF_TRY(launch_gemm(g, st));
+  return launch_logsoftmax_from_stats(out, M, N, stats, n_stats, lse, st);
+}
+
+int dflash_workspace_configure(void* ws, unsigned long long wait_limit_ns, int hold, df_stream stream) {
+  if (!ws) return DF_ERR_WORKSPACE;
+  struct {
+    unsigned long long limit;
+    int hold;
+  } h{wait_limit_ns, hold};
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(base + offsetof(WsHeader, wait_limit_ns), &h.limit, sizeof(h.limit), cudaMemcpyHostToDevice,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(base + offsetof(WsHeader, hold), &h.hold, sizeof(h.hold), cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return DF_ERR_CUDA;
+  return DF_OK;
+}
+
 int dflash_linear(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out, int accumulate, void* ws,
                   size_t ws_bytes, df_stream stream) {
   if (M < 0 || N < 0 || K <= 0) return DF_ERR_ARG;

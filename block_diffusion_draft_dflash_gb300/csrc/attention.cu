@@ -25,10 +25,9 @@
 // up the other product.
 // The key range of a sequence is split over CTAs (split-KV) when the grid would
 // otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
-#include <mutex>
-
 #include "attention.h"
 #include "common.cuh"
+#include "runtime.h"
 #include "trace.h"
 
 namespace df {
@@ -94,7 +93,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // core, so at most PV_{j-1} is still pending when block j's softmax looks at O.
   uint64_t* p_full = s_full + kSBufs;
   uint64_t* o_done = p_full + kSBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + kSBufs);
+  uint64_t* mma_drain = o_done + kSBufs;  // completion of every MMA issued, when the issuer gives up
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   __shared__ float red_max[2][kCG][128];  // [block parity][column group][row]
   __shared__ float red_sum[kCG][128];
 
@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = 0; i < kVStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
     for (int i = 0; i < kSBufs; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < kSBufs; ++i) { mbar_init(&p_full[i], kSoftThreads); mbar_init(&o_done[i], 1); }
+    mbar_init(mma_drain, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // after its P was read, and S_k complete implies every PV up to k - 3 complete.
       int s_next = 0, pv_next = 0, idle = 0;
       uint64_t t_last = globaltimer();
+      const uint64_t limit = wait_limit(p.status);
       while (ok && pv_next < nblk) {
         if (s_next < nblk && s_next - pv_next < kSBufs &&
             mbar_test_wait(&k_full[s_next % kKStages], (s_next / kKStages) & 1)) {
@@ -222,14 +224,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                    mbar_test_wait(&v_full[pv_next % kVStages], (pv_next / kVStages) & 1)) {
           issue_pv(pv_next++);
         } else {
-          if ((++idle & 1023) == 0) {  // bounded: give up after kWaitLimitNs without progress
-            if (globaltimer() - t_last > kWaitLimitNs) { set_status(p.status, DF_ERR_TIMEOUT, 13); ok = false; }
+          if ((++idle & 1023) == 0) {  // bounded: give up after the wait limit without progress
+            if (globaltimer() - t_last > limit) { set_status(p.status, DF_ERR_TIMEOUT, 13); ok = false; }
             else if (p.status && *(volatile int*)p.status == DF_ERR_TIMEOUT) ok = false;
           }
           continue;
         }
         idle = 0;
         t_last = globaltimer();
+      }
+      if (!ok && (s_next > 0 || pv_next > 0)) {
+        // giving up: the MMAs already issued must finish before TMEM is freed
+        mma_commit(mma_drain);
+        mbar_wait(mma_drain, 0, nullptr, 0);
       }
     }
   } else {
@@ -479,7 +486,7 @@ static int make_tmap(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t
 
 int attn_num_splits(int b, int Hkv, int n_qtiles, int max_keys) {
   const int units = b * Hkv * n_qtiles;
-  const int nsm = num_sms_attn();
+  const int nsm = num_sms();
   const int nb = (max_keys + kKB - 1) / kKB;
   // fill one wave: as many splits as whole copies of the unit set fit on the SMs
   int ns = units >= nsm ? 1 : nsm / units;
@@ -487,17 +494,6 @@ int attn_num_splits(int b, int Hkv, int n_qtiles, int max_keys) {
   if (ns > kAttnMaxSplits) ns = kAttnMaxSplits;
   if (ns < 1) ns = 1;
   return ns;
-}
-
-int num_sms_attn() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
 }
 
 int launch_attention(const AttnArgs& a, cudaStream_t st) {
@@ -533,12 +529,7 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
   p.out = a.out; p.o_part = a.o_part; p.ml_part = a.ml_part;
   p.status = a.status;
   const size_t smem = 1024 + kTileBytes * (1 + kKStages + kVStages) + 256;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [smem] {
-    attr_err = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  });
-  if (attr_err != cudaSuccess) return DF_ERR_CUDA;
+  if (ensure_dynamic_smem(attn_tc_kernel, smem) != cudaSuccess) return DF_ERR_CUDA;
   const int grid = a.b * a.Hkv * n_qtiles * a.nsplit;
   {
     DF_TRACE(a.anc ? "attention_tree" : "attention_draft", st);

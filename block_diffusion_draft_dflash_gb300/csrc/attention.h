@@ -45,7 +45,6 @@ struct AttnParams {
 
 int launch_attention(const AttnArgs& a, cudaStream_t st);
 int attn_num_splits(int b, int Hkv, int n_qtiles, int max_keys);
-int num_sms_attn();
 size_t attn_partial_bytes(int b, int T, int Hq, int nsplit);
 
 }  // namespace df

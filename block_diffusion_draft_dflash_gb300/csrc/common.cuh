@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <utility>
@@ -21,9 +22,12 @@ namespace df {
 struct WsHeader {        // first 256 bytes of every workspace
   int status;            // first device-side error code (0 = none)
   int detail;            // kernel-specific detail for that error
-  int pad[62];
+  unsigned long long wait_limit_ns;  // limit of every bounded wait (0 = kWaitLimitNs)
+  int hold;              // test hook: nonzero makes each GEMM wait (bounded) for it to read 0
+  int pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
+static_assert(offsetof(WsHeader, wait_limit_ns) == 8 && offsetof(WsHeader, hold) == 16, "header layout");
 
 DF_DEV void set_status(int* status, int code, int detail = 0) {
   if (status && atomicCAS(status, 0, code) == 0) status[1] = detail;
@@ -36,6 +40,14 @@ DF_DEV uint64_t globaltimer() {
 }
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// The wait limit of a workspace: its header's setting, else kWaitLimitNs.  Waits given no
+// status word (the drains of a kernel that is giving up) always use kWaitLimitNs.
+DF_DEV uint64_t wait_limit(const int* status) {
+  if (!status) return kWaitLimitNs;
+  const uint64_t l = *reinterpret_cast<const volatile unsigned long long*>(status + 2);
+  return l ? l : kWaitLimitNs;
+}
 
 // --------------------------------------------------------------------------- smem / mbarrier
 DF_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -69,19 +81,38 @@ DF_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for phase `parity` of `bar` to complete.  Returns false (and records a
-// timeout) if it does not complete within kWaitLimitNs.
+// timeout) if it does not complete within the workspace's wait limit (wait_limit).
 DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int where) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const uint64_t t0 = globaltimer(), limit = wait_limit(status);
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit) {
       set_status(status, DF_ERR_TIMEOUT, where);
       return false;
     }
     if (status && *(volatile int*)status == DF_ERR_TIMEOUT) return false;  // another role gave up
   }
+}
+
+// Test hook of the failure path: while the workspace header's `hold` word is nonzero the
+// caller waits, bounded by the workspace's wait limit; returns false (and records
+// DF_ERR_TIMEOUT) if the word is still set at the limit.  Nothing in the library sets the
+// word, so a kernel that finds it set always times out, having issued no work.
+DF_DEV bool wait_hold_clear(int* status, int where) {
+  if (!status) return true;
+  const volatile int* hold = status + 4;
+  if (*hold == 0) return true;
+  const uint64_t t0 = globaltimer(), limit = wait_limit(status);
+  while (*hold != 0) {
+    if (globaltimer() - t0 > limit) {
+      set_status(status, DF_ERR_TIMEOUT, where);
+      return false;
+    }
+    __nanosleep(1000);
+  }
+  return true;
 }
 
 // --------------------------------------------------------------------------- TMA

@@ -21,9 +21,8 @@
 //   are held in the warp's registers and every pop is a warp-wide maximum.  The CTA then
 //   writes the node arrays and the ancestor bitsets (one warp per row; each lane owns a
 //   32-bit word).
-#include <mutex>
-
 #include "common.cuh"
+#include "runtime.h"
 #include "trace.h"
 
 namespace df {
@@ -531,14 +530,9 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
       launch_k(topk_hist_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, ghist, status);
       launch_k(topk_collect_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, K, ghist, sc, hi, eq);
       const size_t smem = (size_t)(kCapEq + kMaxK) * 8;
-      static std::once_flag once;
-      static cudaError_t attr_err = cudaSuccess;
-      std::call_once(once, [smem] {
-        attr_err = cudaFuncSetAttribute(topk_final_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        const cudaError_t e = cudaFuncSetAttribute(topk_final_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (attr_err == cudaSuccess) attr_err = e;
-      });
-      if (attr_err != cudaSuccess) return DF_ERR_CUDA;
+      if (ensure_dynamic_smem(topk_final_kernel<true>, smem) != cudaSuccess ||
+          ensure_dynamic_smem(topk_final_kernel<false>, smem) != cudaSuccess)
+        return DF_ERR_CUDA;
       if ((V & 3) == 0)
         launch_k(topk_final_kernel<true>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, hi, eq, topk_id, topk_val, status);
       else
@@ -553,14 +547,7 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
   // registers per lane for the live candidates (at most B + 1)
   const int nreg = (B + 1 + 31) / 32;
   auto launch = [&](auto kern) -> int {
-    static thread_local size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-      for (auto k : {ddtree_heap_kernel<1>, ddtree_heap_kernel<2>, ddtree_heap_kernel<4>, ddtree_heap_kernel<9>,
-                     ddtree_heap_kernel<17>, ddtree_heap_kernel<33>, ddtree_heap_kernel<65>})
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-          return DF_ERR_CUDA;
-      configured = smem;
-    }
+    if (ensure_dynamic_smem(kern, smem) != cudaSuccess) return DF_ERR_CUDA;
     DF_TRACE("ddtree_heap", st);
     launch_k(kern, dim3(b), dim3(256), smem, st, topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok, tok, parent, depth,
              score, anc, status);

@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "partials.cuh"
+#include "runtime.h"
 #include "trace.h"
 
 namespace df {
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = bars + 2 * S;
   uint64_t* tempty = bars + 2 * S + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  uint64_t* mma_drain = bars + 2 * S + 5;  // completion of every MMA issued, when the issuer gives up
   // argmax epilogue: per warp, per 32-column chunk, per lane (= column) running maximum key
   unsigned long long* run_max = reinterpret_cast<unsigned long long*>(bars + 2 * S + 6);
 
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 128); }
+    mbar_init(mma_drain, 1);
     fence_barrier_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -175,7 +178,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
     const uint64_t pol_w = p.w_keep ? policy_evict_last() : policy_evict_first(), pol_x = policy_evict_last();
-    const long long n = it1 - it0;
+    // failure-path test hook: with the header's hold word set, issue nothing and give up
+    const long long n = wait_hold_clear(p.status, 5) ? it1 - it0 : 0;
     auto coords = [&](long long it, int& wt, int& tt, int& k) {
       const long long tile = it / p.k_iters;
       k = (int)(it - tile * p.k_iters);
@@ -236,10 +240,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     long long it = it0;
     Segment sg;
     int si = 0;
-    bool ok = true;
+    bool ok = true, issued_any = false;
     while (ok && next_segment(p, it, it1, sg)) {
       const int acc = si % p.nbuf, use = si / p.nbuf;
-      if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 2)) break;
+      if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 2)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int k = sg.k0; k < sg.k1; ++k) {
@@ -255,11 +259,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc0, accum);
           if (p.sub1) mma_bf16(d_tmem + p.sub0, adesc + 2 * kk, bdesc1 + 2 * kk, idesc1, accum);
         }
+        issued_any = true;
         mma_commit(&empty[stage]);
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
+      if (!ok) break;
       mma_commit(&tfull[acc]);
       ++si;
+    }
+    if (issued_any && !ok) {
+      // giving up: the MMAs already issued must finish before TMEM is freed
+      mma_commit(mma_drain);
+      mbar_wait(mma_drain, 0, nullptr, 0);
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue
@@ -429,17 +440,6 @@ int make_tmap_2d(CUtensorMap* out, const void* ptr, long long rows, long long co
   return DF_OK;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 // Token tile.  Up to 512 tokens form one tile (two MMAs of N <= 256 per k-step, one
 // TMEM buffer), so every weight k-chunk is streamed once; beyond that, equal tiles of at
 // most 256 (double-buffered TMEM) with the weights kept in L2 for the later tiles.
@@ -522,15 +522,14 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   p.stages = stages;
   const size_t smem = 1024 + (size_t)stages * stage_bytes + (2 * stages + 6) * 8 +
                       (g.mode == kGemmArgmax ? 4 * kArgChunks * 32 * 8 : 0);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    for (auto k : {gemm_bf16_tc_kernel<kGemmPartial>, gemm_bf16_tc_kernel<kGemmAtomicAdd>,
-                   gemm_bf16_tc_kernel<kGemmStore>, gemm_bf16_tc_kernel<kGemmArgmax>}) {
-      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      if (e != cudaSuccess) attr_err = e;
-    }
-  });
+  cudaError_t attr_err = cudaSuccess;
+  switch (g.mode) {
+    case kGemmPartial: attr_err = ensure_dynamic_smem(gemm_bf16_tc_kernel<kGemmPartial>, smem); break;
+    case kGemmAtomicAdd: attr_err = ensure_dynamic_smem(gemm_bf16_tc_kernel<kGemmAtomicAdd>, smem); break;
+    case kGemmStore: attr_err = ensure_dynamic_smem(gemm_bf16_tc_kernel<kGemmStore>, smem); break;
+    case kGemmArgmax: attr_err = ensure_dynamic_smem(gemm_bf16_tc_kernel<kGemmArgmax>, smem); break;
+    default: return DF_ERR_ARG;
+  }
   if (attr_err != cudaSuccess) return DF_ERR_CUDA;
   long long grid = num_sms();
   const long long work = p.whole_tiles ? tiles : p.total_iters;

@@ -29,6 +29,5 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st);
 // Bytes of partial-tile slots a kGemmPartial launch of this shape writes.
 size_t gemm_partial_bytes(int M, int N, int K);
 int make_tmap_2d(struct CUtensorMap_st* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows);
-int num_sms();
 
 }  // namespace df

@@ -6,8 +6,10 @@
 //   rope_table_kernel      (cos, sin) of every row's rotary angles, once per forward
 //   qk_norm_rope_kernel    per-head RMSNorm of q and k, rotary embedding, q to its buffer,
 //                          k and v into their cache slots (v transposed)
-//   swiglu_kernel          bf16 act <- silu(gate) * up from the fp32 gate/up accumulator
-//   logsoftmax_rows_kernel fp32 log-softmax of each logits row, in place
+//   res_norm_kernel        partial tiles of a projection + residual, then RMSNorm
+//   swiglu_partial_kernel  bf16 act <- silu(gate) * up from the gate/up partial tiles
+//   lse_from_stats_kernel  log-sum-exp of each LM-head row from the GEMM's softmax partials
+//   sub_lse_kernel         x - lse, in place (the drafter's log-probs)
 //   argmax_finalize_kernel token id from the packed argmax keys
 // Readings: Qwen3-style pre-norm layer (see the oracle); RMSNorm eps and rotary base
 // come from the model config.
@@ -279,57 +281,6 @@ __global__ void __launch_bounds__(256) swiglu_partial_kernel(SwigluArgs a) {
   *reinterpret_cast<uint2*>(a.act + (size_t)t * a.F + f) = o;
 }
 
-// act[r][f] = silu(gu[r][f]) * gu[r][F + f]
-__global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ gu, int rows, int F,
-                                                     df_bf16* __restrict__ act) {
-  pdl_wait();
-  pdl_trigger();
-  const long long n4 = (long long)rows * F / 4;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-    const long long e = i * 4;
-    const long long r = e / F;
-    const int f = (int)(e % F);
-    const float4 g = *reinterpret_cast<const float4*>(gu + r * 2 * F + f);
-    const float4 u = *reinterpret_cast<const float4*>(gu + r * 2 * F + F + f);
-    auto sl = [](float x) { return x / (1.f + __expf(-x)); };
-    uint2 o;
-    o.x = (uint32_t)f_to_bf16(sl(g.x) * u.x) | ((uint32_t)f_to_bf16(sl(g.y) * u.y) << 16);
-    o.y = (uint32_t)f_to_bf16(sl(g.z) * u.z) | ((uint32_t)f_to_bf16(sl(g.w) * u.w) << 16);
-    *reinterpret_cast<uint2*>(act + e) = o;
-  }
-}
-
-// grid: rows; block 1024.  Two passes: online max/sum, then x - (max + log(sum)).
-__global__ void __launch_bounds__(1024) logsoftmax_rows_kernel(float* __restrict__ x, int V) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float sm[32], ss[32];
-  float* row = x + (size_t)blockIdx.x * V;
-  float m = -INFINITY, s = 0.f;
-  for (int i = threadIdx.x; i < V; i += blockDim.x) {
-    const float v = row[i];
-    if (v > m) { s = s * __expf(m - v) + 1.f; m = v; }
-    else s += __expf(v - m);
-  }
-  // combine (m, s) pairs: warp, then block
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float mm = fmaxf(m, m2);
-    s = (m == -INFINITY ? 0.f : s * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
-    m = mm;
-  }
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if (lane == 0) { sm[w] = m; ss[w] = s; }
-  __syncthreads();
-  float M = -INFINITY;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, sm[i]);
-  float S = 0.f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) S += sm[i] == -INFINITY ? 0.f : ss[i] * __expf(sm[i] - M);
-  const float lse = M + logf(S);
-  for (int i = threadIdx.x; i < V; i += blockDim.x) row[i] = row[i] - lse;
-}
-
 // lse[r] from the GEMM epilogue's (max, sum exp) partials of row r.
 __global__ void __launch_bounds__(1024) lse_from_stats_kernel(const float2* __restrict__ stats, int n_stats,
                                                               float* __restrict__ lse) {
@@ -382,13 +333,6 @@ __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ am
   if (r < rows) out[r] = (int32_t)(~(uint32_t)(amax[r] & 0xFFFFFFFFull));
 }
 
-__global__ void add_lengths_kernel(int32_t* len, const int32_t* __restrict__ add, int b) {
-  pdl_wait();
-  pdl_trigger();
-  const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s < b) len[s] += add[s];
-}
-
 // ----------------------------------------------------------------------------- launchers
 int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
                  float* h, int rows, int* status, cudaStream_t st) {
@@ -423,14 +367,6 @@ int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st) {
            dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
-int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st) {
-  const long long n4 = (long long)rows * F / 4;
-  long long grid = (n4 + 255) / 256;
-  if (grid > 4 * 152) grid = 4 * 152;
-  if (grid < 1) grid = 1;
-  launch_k(swiglu_kernel, dim3((unsigned)grid), dim3(256), 0, st, gu, rows, F, act);
-  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
-}
 int launch_res_norm(const ResNormArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return DF_OK;
   if (a.d % 128 || a.d > 8192) return DF_ERR_SHAPE;
@@ -449,10 +385,6 @@ int launch_swiglu_partial(const SwigluArgs& a, cudaStream_t st) {
   launch_k(swiglu_partial_kernel, dim3(dim3(a.rows, (a.F + 1023) / 1024)), dim3(256), 0, st, a);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
-int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st) {
-  launch_k(logsoftmax_rows_kernel, dim3(rows), dim3(1024), 0, st, x, V);
-  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
-}
 int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
                                  cudaStream_t st) {
   DF_TRACE("logsoftmax", st);
@@ -463,10 +395,6 @@ int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, 
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st) {
   DF_TRACE("argmax_finalize", st);
   launch_k(argmax_finalize_kernel, dim3((rows + 255) / 256), dim3(256), 0, st, amax, rows, out);
-  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
-}
-int launch_add_lengths(int32_t* len, const int32_t* add, int b, cudaStream_t st) {
-  launch_k(add_lengths_kernel, dim3((b + 255) / 256), dim3(256), 0, st, len, add, b);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

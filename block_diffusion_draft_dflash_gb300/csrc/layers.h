@@ -73,14 +73,11 @@ int launch_rmsnorm(const RmsNormArgs& a, cudaStream_t st);
 // Rotary table of every row of a forward (the positions are the same in every layer).
 int launch_rope_table(const QkRopeArgs& a, float2* table, cudaStream_t st);
 int launch_qk_rope(const QkRopeArgs& a, cudaStream_t st);
-int launch_swiglu(const float* gu, int rows, int F, df_bf16* act, cudaStream_t st);
 int launch_res_norm(const ResNormArgs& a, cudaStream_t st);
 int launch_swiglu_partial(const SwigluArgs& a, cudaStream_t st);
-int launch_logsoftmax(float* x, int rows, int V, cudaStream_t st);
 // In-place log-softmax of rows whose (max, sum exp) partials came from the LM-head GEMM.
 int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
                                  cudaStream_t st);
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st);
-int launch_add_lengths(int32_t* len, const int32_t* add, int b, cudaStream_t st);
 
 }  // namespace df

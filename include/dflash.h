@@ -28,8 +28,11 @@
  *     are passed as uint16_t bit patterns (df_bf16).  Every pointer must be 16-byte
  *     aligned (DF_ERR_ALIGN otherwise).
  *   - Host-detectable errors are returned at once and nothing is launched.  Errors the
- *     GPU finds (NaN log-probs, an exhausted wait) are recorded in the workspace's status
- *     word; dflash_workspace_status() returns and clears it.
+ *     GPU finds (NaN log-probs, an exhausted wait, a full cache) are recorded in the
+ *     workspace's status word; dflash_workspace_status() returns and clears it.  Every
+ *     device-side wait is bounded (2 s unless dflash_workspace_configure sets otherwise).
+ *   - Host-side state (kernel attributes, SM counts, tensor maps) is kept per device, so
+ *     one process may use the library on several GPUs in turn.
  *   - The cache layout is [layer][batch][kv_head][slot][head_dim] for K and
  *     [layer][batch][kv_head][head_dim][slot] for V (V is stored transposed so that
  *     every tensor-core operand is K-major).  Slot s of a sequence holds the token at
@@ -175,6 +178,8 @@ int ddtree_build(const float* logprobs, int b, int D, int V, int B, const int32_
  *     word first; the top-K lists are fully rewritten before they are read.
  *   - Device-side errors cannot be handed back (there is no workspace to read): when a
  *     log-probability is NaN the outputs of that call are left unwritten.
+ *   - The looked-up address is kept for the life of the process: the library must not be
+ *     used on a device after its primary context has been reset (cudaDeviceReset).
  * ------------------------------------------------------------------------------------ */
 int ddtree_build_static(const float* logprobs, int b, int D, int V, int B, const int32_t* root_tok,
                         int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* anc,
@@ -282,6 +287,17 @@ size_t dflash_linear_argmax_workspace_size(int M);
 int dflash_linear_argmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, int32_t* out,
                          void* ws, size_t ws_bytes, df_stream stream);
 
+/* dflash_linear_logsoftmax -- out[t][n] = log-softmax over n of (X W^T)[t]: the drafter's LM
+ * head of dflash_draft_block, exactly its sequence of kernels (logits stored with per-tile
+ * softmax partials, then the log-sum-exp of each row subtracted).
+ * [DDTree] "핵심 아이디어": the drafter gives one distribution per block position, and the
+ * tree builder reads those distributions as log-probabilities.
+ *   X [M][K] bf16, W [N][K] bf16, K a multiple of 64, out [M][N] fp32.
+ *   Workspace: dflash_linear_logsoftmax_workspace_size(M, N) bytes. */
+size_t dflash_linear_logsoftmax_workspace_size(int M, int N);
+int dflash_linear_logsoftmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out,
+                             void* ws, size_t ws_bytes, df_stream stream);
+
 /* ------------------------------------------------------------------------------------
  * Status and device queries.
  * ------------------------------------------------------------------------------------ */
@@ -296,6 +312,15 @@ int dflash_trace_read(int max_entries, char* names, double* total_ms, int* count
 /* Reads and clears the device status word of a workspace (synchronises `stream`).
  * Returns DF_OK or the first device-side error recorded since the last read. */
 int dflash_workspace_status(void* ws, df_stream stream);
+/* Failure-path settings of a workspace (synchronises `stream`), kept until changed:
+ *   wait_limit_ns  limit of every bounded device-side wait of calls using this workspace
+ *                  (0 = the default, 2 s); a wait that runs out records DF_ERR_TIMEOUT and
+ *                  its kernel returns without touching TMEM or shared memory still in use
+ *   hold           test hook: nonzero makes every projection GEMM of such a call wait for
+ *                  the word to read 0 before it issues any work.  Nothing clears it, so the
+ *                  wait runs out and the call reports DF_ERR_TIMEOUT; set 0 to go on.
+ * Zero-initialised workspaces start with both at 0. */
+int dflash_workspace_configure(void* ws, unsigned long long wait_limit_ns, int hold, df_stream stream);
 /* Static text for a status code. */
 const char* dflash_status_string(int status);
 /* DF_OK if the current CUDA device is compute capability 10.3 (GB300). */

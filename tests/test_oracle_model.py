@@ -261,3 +261,38 @@ def test_drafter_block_matches_torch_library_formulation():
     lp2, n2, logits2 = step.draft_block(dw, feat[3:], ctx2, n2, 23)
     assert n2 == 5
     np.testing.assert_allclose(logits2, rlogits, rtol=1e-10, atol=1e-12)
+
+
+def _first_max_by_scan(row):
+    """Lowest index of the row's maximum: one pass, a later index replaces the running best
+    only when strictly larger."""
+    best = 0
+    for i in range(1, len(row)):
+        if row[i] > row[best]:
+            best = i
+    return best
+
+
+def test_argmax_lowest_resolves_planted_ties_to_lowest_id():
+    # rows whose maximum occurs at several positions (exact float64 ties), placed before,
+    # around and after the other entries; the greedy choice is the lowest of those ids
+    g = np.random.default_rng(17)
+    V = 97
+    logits = g.normal(0, 1, size=(40, V))
+    expect = []
+    for r in range(logits.shape[0]):
+        k = 2 + r % 4
+        pos = np.sort(g.choice(V, size=k, replace=False))
+        logits[r, pos] = logits[r].max() + 1.0 + (r % 3)
+        expect.append(int(pos[0]))
+    logits[0, :] = 0.25                     # every entry ties: id 0
+    expect[0] = 0
+    logits[1, :] = -np.inf                  # all -inf: still id 0
+    logits[1, 50] = -np.inf
+    expect[1] = 0
+    logits[2, V - 1] = logits[2].max() + 5  # a single maximum at the last id
+    expect[2] = V - 1
+    got = model.argmax_lowest(logits)
+    assert got.dtype == np.int32
+    np.testing.assert_array_equal(got, expect)
+    np.testing.assert_array_equal(got, [_first_max_by_scan(row) for row in logits])
