@@ -52,6 +52,9 @@ _SIGS = {
     "ddtree_build": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int] + [C.c_void_p] * 7 +
                      [C.c_size_t, C.c_void_p]),
     "ddtree_build_static": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int] + [C.c_void_p] * 7),
+    "dflash_chain_build_workspace_size": (C.c_size_t, [C.c_int, C.c_int]),
+    "dflash_chain_build": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int] + [C.c_void_p] * 7 +
+                           [C.c_size_t, C.c_void_p]),
     "tree_verify_attention_workspace_size": (C.c_size_t, [C.c_int] * 6),
     "tree_verify_attention": (C.c_int, [C.c_int] * 5 + [C.c_void_p] * 3 + [C.c_int, C.c_void_p, C.c_void_p,
                               C.c_float, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -178,6 +181,24 @@ def ddtree_build_static(logprobs, B, out, root_tok=None):
     _check("ddtree_build_static", load().ddtree_build_static(
         _p(logprobs), b, D, V, B, _p(root_tok), _p(out["tok"]), _p(out["parent"]), _p(out["depth"]),
         _p(out["score"]), _p(out["anc"]), _stream()))
+
+
+def chain_build_workspace_size(b, D):
+    return load().dflash_chain_build_workspace_size(b, D)
+
+
+def chain_build(logprobs, out, ws: Workspace, root_tok=None):
+    """logprobs [b][D][V] fp32 -> the argmax chain in out (tok/parent/depth/score/anc, D+1 nodes)."""
+    b, D, V = logprobs.shape
+    _dev(logprobs, torch.float32, "logprobs")
+    for k in ("tok", "parent", "depth"):
+        _dev(out[k], torch.int32, k)
+    _dev(out["score"], torch.float32, "score")
+    _dev(out["anc"], torch.int32, "anc")
+    _dev(root_tok, torch.int32, "root_tok")
+    _check("dflash_chain_build", load().dflash_chain_build(
+        _p(logprobs), b, D, V, _p(root_tok), _p(out["tok"]), _p(out["parent"]), _p(out["depth"]),
+        _p(out["score"]), _p(out["anc"]), ws.ptr, ws.nbytes, _stream()))
 
 
 def tree_verify_attention_workspace_size(b, n_tree, Hq, Hkv, hd, cap):

@@ -15,6 +15,8 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
                   int32_t* parent, int32_t* depth, float* score, uint32_t* anc, int32_t* topk_id, float* topk_val,
                   int* status, cudaStream_t st, void* chunk_scratch);
 size_t ddtree_heap_smem(int D, int K, int B);
+int launch_chain(const float* lp, int b, int D, int V, const int32_t* root_tok, int32_t* tok, int32_t* parent,
+                 int32_t* depth, float* score, uint32_t* anc, unsigned long long* keys, int* status, cudaStream_t st);
 size_t topk_chunked_scratch_bytes(int rows);
 size_t accept_scratch_bytes(int b);
 int launch_accept(int b, int n_tree, const int32_t* choice, const int32_t* tok, const int32_t* parent,
@@ -293,6 +295,27 @@ int ddtree_build(const float* logprobs, int b, int D, int V, int B, const int32_
                        (cudaStream_t)stream, chunk);
 }
 
+// -------------------------------------------------------------------------- chain
+size_t dflash_chain_build_workspace_size(int b, int D) {
+  Carver cv(nullptr);
+  cv.take<unsigned long long>((size_t)(b > 0 ? b : 1) * (D > 0 ? D : 1));
+  return cv.off;
+}
+
+int dflash_chain_build(const float* logprobs, int b, int D, int V, const int32_t* root_tok, int32_t* tok,
+                       int32_t* parent, int32_t* depth, float* score, uint32_t* anc, void* ws, size_t ws_bytes,
+                       df_stream stream) {
+  if (b < 0 || D < 1 || D > 31 || V < 1) return DF_ERR_ARG;
+  if (b == 0) return DF_OK;
+  if (!logprobs || !tok || !parent || !depth || !score || !anc) return DF_ERR_ARG;
+  if (!al16(logprobs) || !al16(tok) || !al16(parent) || !al16(depth) || !al16(score) || !al16(anc)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < dflash_chain_build_workspace_size(b, D)) return DF_ERR_WORKSPACE;
+  Carver cv(ws);
+  unsigned long long* keys = cv.take<unsigned long long>((size_t)b * D);
+  return launch_chain(logprobs, b, D, V, root_tok, tok, parent, depth, score, anc, keys, status_of(ws),
+                      (cudaStream_t)stream);
+}
+
 // ------------------------------------------------------------------------- attention
 size_t tree_verify_attention_workspace_size(int b, int n_tree, int Hq, int Hkv, int hd, int cap) {
   (void)hd;
@@ -370,8 +393,9 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
   if (!w || !w->layers || !w->embed || !w->final_norm || b < 0 || n_tree < 1 || cap <= 0) return DF_ERR_ARG;
   if (cap % 8) return DF_ERR_SHAPE;
   if (b == 0) return DF_OK;
-  if (!tok || !depth || !anc || !k_cache || !v_cache || !cache_len || !choice) return DF_ERR_ARG;
-  if (!al16(k_cache) || !al16(v_cache) || !al16(anc) || (tree_feat && !al16(tree_feat))) return DF_ERR_ALIGN;
+  if (!tok || !k_cache || !v_cache || !cache_len || !choice) return DF_ERR_ARG;
+  if ((depth == nullptr) != (anc == nullptr)) return DF_ERR_ARG;  // both NULL: a causal chain
+  if (!al16(k_cache) || !al16(v_cache) || (anc && !al16(anc)) || (tree_feat && !al16(tree_feat))) return DF_ERR_ALIGN;
   if (!ws || ws_bytes < dflash_target_tree_forward_workspace_size(c, b, n_tree)) return DF_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   TargetWs W;
@@ -403,7 +427,7 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
     if (li == 0) DF_TRY(launch_rope_table(qk, W.B.rope, st));
     AttnArgs& at = L.at;
     at.b = b; at.T = n_tree; at.Hq = c->n_q_heads; at.Hkv = Hkv; at.cap = cap;
-    at.dense_len = cache_len; at.dense_add = 0; at.tail_len = n_tree; at.anc = anc;
+    at.dense_len = cache_len; at.dense_add = 0; at.tail_len = n_tree; at.anc = anc; at.causal = anc == nullptr;
     at.scale = 1.0f / sqrtf(128.f);
     at.nsplit = nsplit_for(b, n_tree, c->n_q_heads, Hkv, cap);
     at.status = status;

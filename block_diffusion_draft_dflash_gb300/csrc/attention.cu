@@ -55,6 +55,17 @@ DF_DEV uint32_t anc_bits32(const uint32_t* row, int W, int t0) {
   return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
 }
 
+// Causal tail bits for tail indices t0 .. t0+31: set where 0 <= t <= node (a chain whose
+// node i sees tail slots 0 .. i).
+DF_DEV uint32_t causal_bits32(int t0, int node) {
+  const int lo = t0 < 0 ? -t0 : 0;           // first bit with t >= 0
+  const int hi = node - t0 + 1;              // bits below hi have t <= node
+  if (hi <= lo || lo >= 32) return 0u;
+  const uint32_t below_hi = hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u);
+  const uint32_t from_lo = lo == 0 ? 0xFFFFFFFFu : ~((1u << lo) - 1u);
+  return below_hi & from_lo;
+}
+
 // Dense bits for keys j0 .. j0+31: set where j < dense_len.
 DF_DEV uint32_t dense_bits32(int j0, int dense_len) {
   const int n = dense_len - j0;
@@ -279,6 +290,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int j0 = key0 + 32 * g;
             uint32_t bits = row_ok ? dense_bits32(j0, dense_len) : 0u;
             if (anc_row) bits |= anc_bits32(anc_row, p.W, j0 - dense_len);
+            else if (p.causal && row_ok) bits |= causal_bits32(j0 - dense_len, node);
             adm[g] = bits;
           }
 #pragma unroll
@@ -523,6 +535,7 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
   p.b = a.b; p.T = a.T; p.Hq = a.Hq; p.Hkv = a.Hkv; p.cap = a.cap;
   p.dense_len = a.dense_len; p.dense_add = a.dense_add; p.tail_len = a.tail_len;
   p.anc = a.anc; p.W = a.anc ? (a.tail_len + 31) / 32 : 0;
+  p.causal = a.anc ? 0 : a.causal;
   p.scale = a.scale;
   p.n_qtiles = n_qtiles;
   p.nsplit = a.nsplit;
@@ -532,7 +545,7 @@ int launch_attention(const AttnArgs& a, cudaStream_t st) {
   if (ensure_dynamic_smem(attn_tc_kernel, smem) != cudaSuccess) return DF_ERR_CUDA;
   const int grid = a.b * a.Hkv * n_qtiles * a.nsplit;
   {
-    DF_TRACE(a.anc ? "attention_tree" : "attention_draft", st);
+    DF_TRACE(a.anc ? "attention_tree" : a.causal ? "attention_causal" : "attention_draft", st);
     launch_k(attn_tc_kernel, dim3(grid), dim3(kAttnThreads), smem, st, tq, tk, tv, p);
   }
   if (cudaGetLastError() != cudaSuccess) return DF_ERR_CUDA;

@@ -20,7 +20,9 @@ struct AttnArgs {
   const int32_t* dense_len;
   int dense_add;
   int tail_len;
-  const uint32_t* anc;     // [b][T][ceil(tail_len/32)] or null (tail fully visible is not supported: use dense)
+  const uint32_t* anc;     // [b][T][ceil(tail_len/32)], or null: then the tail is causal
+                           //   (row i sees tail slots 0 .. i) if `causal`, else not visible
+  int causal;
   float scale;
   int nsplit;
   df_bf16* out;            // [b][T][Hq][128]
@@ -35,6 +37,7 @@ struct AttnParams {
   int dense_add, tail_len;
   const uint32_t* anc;
   int W;
+  int causal;
   float scale;
   int n_qtiles, nsplit;
   df_bf16* out;

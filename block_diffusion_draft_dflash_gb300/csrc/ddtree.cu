@@ -562,4 +562,93 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
   if (nreg <= 65) return launch(ddtree_heap_kernel<65>);
   return DF_ERR_SHAPE;
 }
+
+// ----------------------------------------------------------------------------- chain
+// Vanilla DFlash draft (summary of "Accelerating Speculative Decoding with Block Diffusion
+// Draft Trees", section "실험 결과", compares it with DDTree at the same block size): the
+// drafter's most likely token at every position, verified as one causal chain.
+//
+// chain_argmax_kernel: grid (ceil(V / kChunk), rows), one block per 8192-entry chunk of a
+//   row; the block's maximum key ((order-preserving log-prob bits << 32) | ~token id, so
+//   the largest value wins and, among equal values, the lowest id) is folded into the
+//   row's key with one 64-bit atomic maximum.
+// chain_finalize_kernel: one warp per sequence: node i (1..D) carries position i's token,
+//   parent i - 1, depth i, score = fp32 sum of log-probs root first; ancestor row i has
+//   bits 0..i set.
+__global__ void __launch_bounds__(kChunkThreads) chain_argmax_kernel(const float* __restrict__ lp, int V,
+                                                                     unsigned long long* __restrict__ keys,
+                                                                     int* status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ unsigned long long red[kChunkThreads / 32];
+  const size_t row = blockIdx.y;
+  const float* x = lp + row * (size_t)V;
+  const int i0 = blockIdx.x * kChunk, i1 = min(V, i0 + kChunk);
+  unsigned long long best = 0ull;
+  bool nan = false;
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    const float f = __ldg(x + i);
+    nan |= isnan(f);
+    const unsigned long long k = ((unsigned long long)float_key(f) << 32) | (uint32_t)(~(uint32_t)i);
+    best = k > best ? k : best;
+  }
+  if (__any_sync(0xffffffffu, nan) && (threadIdx.x & 31) == 0) set_status(status, DF_ERR_NAN, (int)row);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+    best = y > best ? y : best;
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) best = red[w] > best ? red[w] : best;
+    atomicMax(keys + row, best);
+  }
+}
+
+__global__ void __launch_bounds__(32) chain_finalize_kernel(const unsigned long long* __restrict__ keys, int D,
+                                                            const int32_t* __restrict__ root_tok,
+                                                            int32_t* __restrict__ tok, int32_t* __restrict__ parent,
+                                                            int32_t* __restrict__ depth, float* __restrict__ score,
+                                                            uint32_t* __restrict__ anc, const int* status) {
+  pdl_wait();
+  pdl_trigger();
+  if (status && *(volatile const int*)status == DF_ERR_NAN) return;
+  const int s = blockIdx.x, lane = threadIdx.x;
+  const int n = D + 1, W = (n + 31) / 32;
+  const size_t o = (size_t)s * n;
+  if (lane == 0) {
+    float sc = 0.f;
+    tok[o] = root_tok ? root_tok[s] : -1;
+    parent[o] = -1;
+    depth[o] = 0;
+    score[o] = 0.f;
+    for (int i = 1; i <= D; ++i) {
+      const unsigned long long k = keys[(size_t)s * D + i - 1];
+      sc = sc + key_float((uint32_t)(k >> 32));
+      tok[o + i] = (int32_t)(~(uint32_t)(k & 0xFFFFFFFFull));
+      parent[o + i] = i - 1;
+      depth[o + i] = i;
+      score[o + i] = sc;
+    }
+  }
+  for (int e = lane; e < n * W; e += 32) {
+    const int i = e / W, w = e % W;
+    const int nb = i + 1 - 32 * w;  // bits 0..i set
+    anc[o * W + e] = nb >= 32 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : ((1u << nb) - 1u));
+  }
+}
+
+int launch_chain(const float* lp, int b, int D, int V, const int32_t* root_tok, int32_t* tok, int32_t* parent,
+                 int32_t* depth, float* score, uint32_t* anc, unsigned long long* keys, int* status, cudaStream_t st) {
+  DF_TRACE("chain", st);
+  const int rows = b * D;
+  launch_k(zero_u32_kernel, dim3((unsigned)((2 * rows + 255) / 256)), dim3(256), 0, st,
+           reinterpret_cast<uint32_t*>(keys), (size_t)2 * rows);
+  launch_k(chain_argmax_kernel, dim3((V + kChunk - 1) / kChunk, rows), dim3(kChunkThreads), 0, st, lp, V, keys,
+           status);
+  launch_k(chain_finalize_kernel, dim3(b), dim3(32), 0, st, keys, D, root_tok, tok, parent, depth, score, anc,
+           status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
 }  // namespace df

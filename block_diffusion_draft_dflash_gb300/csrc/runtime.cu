@@ -30,7 +30,8 @@ int num_sms() {
 }
 
 cudaError_t ensure_dynamic_smem(const void* func, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;  // no opt-in needed
+  // Set even for small sizes: a kernel's static shared memory counts against the default
+  // 48 KB as well, so a kernel with both needs the opt-in below that size.
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> g(mu);

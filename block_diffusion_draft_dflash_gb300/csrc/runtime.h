@@ -11,9 +11,10 @@ namespace df {
 // SM count of the current device (cached per device).
 int num_sms();
 
-// Makes sure `func` may be launched with `bytes` of dynamic shared memory on the current
-// device (cudaFuncSetAttribute once per device and kernel, raised when a larger size is
-// asked for).  Returns cudaSuccess or the error of the attribute call.
+// Makes sure `func` may be launched with `bytes` of dynamic shared memory (beside its
+// static shared memory) on the current device: cudaFuncSetAttribute on the first launch
+// per device and kernel, again when a larger size is asked for.  Returns cudaSuccess or
+// the error of the attribute call.
 cudaError_t ensure_dynamic_smem(const void* func, size_t bytes);
 
 template <typename F>

@@ -8,8 +8,8 @@ call, and runs a step as the four library calls in order:
     dflash_draft_block -> ddtree_build -> dflash_target_tree_forward -> accept_and_compact
 
 Everything stays on the device; the only host work is launching.  ``prefill`` runs the
-prompt through the target as a chain tree (causal mask) and hands its feature rows to
-the first drafter call.
+prompt through the target as a causal chain and hands its feature rows to the first
+drafter call.
 """
 from __future__ import annotations
 
@@ -106,27 +106,25 @@ class DeviceModel:
         return 2 * n
 
 
-def chain_tree(b, T, device="cuda"):
-    """Parent/depth/ancestor arrays of a chain of T nodes (a causal block)."""
-    parent = torch.arange(-1, T - 1, dtype=torch.int32, device=device).repeat(b, 1)
-    depth = torch.arange(T, dtype=torch.int32, device=device).repeat(b, 1)
-    W = (T + 31) // 32
-    n_set = np.clip(np.arange(1, T + 1)[:, None] - 32 * np.arange(W)[None, :], 0, 32)  # bits set per word
-    anc = np.where(n_set >= 32, np.uint64(0xFFFFFFFF), (np.uint64(1) << n_set.astype(np.uint64)) - np.uint64(1))
-    anc_t = torch.from_numpy(anc.astype(np.uint32).view(np.int32)).to(device).repeat(b, 1, 1).contiguous()
-    return parent, depth, anc_t
-
-
 class SpecDecoder:
-    """State and buffers for b sequences; `step()` runs one speculative step on the GPU."""
+    """State and buffers for b sequences; `step()` runs one speculative step on the GPU.
+
+    mode "tree": DDTree, the B most probable prefixes verified as one flattened tree.
+    mode "chain": vanilla DFlash, the drafter's most likely token at each of the D
+    positions verified as one chain (B is then D).
+    """
 
     def __init__(self, target: DeviceModel, drafter: DeviceModel, b: int, B: int, cap: int, prompt_len: int = 0,
-                 device="cuda"):
+                 device="cuda", mode: str = "tree"):
+        assert mode in ("tree", "chain")
         ts, ds = target.shape, drafter.shape
         self.t, self.d = target, drafter
-        self.b, self.B = b, B
+        self.mode = mode
         self.L = ds.block_size
         self.D = self.L - 1
+        if mode == "chain":
+            B = self.D
+        self.b, self.B = b, B
         self.T = B + 1
         self.cap = cap
         self.device = device
@@ -154,7 +152,8 @@ class SpecDecoder:
         self.acc = dict(n_new=self.n_new, acc_tok=zi(b, self.max_new), n_acc=zi(b), new_bonus=self.bonus,
                         src_slot=zi(b, self.max_new))
         self.ws_draft = _lib.Workspace(_lib.draft_block_workspace_size(drafter.cfg, b, self.max_new), device)
-        self.ws_tree = _lib.Workspace(_lib.ddtree_build_workspace_size(b, self.D, ds.vocab, B), device)
+        self.ws_tree = _lib.Workspace(_lib.chain_build_workspace_size(b, self.D) if mode == "chain" else
+                                      _lib.ddtree_build_workspace_size(b, self.D, ds.vocab, B), device)
         self.ws_verify = _lib.Workspace(_lib.target_tree_forward_workspace_size(target.cfg, b, T), device)
         self.ws_accept = _lib.Workspace(_lib.accept_and_compact_workspace_size(b, T), device)
         self.prompt_len = prompt_len
@@ -170,11 +169,11 @@ class SpecDecoder:
         """Prompt pass through the target (chain tree at N = 0); sets the first bonus token."""
         b, P = prompt.shape
         assert P == self.prompt_len
-        parent, depth, anc = chain_tree(b, P, self.device)
         choice = torch.zeros(b, P, dtype=torch.int32, device=self.device)
         self.cache_len.zero_()
         self.ctx_len.zero_()
-        _lib.target_tree_forward(self.t.cfg, self.t.weights, prompt.to(torch.int32).contiguous(), depth, anc,
+        # depth and ancestor rows omitted: the library runs the rows as a causal chain
+        _lib.target_tree_forward(self.t.cfg, self.t.weights, prompt.to(torch.int32).contiguous(), None, None,
                                  self.k_cache, self.v_cache, self.cache_len, choice, self.prompt_feat, self.ws_prefill)
         self.cache_len.fill_(P)
         self.bonus.copy_(choice[:, -1])
@@ -192,7 +191,10 @@ class SpecDecoder:
                              self.ctx_len, self.bonus, self.logprobs, self.ws_draft)
 
     def build_tree(self):
-        _lib.ddtree_build(self.logprobs, self.B, self.tree, self.ws_tree, root_tok=self.bonus)
+        if self.mode == "chain":
+            _lib.chain_build(self.logprobs, self.tree, self.ws_tree, root_tok=self.bonus)
+        else:
+            _lib.ddtree_build(self.logprobs, self.B, self.tree, self.ws_tree, root_tok=self.bonus)
 
     def verify(self):
         _lib.target_tree_forward(self.t.cfg, self.t.weights, self.tree["tok"], self.tree["depth"], self.tree["anc"],

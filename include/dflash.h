@@ -186,6 +186,27 @@ int ddtree_build_static(const float* logprobs, int b, int D, int V, int B, const
                         df_stream stream);
 
 /* ------------------------------------------------------------------------------------
+ * dflash_chain_build -- the vanilla DFlash draft: one chain of the per-position argmax.
+ *
+ * [DDTree] "실험 결과": DDTree is compared with plain DFlash at the same block size, which
+ * verifies the drafter's block as it is: the most likely token at every position, one
+ * causal chain.  [DFlash] "DFlash의 핵심 아이디어" (3): the block is drafted in one pass
+ * and checked by the target in one pass.
+ *
+ * Same inputs and output layout as ddtree_build with B = D: node i (1..D) is position i's
+ * most likely token (lowest id among exactly equal log-probs), parent i - 1, depth i,
+ * score = fp32 sum of the log-probs of positions 1..i added root first; ancestor row i has
+ * bits 0..i set (a causal mask).  NaN log-probs -> DF_ERR_NAN (device), outputs unwritten.
+ *   logprobs  [b][D][V] fp32;  root_tok [b] or NULL (tok[s][0] = -1)
+ *   tok, parent, depth [b][D+1] int32;  score [b][D+1] fp32;  anc [b][D+1][ceil((D+1)/32)]
+ * Limits: 1 <= D <= 31, V >= 1.
+ * ------------------------------------------------------------------------------------ */
+size_t dflash_chain_build_workspace_size(int b, int D);
+int dflash_chain_build(const float* logprobs, int b, int D, int V, const int32_t* root_tok,
+                       int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* anc,
+                       void* ws, size_t ws_bytes, df_stream stream);
+
+/* ------------------------------------------------------------------------------------
  * tree_verify_attention -- ancestor-only attention of flattened tree rows (DDTree).
  *
  * [DDTree] "방법론 자세히 보기": the flattened tree goes through the target in one pass;
@@ -220,9 +241,12 @@ int tree_verify_attention(int b, int n_tree, int Hq, int Hkv, int hd,
  * its K/V go to slot cache_len[s] + i of every layer; attention is tree_verify_attention.
  * Outputs the greedy choice (argmax, lowest id on ties) after every node and the residual
  * outputs of the feature layers.  With n_tree = 1 this is one plain decode step; with a
- * chain (parent i-1, causal anc) it is a prompt pass.
+ * chain it is a prompt pass ([DFlash] "DFlash의 핵심 아이디어" (1, 2): the prompt's
+ * feature rows become the drafter's first context).
  *
  *   tok, depth [b][n_tree] int32;  anc [b][n_tree][ceil(n_tree/32)] uint32
+ *             depth and anc both NULL: the rows are a chain (a causal prompt pass): row i
+ *             is rotated at cache_len + i and sees tree slots 0 .. i
  *   k_cache   [n_layers][b][Hkv][cap][hd],  v_cache [n_layers][b][Hkv][hd][cap]  bf16
  *   cache_len [b] int32 (not modified); needs cache_len + n_tree <= cap
  *   choice    [b][n_tree] int32 out

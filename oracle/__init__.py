@@ -20,6 +20,9 @@ Sources, cited by page and section throughout:
 Parity pins (see tests/test_oracle_*.py):
   ddtree.build_tree       brute-force top-B enumeration, prefix-closed optimality,
                           Monte-Carlo acceptance identity.      PINNED
+  ddtree.build_chain      exhaustive search over all token sequences (the chain is
+                          the best sequence, ties to the lowest ids); equals build_tree
+                          with B = D when each position has a dominant token.  PINNED
   ddtree.log_softmax      normalisation, shift invariance, scipy.     PINNED
   ddtree.topk_sorted      heapq.nlargest on the same key.            PINNED
   model.rms_norm / rope   closed forms (unit RMS, rotation, relative position). PINNED

@@ -104,6 +104,31 @@ def build_tree(lp: np.ndarray, B: int):
                 rank=np.array(rank, np.int32))
 
 
+def build_chain(lp: np.ndarray):
+    """Vanilla DFlash draft: the most likely token at every position, as one chain.
+
+    [DDTree] section "실험 결과": DDTree is measured against plain DFlash at the same block
+    size, which verifies the drafter's block as it stands, one token per position.
+    [DFlash] section "DFlash의 핵심 아이디어" (3): one drafter pass fills the block.
+    Readings: the most likely token is the lowest id among exactly equal log-probs (the
+    same rule as the greedy target); the chain uses the tree's arrays (root = index 0,
+    node i at depth i with parent i - 1, fp32 score summed root first).
+    """
+    lp = np.asarray(lp, dtype=np.float32)
+    if np.isnan(lp).any():
+        raise TreeError("NaN log-probability")
+    D, V = lp.shape
+    tok, parent, depth, score = [-1], [-1], [0], [np.float32(0.0)]
+    for d in range(D):
+        i = int(np.argmax(lp[d]))  # first occurrence of the maximum = lowest id
+        tok.append(i)
+        parent.append(d)
+        depth.append(d + 1)
+        score.append(np.float32(score[-1] + lp[d, i]))
+    return dict(tok=np.array(tok, np.int32), parent=np.array(parent, np.int32),
+                depth=np.array(depth, np.int32), score=np.array(score, np.float32))
+
+
 def ancestor_mask(parent: np.ndarray) -> np.ndarray:
     """Bit j of row i is set iff node j is node i or one of its ancestors.
 

@@ -94,3 +94,49 @@ def test_budget_over_prefix_count_rejected():
                                    for k in ("tok", "parent", "depth", "anc")} |
                           {"score": torch.zeros(1, 14, device="cuda")}, _lib.Workspace(4096))
     assert e.value.code == -1
+
+
+def _gpu_chain(lp, root=None):
+    from gpu_util import tree_out
+    b, D, V = lp.shape
+    lp_t = torch.from_numpy(np.ascontiguousarray(lp, dtype=np.float32)).cuda()
+    out = tree_out(b, D + 1)
+    ws = _lib.Workspace(_lib.chain_build_workspace_size(b, D))
+    root_t = None if root is None else torch.as_tensor(root, dtype=torch.int32, device="cuda")
+    _lib.chain_build(lp_t, out, ws, root_tok=root_t)
+    torch.cuda.synchronize()
+    st = ws.status()
+    res = {k: v.cpu().numpy() for k, v in out.items()}
+    res["anc"] = res["anc"].view(np.uint32)
+    return res, st
+
+
+@pytest.mark.parametrize("b,D,V,mode", [(64, 15, 151936, "plain"), (3, 15, 151936, "ties"), (2, 31, 1001, "neginf"),
+                                        (4, 1, 7, "ties")])
+def test_chain_build_bit_exact(b, D, V, mode):
+    # vanilla DFlash: the per-position argmax chain, bit-exact against the oracle
+    x = synth.ddtree_logits(1002, b, D, V)
+    if mode == "ties":
+        x = np.round(x)          # many exactly equal log-probs, the maximum among them
+    lp = ddtree.log_softmax(x)
+    if mode == "neginf":
+        lp[np.random.default_rng(0).random(lp.shape) < 0.5] = -np.inf
+        lp[0, 0, :] = -np.inf    # a whole row of -inf: the chain takes id 0
+    root = list(range(100, 100 + b))
+    g, st = _gpu_chain(lp, root)
+    assert st == 0
+    for s in range(b):
+        o = ddtree.build_chain(lp[s])
+        assert g["tok"][s][0] == root[s]
+        np.testing.assert_array_equal(g["tok"][s][1:], o["tok"][1:])
+        np.testing.assert_array_equal(g["parent"][s], o["parent"])
+        np.testing.assert_array_equal(g["depth"][s], o["depth"])
+        np.testing.assert_array_equal(g["score"][s].view(np.uint32), o["score"].view(np.uint32))
+        np.testing.assert_array_equal(g["anc"][s], ddtree.ancestor_mask(o["parent"]))
+
+
+def test_chain_nan_is_reported():
+    lp = ddtree.log_softmax(np.random.default_rng(3).normal(size=(2, 3, 500)))
+    lp[1, 2, 499] = np.nan
+    _, st = _gpu_chain(lp)
+    assert st == -6

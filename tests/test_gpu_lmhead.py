@@ -92,7 +92,7 @@ def test_logsoftmax_full_vocab_within_1e3(embed, M):
     W, W_host = W0.clone(), Wh0.copy()
     X = synth.normal(3003, f"lmhead.lsX{M}", (M, K))
     # a few rows with a dominant token (peaked distributions) beside flat ones
-    _plant_rows(X, W, W_host, [(t, 1000 + 7919 * t) for t in range(0, M, 3)])
+    _plant_rows(X, W, W_host, [(t, (1000 + 7919 * t) % V) for t in range(0, M, 3)])
     out = torch.full((M, V), np.nan, dtype=torch.float32, device="cuda")
     ws = _lib.linear_logsoftmax(bf16_dev(X), W, out)
     torch.cuda.synchronize()

@@ -113,14 +113,14 @@ def test_draft_block_matches_oracle(models, b, ctx0, n_new):
                 rel_close(gv[l], ctx.v[l][ctx0[s]:n1].transpose(1, 2, 0))
 
 
-@pytest.mark.parametrize("B", [16, DS.block_size - 1])  # a tree, and a budget of D nodes (the DFlash chain size)
-def test_speculative_loop_is_lossless(models, B):
+@pytest.mark.parametrize("mode,B", [("tree", 16), ("chain", 0)])  # DDTree, and vanilla DFlash (argmax chain)
+def test_speculative_loop_is_lossless(models, mode, B):
     """Spec output equals the target's greedy choice at every position whose margin is clear."""
     tw, dw, tm, dm = models
     b, P, n_gen, cap = 2, 40, 48, 512
     prompt = synth.uniform_ints(2001, "prompt", (b, P), 0, TS.vocab)
     ref = [step.greedy_generate(tw, prompt[s], n_gen + 16, cap) for s in range(b)]
-    dec = engine.SpecDecoder(tm, dm, b, B, cap, prompt_len=P)
+    dec = engine.SpecDecoder(tm, dm, b, B, cap, prompt_len=P, mode=mode)
     dec.prefill(torch.from_numpy(prompt).cuda())
     outs = [[int(x)] for x in dec.bonus.cpu().tolist()]
     rng = np.random.default_rng(5)
@@ -226,3 +226,44 @@ def test_target_tree_forward_qwen3_width():
     # the tree rows' K/V went to slots N .. N + B of the cache
     ok = to_np(k)[0, 0][:, N[0]:N[0] + T].transpose(1, 0, 2)
     rel_close(ok, cache.k[0][N[0]:N[0] + T])
+
+
+def test_prefill_and_first_context_match_oracle(models):
+    # prompt scale: 2 x 1024 prompt rows, so the target's GEMMs run several token tiles of 256
+    # (M = 2048) and the attention a causal tail of 1024 keys (no ancestor bitmask: the library
+    # masks the chain itself); then the drafter fuses all 1024 feature rows into its context
+    tw, dw, tm, dm = models
+    b, P = 2, 1024
+    cap = P + 64
+    prompt = synth.uniform_ints(2002, "long_prompt", (b, P), 0, TS.vocab)
+    dec = engine.SpecDecoder(tm, dm, b, 16, cap, prompt_len=P)
+    choice = dec.prefill(torch.from_numpy(prompt).cuda())
+    dec.draft()
+    torch.cuda.synchronize()
+    assert dec.ws_prefill.status() == 0 and dec.ws_draft0.status() == 0
+    assert dec.ctx_len.cpu().tolist() == [P] * b
+    g_choice = choice.cpu().numpy()
+    g_feat = to_np(dec.prompt_feat)
+    g_lp = dec.logprobs.cpu().numpy()
+    bonus = dec.bonus.cpu().numpy()
+    for s in range(b):
+        cache = step.KVCache.empty(TS, cap)
+        och, ofeat, ologits = step.target_tree_forward(tw, prompt[s], np.arange(-1, P - 1), np.arange(P), cache, 0)
+        rel_close(g_feat[s], ofeat)
+        _clear_choice(g_choice[s], och, ologits)
+        gk = to_np(dec.k_cache[:, s, :, :P])            # [L][Hkv][P][hd]
+        gv = to_np(dec.v_cache[:, s, :, :, :P])         # [L][Hkv][hd][P]
+        for l in range(TS.n_layers):
+            rel_close(gk[l], cache.k[l][:P].transpose(1, 0, 2))
+            rel_close(gv[l], cache.v[l][:P].transpose(1, 2, 0))
+        # the first drafter call on the GPU's own feature rows and bonus token
+        ctx = step.KVCache.empty(DS, cap)
+        olp, n1, _ = step.draft_block(dw, g_feat[s].astype(np.float64), ctx, 0, int(bonus[s]))
+        assert n1 == P
+        rel_close(g_lp[s], olp)
+        np.testing.assert_allclose(np.exp(g_lp[s].astype(np.float64)).sum(-1), 1.0, atol=1e-3)
+        ck = to_np(dec.ctx_k[:, s, :, :P])
+        cv = to_np(dec.ctx_v[:, s, :, :, :P])
+        for l in range(DS.n_layers):
+            rel_close(ck[l], ctx.k[l][:P].transpose(1, 0, 2))
+            rel_close(cv[l], ctx.v[l][:P].transpose(1, 2, 0))

@@ -5,6 +5,7 @@ every prefix, an exhaustive search over prefix-closed trees, Monte-Carlo samplin
 factorized distribution, a library sort, or a closed form.
 """
 import heapq
+import itertools
 
 import numpy as np
 import pytest
@@ -145,3 +146,53 @@ def test_parents_precede_children_at_config_scale():
     assert np.all(t["depth"][1:] == t["depth"][t["parent"][1:]] + 1)
     s = t["score"][1:].astype(np.float64)
     assert np.all(np.diff(s) <= 0)  # pop order is by score
+
+
+@pytest.mark.parametrize("V,D", [(2, 4), (3, 3), (5, 2), (4, 4)])
+@pytest.mark.parametrize("mode", ["plain", "ties", "neginf"])
+def test_chain_is_best_sequence_by_exhaustive_search(V, D, mode):
+    # the DFlash chain: over all V^D token sequences, the one whose fp32 root-first sum is
+    # largest, and among those the lexicographically lowest ids
+    g = np.random.default_rng(V * 10 + D)
+    x = g.normal(0, 2, size=(D, V))
+    if mode == "ties":
+        x = np.round(x)
+    lp = ddtree.log_softmax(x)
+    if mode == "neginf":
+        lp[g.random(lp.shape) < 0.3] = -np.inf
+    best, best_seq = None, None
+    for seq in itertools.product(range(V), repeat=D):   # lexicographic order
+        s = np.float32(0.0)
+        for d, t in enumerate(seq):
+            s = np.float32(s + lp[d, t])
+        if best is None or s > best:
+            best, best_seq = s, seq
+    c = ddtree.build_chain(lp)
+    np.testing.assert_array_equal(c["tok"][1:], best_seq)
+    assert c["score"][-1].view(np.uint32) == np.float32(best).view(np.uint32)
+    np.testing.assert_array_equal(c["parent"], np.arange(-1, D))
+    np.testing.assert_array_equal(c["depth"], np.arange(D + 1))
+    # every prefix score is the fp32 running sum, root first
+    run = np.float32(0.0)
+    for d in range(D):
+        run = np.float32(run + lp[d, c["tok"][d + 1]])
+        assert c["score"][d + 1].view(np.uint32) == run.view(np.uint32)
+
+
+def test_chain_equals_tree_of_budget_d_with_dominant_tokens():
+    D, V = 7, 300
+    g = np.random.default_rng(21)
+    x = g.normal(0, 1, size=(D, V))
+    x[np.arange(D), g.integers(0, V, size=D)] += 25.0
+    lp = ddtree.log_softmax(x)
+    c, t = ddtree.build_chain(lp), ddtree.build_tree(lp, D)
+    for k in ("tok", "parent", "depth"):
+        np.testing.assert_array_equal(c[k], t[k])
+    np.testing.assert_array_equal(c["score"].view(np.uint32), t["score"].view(np.uint32))
+
+
+def test_chain_nan_rejected():
+    lp = _rand_lp(1, 3, 5)
+    lp[2, 1] = np.nan
+    with pytest.raises(ddtree.TreeError):
+        ddtree.build_chain(lp)
