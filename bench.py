@@ -4,12 +4,21 @@ Workload (default): one DFlash + DDTree speculative step per iteration, b = 1 se
   target: 36 layers, d 4096, 32 q / 8 kv heads x 128, SwiGLU 12288, vocab 151936, bf16;
   drafter: 5 layers of the same width, context fused from 5 target layers;
   block 16 (15 draft depths), tree budget B = 256, 4096-token context (prefilled
-  untimed through the same library), random-init weights (std 0.02), random prompt.
-A step = dflash_draft_block -> ddtree_build -> dflash_target_tree_forward ->
+  untimed through the same library), random-init weights (std 0.02), random prompt;
+  acceptance planted at rate 0.9 (the drafter's log-probs lean on the target's own greedy
+  continuation at each depth with that probability; harness kernel in the timed step).
+A step = dflash_draft_block -> (plant) -> ddtree_build -> dflash_target_tree_forward ->
 accept_and_compact, captured once as a CUDA graph and replayed.
 
   python bench.py [--gpus N --steps K --warmup W --batch b --budget B --ctx N]
-  python bench.py --impl reference     (the CPU oracle, timed on a bounded sample)
+                  [--accept-rate r] [--draft-mode tree|chain]
+  python bench.py --mode ddtree    DDTree build alone: b = 64, vocab 151936, B swept
+  python bench.py --mode draft     drafter forward alone: ctx 2048, b = 1, 4, 16
+  python bench.py --mode verify    tree attention alone (B = 256, 512 x ctx 2048, 4096,
+                                   8192), then walk + compaction over 36 layers
+  python bench.py --mode prefill   prompt pass (target chain + drafter context), 512 and
+                                   4096 tokens
+  python bench.py --impl reference (the CPU oracle, timed on a bounded sample)
 
 Several GPUs run independent replicas (the step has no cross-sequence exchange):
 weak scaling, value = sum over ranks.
@@ -39,8 +48,16 @@ def parse():
     ap.add_argument("--budget", type=int, default=256)
     ap.add_argument("--ctx", type=int, default=4096)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--mode", default="step", choices=["step", "ddtree", "draft", "verify", "prefill"])
+    ap.add_argument("--accept-rate", type=float, default=0.9,
+                    help="probability per draft depth that the drafter's log-probs lean on the target's greedy "
+                         "continuation (0 = no planting)")
+    ap.add_argument("--plant-bias", type=float, default=16.0, help="logit bias of a planted token")
+    ap.add_argument("--draft-mode", default="tree", choices=["tree", "chain"],
+                    help="tree: DDTree of B nodes; chain: vanilla DFlash (argmax chain of 15)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree", "layer"],
+    ap.add_argument("--oracle-sample-json", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree", "draft", "layer"],
                     help="run one small isolated case of a kernel a few times (for ncu captures), no JSON")
     ap.add_argument("--case-n", type=int, default=24576, help="gemm case: weight rows (output features)")
     ap.add_argument("--case-k", type=int, default=4096, help="gemm case: reduction length")
@@ -48,16 +65,19 @@ def parse():
 
 
 def workload_name(a):
+    draft = f"B={a.budget}" if a.draft_mode == "tree" else "DFlash chain of 15 (no tree)"
     return (f"DFlash+DDTree spec step, Qwen3-8B-shaped target (36L) + 5L drafter, block 16, "
-            f"B={a.budget}, ctx {a.ctx}, b={a.batch}")
+            f"{draft}, ctx {a.ctx}, b={a.batch}, acceptance planted at {a.accept_rate}")
 
 
-def config(a):
-    return {"workload": workload_name(a), "global_batch": a.batch * a.gpus, "block": 16, "budget": a.budget,
-            "ctx": a.ctx, "target_layers": 36, "drafter_layers": 5, "vocab": 151936,
+def config(a, impl="gb300"):
+    timing = ("CUDA graph replay of whole steps, CUDA events on the launching stream" if impl == "gb300" else
+              "oracle on the host cores: wall-clock of a bounded sample of one step, scaled to the whole step")
+    return {"workload": workload_name(a), "global_batch": a.batch * a.gpus, "block": 16,
+            "budget": a.budget if a.draft_mode == "tree" else 15, "draft_mode": a.draft_mode,
+            "accept_rate": a.accept_rate, "ctx": a.ctx, "target_layers": 36, "drafter_layers": 5, "vocab": 151936,
             "l2": "inputs larger than L2 (about 17 GB of weights streamed per step)",
-            "timing": "CUDA graph replay of whole steps, CUDA events on the launching stream",
-            "parallelism": f"replicas x{a.gpus}"}
+            "timing": timing, "parallelism": f"replicas x{a.gpus}"}
 
 
 # ------------------------------------------------------------------------ oracle timing
@@ -116,18 +136,36 @@ def oracle_sample(a, budget_s=25.0):
     t_head_row = (time.perf_counter() - t0) / 2 * (TS.vocab / Vs)
     est = t_tree + t_layer * (T / rows) * TS.n_layers + t_dlayer * DS.n_layers + t_head_row * (T + 15)
     wall = time.perf_counter() - t_all
-    cores = os.cpu_count()
-    try:
-        from threadpoolctl import threadpool_info  # type: ignore
-        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=cores)
-    except Exception:
-        pass
-    return {"value": 1.0 / est, "unit": "spec steps/s", "cores": cores, "kind": "oracle",
-            "sample": (f"oracle (numpy fp64, BLAS on all cores, Python loops on one) timed on: DDTree build B={B}; "
-                       f"1 target layer x {rows} of {T} tree rows (ctx {N}); 1 drafter layer x 16 rows; 2 LM-head "
-                       f"rows x {Vs} vocab; scaled to 36+5 layers, {T} tree rows, {T + 15} full LM-head rows, "
-                       f"b=1 (sample wall {wall:.1f}s)"),
-            "est_s_per_step": est}
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0) or (os.cpu_count() or 1)
+    return {"value": 1.0 / est, "unit": "spec steps/s", "cores": threads, "kind": "oracle",
+            "sample": (f"oracle (numpy fp64, BLAS on {threads} thread(s), Python loops on one) timed on: DDTree "
+                       f"build B={B}; 1 target layer x {rows} of {T} tree rows (ctx {N}); 1 drafter layer x 16 rows; "
+                       f"2 LM-head rows x {Vs} vocab; scaled to 36+5 layers, {T} tree rows, {T + 15} full LM-head "
+                       f"rows, b=1 (sample wall {wall:.1f}s)"),
+            "est_s_per_step": est, "sample_wall_s": wall}
+
+
+def oracle_sample_threads(a, threads):
+    """oracle_sample in a child process whose BLAS is limited to `threads` threads."""
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--oracle-sample-json",
+                        "--budget", str(a.budget), "--ctx", str(a.ctx)], env=env, capture_output=True, text=True,
+                       timeout=900)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(a):
+    """The oracle on all host cores (the reported value) and on one thread, same sample."""
+    cb = oracle_sample(a)
+    one = oracle_sample_threads(a, 1)
+    out = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    out["nproc"] = os.cpu_count()
+    out["one_thread_value"] = one["value"] if one else None
+    return out, cb
 
 
 # ------------------------------------------------------------------------------ GPU arm
@@ -180,7 +218,7 @@ class Clocks:
 
 
 # kernels launched per traced call of each class (the rest launch one kernel per call)
-KERNELS_PER_CALL = {"topk": 4, "accept_compact": 3, "logsoftmax": 2}
+KERNELS_PER_CALL = {"topk": 4, "accept_compact": 3, "logsoftmax": 2, "chain": 3}
 
 
 def gemm_algorithmic(b, B, nd_ctx_rows=16):
@@ -296,6 +334,44 @@ def step_roofline_ms(b, B, N, hbm_gbs, tc_tflops):
     return t * 1e3, sum(p[0] for p in parts)
 
 
+def load_peaks():
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        peaks = {}
+    return (float(peaks.get("hbm_gbs", 6800.0)), float(peaks.get("bf16_tflops", 1900.0)),
+            float(peaks.get("bf16_tflops_sustained", 1700.0)), "measured" if peaks else "fallback")
+
+
+def greedy_reference(dec, prompt, n, dev):
+    """The target's own greedy continuation of each prompt: prefill, then n plain decode
+    steps through the library (one node per sequence per call).  Returns [b][P + n + 1]
+    int32 on the device (prompt, then the greedy tokens); leaves the caches dirty (the
+    caller prefills again)."""
+    import torch
+
+    from block_diffusion_draft_dflash_gb300 import _lib
+    b, P = prompt.shape
+    dec.prefill(prompt)
+    ref = torch.zeros(b, P + n + 1, dtype=torch.int32, device=dev)
+    ref[:, :P] = prompt.to(torch.int32)
+    ref[:, P] = dec.bonus
+    tok = dec.bonus.clone().view(b, 1)
+    depth = torch.zeros(b, 1, dtype=torch.int32, device=dev)
+    anc = torch.ones(b, 1, 1, dtype=torch.int32, device=dev)
+    ch = torch.zeros(b, 1, dtype=torch.int32, device=dev)
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(dec.t.cfg, b, 1), dev)
+    for i in range(n):
+        _lib.target_tree_forward(dec.t.cfg, dec.t.weights, tok, depth, anc, dec.k_cache, dec.v_cache, dec.cache_len,
+                                 ch, None, ws)
+        dec.cache_len.add_(1)
+        ref[:, P + 1 + i] = ch[:, 0]
+        tok.copy_(ch)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    return ref
+
+
 def run_gpu(a, rank, world, local_rank):
     import numpy as np
     import torch
@@ -307,28 +383,35 @@ def run_gpu(a, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     _lib.load()
     assert _lib.load().dflash_check_device() == 0, "needs a compute-capability 10.3 GPU"
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except Exception:
-        pass
-    hbm = float(peaks.get("hbm_gbs", 6800.0))
-    tc_burst = float(peaks.get("bf16_tflops", 1900.0))
-    tc_sust = float(peaks.get("bf16_tflops_sustained", 1700.0))
-    peak_src = "measured" if peaks else "fallback"
+    hbm, tc_burst, tc_sust, peak_src = load_peaks()
 
     TS, DS = synth.QWEN3_8B_TARGET, synth.DFLASH_QWEN3_8B_DRAFTER
     seed = 1000 + 5 + rank
     tm = engine.DeviceModel.random(TS, seed, "target", dev)
     dm = engine.DeviceModel.random(DS, seed, "drafter", dev, embed=tm.embed, n_feat=TS.n_feat)
-    b, B, N = a.batch, a.budget, a.ctx
-    n_steps = a.warmup + a.steps + 4
-    cap = ((N + (B + 1) + 16 * (n_steps + 2) + 64) + 127) // 128 * 128
-    dec = engine.SpecDecoder(tm, dm, b, B, cap, prompt_len=N, device=dev)
+    b, N = a.batch, a.ctx
+    n_steps = 1 + a.warmup + 2 + 2 * a.steps + 3
+    cap = ((N + (a.budget + 1) + 16 * (n_steps + 2) + 64) + 127) // 128 * 128
+    dec = engine.SpecDecoder(tm, dm, b, a.budget, cap, prompt_len=N, device=dev, mode=a.draft_mode)
+    B, T = dec.B, dec.T
     prompt = torch.from_numpy(synth.uniform_ints(seed, "prompt", (b, N), 0, TS.vocab)).to(dev)
-    dec.prefill(prompt)
-    dec.step()  # first step builds the drafter's context over the whole prompt
+    ref = None
+    if a.accept_rate > 0:
+        # untimed: the target's greedy continuation, which the plant leans the drafter on
+        ref = greedy_reference(dec, prompt, 16 * n_steps + 16, dev)
+        dec.plant = lambda d: _lib.plant_logprobs(d.logprobs, ref, d.cache_len, a.accept_rate, a.plant_bias,
+                                                  seed)
+    # prompt pass and the drafter's first context build, timed once each (untimed region)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     torch.cuda.synchronize()
+    ev[0].record()
+    dec.prefill(prompt)
+    ev[1].record()
+    dec.step()  # first step: the drafter's context over the whole prompt, then a full step
+    ev[2].record()
+    torch.cuda.synchronize()
+    prefill = {"prompt_tokens": N, "target_chain_ms": round(ev[0].elapsed_time(ev[1]), 3),
+               "first_step_ms": round(ev[1].elapsed_time(ev[2]), 3)}
     # free the prefill-only buffers
     del dec.ws_prefill, dec.ws_draft0, dec.prompt_feat
     torch.cuda.empty_cache()
@@ -346,11 +429,11 @@ def run_gpu(a, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     if world > 1:
         torch.distributed.barrier()
+    len0 = dec.cache_len.clone()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # the nvidia-smi samples go to $BENCH_OUT_DIR (default: the temp directory)
     clocks = Clocks(os.path.join(os.environ.get("BENCH_OUT_DIR", tempfile.gettempdir()), f"clocks_rank{rank}.csv"))
-    n_acc_before = None
     with clocks:
         time.sleep(0.3)
         e0.record(stream)
@@ -359,6 +442,7 @@ def run_gpu(a, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / a.steps, world, dev)
+    tau = float((dec.cache_len - len0).sum().item()) / (a.steps * b)  # tokens committed per step and sequence
     st = dec.status()
     assert st == 0, f"device status {st}"
 
@@ -371,7 +455,8 @@ def run_gpu(a, rank, world, local_rank):
     h_n = torch.empty(b, dtype=torch.int32).pin_memory()
     # host-side bookkeeping on numpy views of the same pinned buffers (no per-op dispatch)
     in_np, tok_np, n_np, rows = h_in.numpy(), h_tok.numpy(), h_n.numpy(), np.arange(b)
-    emitted = 0
+    pos_np = dec.cache_len.cpu().numpy().astype(np.int64)  # position of each sequence's bonus token
+    emitted, outs = 0, []
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -383,15 +468,34 @@ def run_gpu(a, rank, world, local_rank):
         h_n.copy_(dec.acc["n_acc"], non_blocking=True)
         torch.cuda.current_stream().synchronize()
         emitted += int(n_np.sum()) + b
+        outs.append((tok_np.copy(), n_np.copy()))
         in_np[:] = tok_np[rows, n_np]  # each sequence's new bonus token follows its accepted ones
     e2e_s = max_over_ranks((time.perf_counter() - t0) / a.steps, world, dev)
+    # the emitted tokens against the greedy reference (outside the timed region): tokens at
+    # positions pos + 1 .. pos + a + 1 of each step
+    mismatch, diverged = 0, 0
+    if ref is not None:
+        ref_np = ref.cpu().numpy()
+        first_bad = np.full(b, -1)
+        for tk, na in outs:
+            for s_ in range(b):
+                n_e = int(na[s_]) + 1
+                lo = int(pos_np[s_]) + 1
+                want = ref_np[s_, lo:lo + n_e]
+                got = tk[s_, :len(want)]
+                bad = int(np.sum(got != want))
+                mismatch += bad
+                if bad and first_bad[s_] < 0:
+                    first_bad[s_] = lo
+                pos_np[s_] += n_e
+        diverged = int(np.sum(first_bad >= 0))
 
     # live per-kernel breakdown (CUDA events around every library launch, eager steps)
     kern, kern_shapes = traced_breakdown(dec, 3)
     # dominant kernel: the target layers' projection GEMMs (gemm_bf16_tc_kernel, partial-tile
     # epilogue), 4 launches per layer; per-launch algorithmic bytes = weights + input rows +
     # output rows (bf16-sized)
-    Mt, d, F = b * (B + 1), 4096, 12288
+    Mt, d, F = b * T, 4096, 12288
     t_bytes = t_flops = t_ms = t_launch = 0.0
     for (Nn, Kk) in ((6144, d), (d, d), (2 * F, d), (d, F)):
         sh = kern_shapes.get(f"gemm {Mt}x{Nn}x{Kk}")
@@ -403,10 +507,10 @@ def run_gpu(a, rank, world, local_rank):
         t_launch += sh["launches_per_step"]
     achieved = t_bytes / (t_ms * 1e-3) / 1e9 if t_ms else 0.0
     traffic = None
-    if b == 1 and B == 256 and gemm_src_hash() == GEMM_TRAFFIC["src_sha256_16"] and t_launch:
+    if b == 1 and T == 257 and gemm_src_hash() == GEMM_TRAFFIC["src_sha256_16"] and t_launch:
         traffic = round(GEMM_TRAFFIC["bytes_per_layer"] / 4)  # per launch, averaged over the four shapes
     g_ms = kern["gemm"]["ms_per_step"]
-    g_bytes, g_flops = gemm_algorithmic(b, B)
+    g_bytes, g_flops = gemm_algorithmic(b, T - 1)
     # the binding resource: HBM while the weights dominate (b = 1: 257 flop per byte, just
     # under the ridge), the tensor cores once b * 257 token rows share each weight byte
     tensor_bound = t_flops / (tc_sust * 1e12) > t_bytes / (hbm * 1e9)
@@ -416,30 +520,355 @@ def run_gpu(a, rank, world, local_rank):
     roof = {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(achieved, 1), "peak": peak_r,
             "unit": "TFLOP/s" if tensor_bound else "GB/s",
             "frac": round(achieved / peak_r, 4), "traffic": traffic,
+            "peak_source": f"{peak_src} ({'sustained bf16' if tensor_bound else 'HBM copy'})",
             "kernel": "gemm_bf16_tc_kernel (partial-tile epilogue): the 4 projection launches of each of the "
                       "36 target layers",
             "algorithmic_bytes_per_launch": round(t_bytes / t_launch) if t_launch else None,
             "launches_per_step": t_launch, "ms_per_step": round(t_ms, 4),
+            "timing": "CUDA events around each launch, in 3 eager traced steps after the timed replays",
             "tflops": round(t_flops / (t_ms * 1e-3) / 1e12, 1) if t_ms else None,
             "all_projection_gemms": {"ms_per_step": g_ms, "algorithmic_bytes_per_step": g_bytes,
                                      "achieved_gbs": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
                                      "launches_per_step": kern["gemm"]["launches_per_step"]}}
-    t_star_ms, step_bytes = step_roofline_ms(b, B, N, hbm, tc_sust)
+    t_star_ms, step_bytes = step_roofline_ms(b, T - 1, N, hbm, tc_sust)
     clk = clocks.summary(local_rank)
     launches = sum(v["launches_per_step"] * KERNELS_PER_CALL.get(k, 1) for k, v in kern.items())
+    acc = {"rate": a.accept_rate, "bias": a.plant_bias, "tokens_per_step": round(tau, 3),
+           "tokens_per_step_e2e": round(emitted / (a.steps * b), 3),
+           "reference_mismatches": mismatch, "sequences_diverged_from_reference": diverged}
     return dict(ms=ms, e2e_s=e2e_s, emitted=emitted, roof=roof, t_star_ms=t_star_ms, step_bytes=step_bytes,
-                clocks=clk, peak_src=peak_src, hbm=hbm, tc=tc_sust, tau=emitted / (a.steps * b),
+                clocks=clk, peak_src=peak_src, hbm=hbm, tc=tc_sust, tau=tau, acc=acc, prefill=prefill,
                 launches=launches, kernels=kern, kernel_shapes=kern_shapes)
 
 
-def kernel_case(a):
-    """Small isolated launches of one kernel at the step's shapes (device footprint < 2 GB)."""
+# --------------------------------------------------------------------------- other modes
+def synth_logprobs(seed, b, D, V, dev):
+    """fp32 log-probs of the synthetic DDTree logits (torch's log-softmax in float64 on the
+    host: input preparation, not the library)."""
+    import torch
+
+    import synth
+    x = torch.from_numpy(synth.ddtree_logits(seed, b, D, V))
+    return torch.log_softmax(x, dim=-1).to(torch.float32).to(dev)
+
+
+def _timed(fn, warmup, steps):
+    """ms per call of fn() (CUDA events on the current stream, after `warmup` calls)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def _traced(fn, n=3):
+    """{kernel class: ms per call} from the library's launch tracing over n eager calls."""
+    import torch
+
+    from block_diffusion_draft_dflash_gb300 import _lib
+    torch.cuda.synchronize()
+    _lib.trace_read()
+    _lib.trace_enable(True)
+    for _ in range(n):
+        fn()
+    torch.cuda.synchronize()
+    rec = _lib.trace_read()
+    _lib.trace_enable(False)
+    out = {}
+    for tag, (ms, cnt) in rec.items():
+        k = tag.split(" ")[0]
+        out[k] = out.get(k, 0.0) + ms / n
+    return {k: round(v, 4) for k, v in out.items()}
+
+
+def _mode_line(a, mode, metric, value, unit, ms, cfg, roof, higher=True, **extra):
+    line = {"mode": mode, "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": round(ms, 4), "higher_is_better": higher, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if mode != "ddtree" else "f32", "data": "synthetic",
+            "config": cfg, "roofline": roof}
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+def run_ddtree_mode(a):
+    """DDTree build in isolation: b = 64 sequences, block 16, vocab 151936, B swept."""
+    import torch
+
+    import synth
+    from block_diffusion_draft_dflash_gb300 import _lib
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    hbm, _, _, src = load_peaks()
+    b, D, V = 64, 15, 151936
+    lp = synth_logprobs(1002, b, D, V, dev)
+    read = b * D * V * 4  # top-K reads each log-prob row once (algorithmic)
+    for B in (16, 64, 256, 512, 1024):
+        T = B + 1
+        z = lambda *sh, dt=torch.int32: torch.zeros(sh, dtype=dt, device=dev)
+        out = dict(tok=z(b, T), parent=z(b, T), depth=z(b, T), score=z(b, T, dt=torch.float32),
+                   anc=z(b, T, (T + 31) // 32))
+        ws = _lib.Workspace(_lib.ddtree_build_workspace_size(b, D, V, B), dev)
+        fn = lambda: _lib.ddtree_build(lp, B, out, ws)
+        ms = _timed(fn, a.warmup, a.steps)
+        assert ws.status() == 0
+        parts = _traced(fn)
+        topk_ms = parts.get("topk", 0.0)
+        ach = read / (topk_ms * 1e-3) / 1e9 if topk_ms else 0.0
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                "traffic": None, "kernel": "topk_hist + topk_collect + topk_final (one read of the log-probs)",
+                "algorithmic_bytes": read, "peak_source": f"{src} HBM copy",
+                "timing": "CUDA events around each launch, 3 eager calls"}
+        cfg = {"workload": f"DDTree build alone: b={b}, block 16 (D=15), vocab {V}, B={B}; N(0,9) logits + one +8 "
+                           f"spike per position", "b": b, "D": D, "V": V, "budget": B,
+               "l2": "input 584 MB > L2"}
+        _mode_line(a, "ddtree", "DDTree builds/s (b=64 sequences per build)", 1000.0 / ms, "builds/s", ms, cfg, roof,
+                   parts_ms=parts, topk_ms=topk_ms, heap_ms=parts.get("ddtree_heap"),
+                   heap_us_per_pop=round(parts.get("ddtree_heap", 0.0) * 1e3 / B, 4))
+
+
+def run_draft_mode(a):
+    """Drafter forward alone at Qwen3-8B shape: ctx 2048, 16 new context rows, b = 1, 4, 16."""
+    import torch
+
+    import synth
+    from block_diffusion_draft_dflash_gb300 import _lib, engine
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    hbm, _, tc_sust, src = load_peaks()
+    DS, nf, d, V = synth.DFLASH_QWEN3_8B_DRAFTER, 5, 4096, 151936
+    dm = engine.DeviceModel.random(DS, 1003, "drafter", dev, n_feat=nf)
+    ctx, L, max_new = 2048, 16, 16
+    cap = (ctx + max_new + L + 127) // 128 * 128
+    w_bytes = dm.weight_bytes()
+    for b in (1, 4, 16):
+        g_ = lambda sh, name, std=1.0: synth.device_normal(sh, std, 1003, f"draft.{b}.{name}", dev)
+        ck, cv = g_((5, b, 8, cap, 128), "k"), g_((5, b, 8, 128, cap), "v")
+        feat = g_((b, max_new, nf * d), "feat")
+        n_new = torch.full((b,), max_new, dtype=torch.int32, device=dev)
+        len0 = torch.full((b,), ctx, dtype=torch.int32, device=dev)
+        ctx_len = len0.clone()
+        bonus = torch.arange(b, dtype=torch.int32, device=dev) * 7 + 11
+        lp = torch.zeros(b, L - 1, V, dtype=torch.float32, device=dev)
+        ws = _lib.Workspace(_lib.draft_block_workspace_size(dm.cfg, b, max_new), dev)
+
+        def call():
+            ctx_len.copy_(len0)
+            _lib.draft_block(dm.cfg, dm.weights, feat, n_new, ck, cv, ctx_len, bonus, lp, ws)
+        call()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s), torch.cuda.graph(gr, stream=s):
+            call()
+        torch.cuda.current_stream().wait_stream(s)
+        ms = _timed(gr.replay, a.warmup, a.steps)
+        assert ws.status() == 0
+        parts = _traced(call)
+        kv = b * 5 * 8 * 128 * 2 * 2 * (ctx + max_new + L)
+        byts = w_bytes + kv + b * max_new * nf * d * 2 + b * (L - 1) * V * 4
+        t_star = byts / (hbm * 1e9) * 1e3
+        ach = byts / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                "traffic": None, "kernel": "whole dflash_draft_block (CUDA graph)", "algorithmic_bytes": byts,
+                "t_star_ms": round(t_star, 4), "peak_source": f"{src} HBM copy"}
+        cfg = {"workload": f"DFlash drafter forward alone, Qwen3-8B shape (5 layers, d 4096, 32/8 x 128, F 12288, "
+                           f"vocab {V}), ctx {ctx}, {max_new} new context rows, block {L}, b={b}", "b": b,
+               "ctx": ctx, "l2": "inputs larger than L2 (3.3 GB of weights per call)"}
+        _mode_line(a, "draft", "drafter block forwards/s (sequences)", b * 1000.0 / ms, "sequences/s", ms, cfg, roof,
+                   parts_ms=parts)
+        del ck, cv, feat, lp, ws, gr
+        torch.cuda.empty_cache()
+
+
+def run_verify_mode(a):
+    """Tree-verification attention alone (one layer, 32/8 heads x 128), then the greedy walk
+    and compaction of 36 layers' caches."""
     import numpy as np
     import torch
 
     import synth
     from block_diffusion_draft_dflash_gb300 import _lib
-    from oracle import ddtree
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    hbm, tc_burst, _, src = load_peaks()
+    trees = {}
+    lp = synth_logprobs(1002, 4, 15, 151936, dev)
+    for B in (256, 512):  # config-2-style trees, built by the library itself
+        T = B + 1
+        z = lambda *sh, dt=torch.int32: torch.zeros(sh, dtype=dt, device=dev)
+        out = dict(tok=z(4, T), parent=z(4, T), depth=z(4, T), score=z(4, T, dt=torch.float32),
+                   anc=z(4, T, (T + 31) // 32))
+        _lib.ddtree_build(lp, B, out, _lib.Workspace(_lib.ddtree_build_workspace_size(4, 15, 151936, B), dev))
+        trees[B] = out
+    for b in (1, 4):
+        for B in (256, 512):
+            T = B + 1
+            tr = [{k_: v_[s_].cpu().numpy() for k_, v_ in trees[B].items()} for s_ in range(b)]
+            anc = trees[B]["anc"][:b].contiguous()
+            sum_depth = sum(int(np.sum(t["depth"] + 1)) for t in tr)
+            for N in (2048, 4096, 8192):
+                cap = (N + T + 7) // 8 * 8
+                g_ = lambda sh, name: synth.device_normal(sh, 1.0, 1004, f"verify.{b}.{B}.{N}.{name}", dev)
+                q, k, v = g_((b, T, 32, 128), "q"), g_((b, 8, cap, 128), "k"), g_((b, 8, 128, cap), "v")
+                out = torch.zeros_like(q)
+                clen = torch.full((b,), N, dtype=torch.int32, device=dev)
+                ws = _lib.Workspace(_lib.tree_verify_attention_workspace_size(b, T, 32, 8, 128, cap), dev)
+                fn = lambda: _lib.tree_verify_attention(q, k, v, clen, anc, 1 / np.sqrt(128), out, ws)
+                ms = _timed(fn, a.warmup, a.steps)
+                assert ws.status() == 0
+                flops = 4 * 128 * 32 * (b * T * N + sum_depth)
+                byts = b * 8 * 128 * 2 * 2 * (N + T) + 2 * b * T * 32 * 128 * 2
+                ach = flops / (ms * 1e-3) / 1e12
+                roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tc_burst, "unit": "TFLOP/s",
+                        "frac": round(ach / tc_burst, 4), "traffic": None,
+                        "kernel": "attn_tc_kernel (tree mode) + attn_combine", "algorithmic_flops": flops,
+                        "algorithmic_bytes": byts, "hbm_frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4),
+                        "peak_source": f"{src} bf16 burst (kernel timed alone)"}
+                cfg = {"workload": f"tree-verification attention alone, one layer, 32 q / 8 kv heads x 128, b={b}, "
+                                   f"B={B} tree nodes + root, ctx {N}", "b": b, "budget": B, "ctx": N,
+                       "l2": "KV larger than L2 from b=4 or ctx 8192; otherwise re-read across iterations"}
+                _mode_line(a, "verify", "tree attentions/s (one layer)", 1000.0 / ms, "calls/s", ms, cfg, roof)
+                del q, k, v, out, ws
+            # greedy walk + compaction over 36 layers at ctx 4096: each node follows its best child's
+            # token with probability 0.7 (else a token no child has)
+            N = 4096
+            cap = (N + T + 7) // 8 * 8
+            rng = np.random.default_rng(B + b)
+            choice = np.zeros((b, T), np.int32)
+            for s_, t in enumerate(tr):
+                kids = [[] for _ in range(T)]
+                for c in range(1, T):
+                    kids[t["parent"][c]].append(c)
+                for i in range(T):
+                    if kids[i] and rng.random() < 0.7:
+                        choice[s_, i] = t["tok"][kids[i][0]]
+                    else:
+                        choice[s_, i] = 151935 - i  # a token no child of this node carries
+                        while choice[s_, i] in {int(t["tok"][c]) for c in kids[i]}:
+                            choice[s_, i] -= 1
+            i32 = lambda x: torch.from_numpy(np.ascontiguousarray(x).astype(np.int32)).to(dev)
+            tok = i32(np.stack([t["tok"] for t in tr]))
+            par = i32(np.stack([t["parent"] for t in tr]))
+            ch = i32(choice)
+            kc = torch.zeros(36, b, 8, cap, 128, dtype=torch.bfloat16, device=dev)
+            vc = torch.zeros(36, b, 8, 128, cap, dtype=torch.bfloat16, device=dev)
+            feat = torch.zeros(b, T, 5 * 4096, dtype=torch.bfloat16, device=dev)
+            nfeat = torch.zeros(b, 16, 5 * 4096, dtype=torch.bfloat16, device=dev)
+            len0 = torch.full((b,), N, dtype=torch.int32, device=dev)
+            clen = len0.clone()
+            o = {k_: torch.zeros(b, *(() if k_ in ("n_new", "n_acc", "new_bonus") else (16,)), dtype=torch.int32,
+                                 device=dev) for k_ in ("n_new", "acc_tok", "n_acc", "new_bonus", "src_slot")}
+            ws = _lib.Workspace(_lib.accept_and_compact_workspace_size(b, T), dev)
+
+            def acc_call():
+                clen.copy_(len0)
+                _lib.accept_and_compact(ch, tok, par, kc, vc, clen, feat, nfeat, o, ws)
+            ms = _timed(acc_call, a.warmup, a.steps)
+            assert ws.status() == 0
+            n_acc = o["n_acc"].cpu().numpy()
+            moved = int(n_acc.sum()) * 36 * 8 * 128 * 2 * 2 * 2 + int(n_acc.sum() + b) * 5 * 4096 * 2 * 2
+            roof = {"bound": "hbm", "achieved": round(moved / (ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(moved / (ms * 1e-3) / 1e9 / hbm, 6), "traffic": None,
+                    "kernel": "accept_walk + compact + gather_feat (latency-bound: a few MB)",
+                    "algorithmic_bytes": moved, "peak_source": f"{src} HBM copy"}
+            cfg = {"workload": f"greedy walk + KV compaction, 36 layers x 8 kv heads, b={b}, B={B}, ctx {N}, "
+                               f"planted target choices (best child followed with p=0.7)", "b": b, "budget": B,
+                   "accepted": n_acc.tolist()}
+            _mode_line(a, "verify", "accept+compact calls/s", 1000.0 / ms, "calls/s", ms, cfg, roof)
+            del kc, vc, feat, nfeat, ws
+            torch.cuda.empty_cache()
+
+
+def run_prefill_mode(a):
+    """The prompt pass: the target over the prompt as one causal chain (36 layers, greedy
+    choice per row, feature capture), then the drafter's first call over all prompt rows."""
+    import torch
+
+    import synth
+    from block_diffusion_draft_dflash_gb300 import _lib, engine
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    hbm, _, tc_sust, src = load_peaks()
+    TS, DS = synth.QWEN3_8B_TARGET, synth.DFLASH_QWEN3_8B_DRAFTER
+    tm = engine.DeviceModel.random(TS, 1006, "target", dev)
+    dm = engine.DeviceModel.random(DS, 1006, "drafter", dev, embed=tm.embed, n_feat=TS.n_feat)
+    d, F, V = 4096, 12288, 151936
+    per_layer = 6144 * d + d * 4096 + 2 * F * d + d * F
+    for P in (512, 4096):
+        b = 1
+        cap = (P + 64 + 127) // 128 * 128
+        dec = engine.SpecDecoder(tm, dm, b, 16, cap, prompt_len=P, device=dev)
+        prompt = torch.from_numpy(synth.uniform_ints(1006, f"prefill{P}", (b, P), 0, V)).to(dev)
+
+        def call():
+            dec.prefill(prompt)
+            dec.draft()
+        call()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        t_ms, d_ms = [], []
+        for _ in range(a.warmup + a.steps):
+            ev[0].record()
+            dec.prefill(prompt)
+            ev[1].record()
+            dec.draft()
+            ev[2].record()
+            torch.cuda.synchronize()
+            t_ms.append(ev[0].elapsed_time(ev[1]))
+            d_ms.append(ev[1].elapsed_time(ev[2]))
+        t_ms, d_ms = sorted(t_ms[a.warmup:]), sorted(d_ms[a.warmup:])
+        tm_ms, dm_ms = t_ms[len(t_ms) // 2], d_ms[len(d_ms) // 2]
+        assert dec.ws_prefill.status() == 0 and dec.ws_draft0.status() == 0
+        parts = _traced(call, 2)
+        t_flops = 2 * b * P * (36 * per_layer + V * d) + 36 * 4 * 128 * 32 * b * P * (P + 1) // 2
+        d_flops = 2 * b * P * (5 * d * d + 5 * 6144 * d) + 2 * 16 * b * (5 * per_layer + V * d)
+        t_bytes = 2 * (36 * per_layer + V * d)
+        ms = tm_ms + dm_ms
+        flops = t_flops + d_flops
+        t_star = max(flops / (tc_sust * 1e12), (t_bytes + 2 * (5 * per_layer + 5 * d * d)) / (hbm * 1e9)) * 1e3
+        ach = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tc_sust, "unit": "TFLOP/s",
+                "frac": round(ach / tc_sust, 4), "traffic": None,
+                "kernel": "whole prompt pass (target chain forward + drafter context build)",
+                "algorithmic_flops": flops, "t_star_ms": round(t_star, 3),
+                "peak_source": f"{src} bf16 sustained"}
+        cfg = {"workload": f"prompt pass of {P} tokens, Qwen3-8B-shaped target (36L) + 5L drafter, b={b}",
+               "prompt": P, "b": b, "l2": "inputs larger than L2 (17 GB of weights)"}
+        _mode_line(a, "prefill", "prompt tokens/s (target chain + drafter context)", b * P * 1000.0 / ms,
+                   "tokens/s", ms, cfg, roof, target_chain_ms=round(tm_ms, 3), drafter_context_ms=round(dm_ms, 3),
+                   parts_ms=parts)
+        del dec
+        torch.cuda.empty_cache()
+
+
+def library_tree(b, B, V, dev, seed=1002):
+    """b config-2-style trees of B nodes built by the library (ddtree_build) on the device."""
+    import torch
+
+    from block_diffusion_draft_dflash_gb300 import _lib
+    lp = synth_logprobs(seed, b, 15, V, dev)
+    T = B + 1
+    z = lambda *sh, dt=torch.int32: torch.zeros(sh, dtype=dt, device=dev)
+    out = dict(tok=z(b, T), parent=z(b, T), depth=z(b, T), score=z(b, T, dt=torch.float32), anc=z(b, T, (T + 31) // 32))
+    _lib.ddtree_build(lp, B, out, _lib.Workspace(_lib.ddtree_build_workspace_size(b, 15, V, B), dev))
+    torch.cuda.synchronize()
+    return out
+
+
+def kernel_case(a):
+    """Small isolated launches of one kernel at the step's shapes (device footprint < 3 GB)."""
+    import numpy as np
+    import torch
+
+    import synth
+    from block_diffusion_draft_dflash_gb300 import _lib, engine
     dev = "cuda:0"
     if a.kernel_case == "gemm":
         # one target projection (default gate/up: 24576 x 4096) on the 257 tree rows; enough
@@ -458,18 +887,15 @@ def kernel_case(a):
         q = synth.device_normal((b, T, 32, 128), 1.0, 5, "case.q", dev)
         k = synth.device_normal((b, 8, cap, 128), 1.0, 5, "case.k", dev)
         v = synth.device_normal((b, 8, 128, cap), 1.0, 5, "case.v", dev)
-        lp = ddtree.log_softmax(synth.ddtree_logits(1002, 1, 15, 2000)[0])
-        anc = ddtree.ancestor_mask(ddtree.build_tree(lp, T - 1)["parent"])
-        anc_t = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(anc, (b,) + anc.shape)).view(np.int32)).to(dev)
+        tr = library_tree(b, T - 1, 2000, dev)
         out = torch.zeros_like(q)
         ws = _lib.Workspace(_lib.tree_verify_attention_workspace_size(b, T, 32, 8, 128, cap), dev)
         clen = torch.full((b,), N, dtype=torch.int32, device=dev)
         for _ in range(4):
-            _lib.tree_verify_attention(q, k, v, clen, anc_t, 1 / np.sqrt(128), out, ws)
+            _lib.tree_verify_attention(q, k, v, clen, tr["anc"], 1 / np.sqrt(128), out, ws)
     elif a.kernel_case == "ddtree":
         b = 64
-        lp = torch.from_numpy(ddtree.log_softmax(synth.ddtree_logits(1002, b, 15, 151936))).to(dev)
-        from block_diffusion_draft_dflash_gb300 import engine  # noqa: F401
+        lp = synth_logprobs(1002, b, 15, 151936, dev)
         T = a.budget + 1
         W = (T + 31) // 32
         z = lambda *sh, dt=torch.int32: torch.zeros(sh, dtype=dt, device=dev)
@@ -477,31 +903,47 @@ def kernel_case(a):
         ws = _lib.Workspace(_lib.ddtree_build_workspace_size(b, 15, 151936, a.budget), dev)
         for _ in range(4):
             _lib.ddtree_build(lp, a.budget, out, ws)
+    elif a.kernel_case == "draft":
+        # the drafter at Qwen3-8B width but 2 layers deep, ctx 2048 + 16 new rows: its dense
+        # attention over context ++ block, the context projections and the LM head
+        import dataclasses
+        DS = dataclasses.replace(synth.DFLASH_QWEN3_8B_DRAFTER, n_layers=2)
+        dm = engine.DeviceModel.random(DS, 5, "drafter", dev, n_feat=5)
+        b, ctx, L, max_new = a.batch, 2048, 16, 16
+        cap = (ctx + max_new + L + 127) // 128 * 128
+        ck = synth.device_normal((2, b, 8, cap, 128), 1.0, 5, "case.dk", dev)
+        cv = synth.device_normal((2, b, 8, 128, cap), 1.0, 5, "case.dv", dev)
+        feat = synth.device_normal((b, max_new, 5 * 4096), 1.0, 5, "case.df", dev)
+        n_new = torch.full((b,), max_new, dtype=torch.int32, device=dev)
+        len0 = torch.full((b,), ctx, dtype=torch.int32, device=dev)
+        ctx_len = len0.clone()
+        bonus = torch.arange(b, dtype=torch.int32, device=dev) + 3
+        lp = torch.zeros(b, L - 1, 151936, dtype=torch.float32, device=dev)
+        ws = _lib.Workspace(_lib.draft_block_workspace_size(dm.cfg, b, max_new), dev)
+        for _ in range(4):
+            ctx_len.copy_(len0)
+            _lib.draft_block(dm.cfg, dm.weights, feat, n_new, ck, cv, ctx_len, bonus, lp, ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
     elif a.kernel_case == "layer":
         # the target tree forward at Qwen3-8B width but 2 layers deep (about 2.5 GB on the
         # device): every projection GEMM in its fused partial-tile mode, 9 GEMM launches a call
         import dataclasses
-        from block_diffusion_draft_dflash_gb300 import engine
         TS = dataclasses.replace(synth.QWEN3_8B_TARGET, n_layers=2, feat_layers=(1, 2))
         tm = engine.DeviceModel.random(TS, 5, "target", dev)
         b, T, N = a.batch, a.budget + 1, a.ctx
         cap = (N + T + 127) // 128 * 128
         k = synth.device_normal((2, b, 8, cap, 128), 1.0, 5, "case.k", dev)
         v = synth.device_normal((2, b, 8, 128, cap), 1.0, 5, "case.v", dev)
-        lp = ddtree.log_softmax(synth.ddtree_logits(1002, 1, 15, 2000)[0])
-        tr = ddtree.build_tree(lp, T - 1)
-        rep = lambda x: torch.from_numpy(np.ascontiguousarray(np.broadcast_to(x, (b,) + x.shape))).to(dev)
-        tt = tr["tok"].astype(np.int32)
-        tt[0] = 1  # the root carries the last accepted token
-        tok = rep(tt)
-        depth = rep(tr["depth"].astype(np.int32))
-        anc = rep(ddtree.ancestor_mask(tr["parent"]).view(np.int32))
+        tr = library_tree(b, T - 1, 2000, dev)
+        tok = tr["tok"].clone()
+        tok[:, 0] = 1  # the root carries the last accepted token
         clen = torch.full((b,), N, dtype=torch.int32, device=dev)
         choice = torch.zeros(b, T, dtype=torch.int32, device=dev)
         feat = torch.zeros(b, T, 2 * TS.d_model, dtype=torch.bfloat16, device=dev)
         ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T), dev)
         for _ in range(4):
-            _lib.target_tree_forward(tm.cfg, tm.weights, tok, depth, anc, k, v, clen, choice, feat, ws)
+            _lib.target_tree_forward(tm.cfg, tm.weights, tok, tr["depth"], tr["anc"], k, v, clen, choice, feat, ws)
         torch.cuda.synchronize()
         assert ws.status() == 0
     torch.cuda.synchronize()
@@ -517,22 +959,35 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if a.impl == "reference":
+        if a.oracle_sample_json:
+            print(json.dumps(oracle_sample(a)))
+            return
         if rank != 0:
             return
         import statistics
         # each "step" of this arm is one bounded oracle sample (about 15-30 s of CPU work)
-        vals = [oracle_sample(a) for _ in range(max(1, min(a.steps, 2)))]
+        n = max(1, min(a.steps, 2))
+        vals = [oracle_sample(a) for _ in range(n)]
         cb = dict(vals[-1])
         cb["value"] = statistics.median(v["value"] for v in vals)
         cb["est_s_per_step"] = 1.0 / cb["value"]
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu["nproc"] = os.cpu_count()
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "spec steps/s",
-                "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup, "ms_per_step": cb["est_s_per_step"] * 1e3,
+                "n_gpus": a.gpus, "steps": n, "warmup": 0, "ms_per_step": cb["est_s_per_step"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config(a),
-                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "data": "synthetic", "config": config(a, impl="reference"),
+                "cpu_baseline": cpu,
+                "sample_wall_s": round(sum(v["sample_wall_s"] for v in vals), 2),
                 "e2e": {"value": cb["value"], "unit": "spec steps/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
+        return
+    if a.mode != "step":
+        if rank != 0:
+            return  # the isolated-kernel modes run on one GPU
+        {"ddtree": run_ddtree_mode, "draft": run_draft_mode, "verify": run_verify_mode,
+         "prefill": run_prefill_mode}[a.mode](a)
         return
     if world > 1:
         import torch
@@ -545,8 +1000,7 @@ def main():
     e2e = world * b / r["e2e_s"]
     cpu = None
     if not a.no_cpu_baseline and world == 1:
-        cb = oracle_sample(a)
-        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu, _ = cpu_baseline(a)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "spec steps/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(r["ms"], 4), "higher_is_better": True, "scaling": "weak",
@@ -560,7 +1014,12 @@ def main():
         "e2e": {"value": round(e2e, 3), "unit": "spec steps/s", "h2d_bytes_per_step": 4 * b,
                 "d2h_bytes_per_step": 4 * b * 16 + 4 * b},
         "tokens_per_step": round(r["tau"], 3),
+        "tokens_per_s": round(value * r["tau"], 1),
+        "acceptance": r["acc"],
+        "prefill": r["prefill"],
         "gpu_launches": int(round(r["launches"] * a.steps)),
+        "kernel_timing": "eager, traced: CUDA events around every launch of 3 steps run without the graph "
+                         "(no programmatic-launch overlap), so the classes sum to more than ms_per_step",
         "kernels": r["kernels"],
         "gemm_shapes": r["kernel_shapes"],
         "clocks": r["clocks"],

@@ -74,6 +74,8 @@ _SIGS = {
     "dflash_linear_logsoftmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                            C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_workspace_configure": (C.c_int, [C.c_void_p, C.c_ulonglong, C.c_int, C.c_void_p]),
+    "dflash_plant_logprobs": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
+                                        C.c_float, C.c_float, C.c_ulonglong, C.c_void_p]),
     "dflash_draft_block_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
     "dflash_draft_block": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_int] + [C.c_void_p] * 4 +
                            [C.c_int] + [C.c_void_p] * 3 + [C.c_size_t, C.c_void_p]),
@@ -298,6 +300,16 @@ def linear_logsoftmax(X, W, out, ws: Workspace = None):
     _check("dflash_linear_logsoftmax", load().dflash_linear_logsoftmax(_p(X), _p(W), M, N, K, _p(out), ws.ptr,
                                                                        ws.nbytes, _stream()))
     return ws
+
+
+def plant_logprobs(logprobs, ref, pos, rate, bias, seed):
+    """Harness: plant agreement with the reference continuation (see dflash_plant_logprobs)."""
+    _dev(logprobs, torch.float32, "logprobs")
+    _dev(ref, torch.int32, "ref")
+    _dev(pos, torch.int32, "pos")
+    b, D, V = logprobs.shape
+    _check("dflash_plant_logprobs", load().dflash_plant_logprobs(
+        _p(logprobs), b, D, V, _p(ref), ref.shape[1], _p(pos), float(rate), float(bias), int(seed), _stream()))
 
 
 def trace_enable(on=True):

@@ -160,10 +160,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint64_t* fullb = is_k ? k_full : v_full;
       uint64_t* emptyb = is_k ? k_empty : v_empty;
       int issued = 0;
-      bool ok = true;
       for (int j = 0; j < nblk; ++j) {
         const int st = j % NS;
-        if (!mbar_wait(&emptyb[st], ((j / NS) & 1) ^ 1, p.status, is_k ? 11 : 15)) { ok = false; break; }
+        if (!mbar_wait(&emptyb[st], ((j / NS) & 1) ^ 1, p.status, is_k ? 11 : 15)) break;
         const int key0 = (kb0 + j) * kKB;
         mbar_arrive_expect_tx(&fullb[st], kTileBytes);
         if (is_k) {
@@ -177,12 +176,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         ++issued;
       }
-      if (!ok) {
-        // wait (bounded) for every load still in flight before the CTA may exit
-        if (is_k) mbar_wait(q_full, 0, nullptr, 0);
-        for (int j = issued - NS > 0 ? issued - NS : 0; j < issued; ++j)
-          mbar_wait(&fullb[j % NS], (j / NS) & 1, nullptr, 0);
-      }
+      // every load issued must have landed before the CTA may exit, also when the MMA issuer
+      // gave up before consuming it (bounded waits; already complete in normal runs)
+      if (is_k) mbar_wait(q_full, 0, nullptr, 0);
+      for (int j = issued - NS > 0 ? issued - NS : 0; j < issued; ++j)
+        mbar_wait(&fullb[j % NS], (j / NS) & 1, nullptr, 0);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && nblk > 0) {

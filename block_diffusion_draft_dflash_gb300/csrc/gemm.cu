@@ -178,8 +178,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
     const uint64_t pol_w = p.w_keep ? policy_evict_last() : policy_evict_first(), pol_x = policy_evict_last();
-    // failure-path test hook: with the header's hold word set, issue nothing and give up
-    const long long n = wait_hold_clear(p.status, 5) ? it1 - it0 : 0;
+    const long long n = it1 - it0;
     auto coords = [&](long long it, int& wt, int& tt, int& k) {
       const long long tile = it / p.k_iters;
       k = (int)(it - tile * p.k_iters);
@@ -209,10 +208,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     int stage = npre % S;
     uint32_t phase = npre == S ? 1u : 0u;
-    bool ok = true;
     long long issued = npre;
     for (long long i = npre; i < n; ++i) {
-      if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 1)) { ok = false; break; }
+      if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 1)) break;
       int wt, tt, k;
       coords(it0 + i, wt, tt, k);
       mbar_arrive_expect_tx(&full[stage], stage_bytes);
@@ -221,8 +219,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ++issued;
       if (++stage == S) { stage = 0; phase ^= 1; }
     }
-    if (!ok) {
-      // Drain: wait (bounded) for the loads still in flight before the CTA may exit.
+    {
+      // Drain: every load issued must have landed before the CTA may exit, also when the MMA
+      // issuer gave up before consuming it (bounded waits; already complete in normal runs).
       const long long n = issued < S ? issued : S;
       int st = stage;
       uint32_t ph = phase;
@@ -240,7 +239,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     long long it = it0;
     Segment sg;
     int si = 0;
-    bool ok = true, issued_any = false;
+    // failure-path test hook: with the header's hold word set, issue no MMA and give up (the
+    // producer then finds no stage released, times out and drains its loads)
+    bool ok = wait_hold_clear(p.status, 5), issued_any = false;
     while (ok && next_segment(p, it, it1, sg)) {
       const int acc = si % p.nbuf, use = si / p.nbuf;
       if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 2)) { ok = false; break; }

@@ -323,6 +323,24 @@ int dflash_linear_logsoftmax(const df_bf16* X, const df_bf16* W, int M, int N, i
                              void* ws, size_t ws_bytes, df_stream stream);
 
 /* ------------------------------------------------------------------------------------
+ * dflash_plant_logprobs -- acceptance planting for synthetic models (benchmark and test
+ * harness; the pages have no counterpart).
+ *
+ * Random-init drafters almost never agree with random-init targets.  For sequence s and
+ * draft position d (1..D), with probability `rate`, row d of the log-probs becomes the
+ * log-softmax of its logits with `bias` added at the reference token r = ref[s][pos[s] + d]:
+ * lp'_i = lp_i - c (i != r), lp'_r = lp_r + bias - c, c = log(1 + exp(lp_r)(e^bias - 1)).
+ * The draw is a counter-based hash (splitmix64) of (seed, s, pos[s], d): no host input per
+ * step, so the call can sit in a captured graph.  Rows whose position is outside the
+ * reference are left as they are.
+ *   logprobs [b][D][V] fp32 in/out;  ref [b][ref_len] int32 (prompt + greedy continuation);
+ *   pos [b] int32: position of the block's row 0 (the target's cache length).
+ * ------------------------------------------------------------------------------------ */
+int dflash_plant_logprobs(float* logprobs, int b, int D, int V, const int32_t* ref, int ref_len,
+                          const int32_t* pos, float rate, float bias, unsigned long long seed,
+                          df_stream stream);
+
+/* ------------------------------------------------------------------------------------
  * Status and device queries.
  * ------------------------------------------------------------------------------------ */
 /* Launch tracing, off by default.  While on, every kernel launch of the library (outside
@@ -341,8 +359,8 @@ int dflash_workspace_status(void* ws, df_stream stream);
  *                  (0 = the default, 2 s); a wait that runs out records DF_ERR_TIMEOUT and
  *                  its kernel returns without touching TMEM or shared memory still in use
  *   hold           test hook: nonzero makes every projection GEMM of such a call wait for
- *                  the word to read 0 before it issues any work.  Nothing clears it, so the
- *                  wait runs out and the call reports DF_ERR_TIMEOUT; set 0 to go on.
+ *                  the word to read 0 before it issues any tensor-core work.  Nothing clears
+ *                  it, so the wait runs out and the call reports DF_ERR_TIMEOUT; set 0 to go on.
  * Zero-initialised workspaces start with both at 0. */
 int dflash_workspace_configure(void* ws, unsigned long long wait_limit_ns, int hold, df_stream stream);
 /* Static text for a status code. */

@@ -83,3 +83,42 @@ def test_accept_and_compact_matches_oracle(b, B, D, n_layers, Hkv, cap):
         nf = new_feat[s].float().cpu().numpy()
         np.testing.assert_array_equal(nf[:a + 1], feat[s][[0] + path])
     assert sum(out["n_acc"].cpu().numpy()) > 0
+
+
+def _splitmix64(x):
+    # published definition (Steele, Lea, Flood 2014), on Python ints mod 2^64
+    M = (1 << 64) - 1
+    x = (x + 0x9E3779B97F4A7C15) & M
+    x = ((x ^ (x >> 30)) * 0xBF58476D1CE4E5B9) & M
+    x = ((x ^ (x >> 27)) * 0x94D049BB133111EB) & M
+    return x ^ (x >> 31)
+
+
+def test_plant_logprobs_harness():
+    # the benchmark's acceptance plant: the planted rows are a renormalised bias at the
+    # reference token, drawn per (seed, sequence, position, depth); the others are unchanged
+    b, D, V, ref_len, rate, bias, seed = 3, 15, 5000, 400, 0.6, 16.0, 77
+    lp = ddtree.log_softmax(np.random.default_rng(0).normal(0, 1.3, size=(b, D, V)))
+    ref = np.random.default_rng(1).integers(0, V, size=(b, ref_len)).astype(np.int32)
+    pos = np.array([10, 200, ref_len - 4], dtype=np.int32)   # the last one runs off the reference
+    lp_t = torch.from_numpy(lp).cuda()
+    _lib.plant_logprobs(lp_t, torch.from_numpy(ref).cuda(), torch.from_numpy(pos).cuda(), rate, bias, seed)
+    got = lp_t.cpu().numpy().astype(np.float64)
+    n_planted = 0
+    for s in range(b):
+        for d in range(1, D + 1):
+            p = int(pos[s]) + d
+            h = _splitmix64(seed ^ _splitmix64((s << 40) ^ (int(pos[s]) << 8) ^ d))
+            planted = p < ref_len and (h >> 11) / 2.0 ** 53 < rate
+            row = lp[s, d - 1].astype(np.float64)
+            if not planted:
+                np.testing.assert_array_equal(got[s, d - 1], row)
+                continue
+            n_planted += 1
+            r = ref[s, p]
+            x = row.copy()
+            x[r] += bias
+            expect = x - np.log(np.sum(np.exp(x)))    # log-softmax of the biased logits
+            np.testing.assert_allclose(got[s, d - 1], expect, atol=2e-5)
+            assert int(np.argmax(got[s, d - 1])) == r
+    assert 10 < n_planted < 3 * D

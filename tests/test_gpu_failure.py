@@ -2,9 +2,10 @@
 
   * a full cache: a tree forward whose slots run past the cache capacity records
     DF_ERR_CAPACITY in the workspace status word (the rows that do not fit are not written)
-  * an exhausted wait: a workspace whose hold word is set makes the GEMM wait for a flag
-    that nothing clears; with a short wait limit the call reports DF_ERR_TIMEOUT, having
-    issued no work, and the same workspace then serves a normal call
+  * an exhausted wait: a workspace whose hold word is set makes the GEMM's MMA issuer wait
+    for a flag that nothing clears; with a short wait limit the call reports DF_ERR_TIMEOUT,
+    having issued no tensor-core work (its loads are drained), and the same workspace then
+    serves a normal call
 """
 import numpy as np
 import pytest
