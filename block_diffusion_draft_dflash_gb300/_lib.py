@@ -303,11 +303,13 @@ def linear_logsoftmax(X, W, out, ws: Workspace = None):
 
 
 def plant_logprobs(logprobs, ref, pos, rate, bias, seed):
-    """Harness: plant agreement with the reference continuation (see dflash_plant_logprobs)."""
+    """Harness: plant agreement with reference tokens (see dflash_plant_logprobs).
+    ref [b][n_pos][D] int32: tokens expected at depths 1..D of a block starting at position p."""
     _dev(logprobs, torch.float32, "logprobs")
     _dev(ref, torch.int32, "ref")
     _dev(pos, torch.int32, "pos")
     b, D, V = logprobs.shape
+    assert ref.shape[0] == b and ref.shape[2] == D
     _check("dflash_plant_logprobs", load().dflash_plant_logprobs(
         _p(logprobs), b, D, V, _p(ref), ref.shape[1], _p(pos), float(rate), float(bias), int(seed), _stream()))
 

@@ -134,7 +134,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int s = u / p.Hkv;
   const int G = p.Hq / p.Hkv, NPT = 128 / G;
   const int dense_len = p.dense_len[s] + p.dense_add;
-  const int Lk = dense_len + p.tail_len;
+  // a causal chain: no row of this tile sees a tail slot past the tile's last node, so the
+  // key blocks beyond it are not visited at all
+  const int last_node = min(p.T, (qt + 1) * NPT) - 1;
+  const int Lk = dense_len + (p.causal ? min(p.tail_len, last_node + 1) : p.tail_len);
   const int nb = (Lk + kKB - 1) / kKB;
   const int kb0 = (int)((long long)nb * split / p.nsplit), kb1 = (int)((long long)nb * (split + 1) / p.nsplit);
   const int nblk = kb1 - kb0;

@@ -2,8 +2,9 @@
 // counterpart).  Random-init drafters almost never agree with random-init targets, so a
 // known fraction of agreement is planted into the drafter's log-probs: for sequence s and
 // draft position d (1..D), with probability `rate`, row d becomes the log-softmax of its
-// logits with `bias` added at the reference token r = ref[s][pos[s] + d] (the target's own
-// greedy continuation):
+// logits with `bias` added at the reference token r = ref[s][pos[s]][d - 1] (the token the
+// harness expects the target to choose at depth d when the block starts at position
+// pos[s]):
 //   lp'_i = lp_i - c  (i != r),   lp'_r = lp_r + bias - c,   c = log(1 + p_r (e^bias - 1)),
 // where p_r = exp(lp_r).  The choice is a counter-based hash of (seed, s, pos[s], d), so a
 // captured graph replays a different draw at every step (pos grows) with no host input.
@@ -22,19 +23,19 @@ DF_DEV uint64_t splitmix64(uint64_t x) {
 // grid: b * D rows; block 512.  One block per row: the correction c is taken from the row
 // before any of it is rewritten.
 __global__ void __launch_bounds__(512) plant_logprobs_kernel(float* __restrict__ lp, int D, int V,
-                                                             const int32_t* __restrict__ ref, int ref_len,
+                                                             const int32_t* __restrict__ ref, int n_pos,
                                                              const int32_t* __restrict__ pos, float rate, float bias,
                                                              unsigned long long seed) {
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.x, s = row / D, d = row % D + 1;
-  const int p = pos[s] + d;
-  if (p < 0 || p >= ref_len) return;
-  const uint64_t h = splitmix64(seed ^ splitmix64(((uint64_t)s << 40) ^ ((uint64_t)(uint32_t)pos[s] << 8) ^ (uint64_t)d));
+  const int p0 = pos[s];
+  if (p0 < 0 || p0 >= n_pos) return;
+  const uint64_t h = splitmix64(seed ^ splitmix64(((uint64_t)s << 40) ^ ((uint64_t)(uint32_t)p0 << 8) ^ (uint64_t)d));
   const double u = (double)(h >> 11) * (1.0 / 9007199254740992.0);  // uniform [0, 1)
   if (!(u < (double)rate)) return;
-  const int r = ref[(size_t)s * ref_len + p];
-  if (r < 0 || r >= V) return;
+  const int r = ref[((size_t)s * n_pos + p0) * D + d - 1];
+  if (r < 0 || r >= V) return;  // no reference for this block
   float* x = lp + (size_t)row * V;
   __shared__ float c_sh;
   if (threadIdx.x == 0) {
@@ -48,15 +49,15 @@ __global__ void __launch_bounds__(512) plant_logprobs_kernel(float* __restrict__
 
 }  // namespace df
 
-extern "C" int dflash_plant_logprobs(float* logprobs, int b, int D, int V, const int32_t* ref, int ref_len,
+extern "C" int dflash_plant_logprobs(float* logprobs, int b, int D, int V, const int32_t* ref, int n_pos,
                                      const int32_t* pos, float rate, float bias, unsigned long long seed,
                                      df_stream stream) {
-  if (b < 0 || D < 1 || V < 1 || ref_len < 0) return DF_ERR_ARG;
-  if (b == 0 || ref_len == 0) return DF_OK;
+  if (b < 0 || D < 1 || V < 1 || n_pos < 0) return DF_ERR_ARG;
+  if (b == 0 || n_pos == 0) return DF_OK;
   if (!logprobs || !ref || !pos) return DF_ERR_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   DF_TRACE("plant", st);
-  df::launch_k(df::plant_logprobs_kernel, dim3(b * D), dim3(512), 0, st, logprobs, D, V, ref, ref_len, pos, rate,
+  df::launch_k(df::plant_logprobs_kernel, dim3(b * D), dim3(512), 0, st, logprobs, D, V, ref, n_pos, pos, rate,
                bias, seed);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

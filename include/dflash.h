@@ -328,15 +328,17 @@ int dflash_linear_logsoftmax(const df_bf16* X, const df_bf16* W, int M, int N, i
  *
  * Random-init drafters almost never agree with random-init targets.  For sequence s and
  * draft position d (1..D), with probability `rate`, row d of the log-probs becomes the
- * log-softmax of its logits with `bias` added at the reference token r = ref[s][pos[s] + d]:
+ * log-softmax of its logits with `bias` added at the reference token r = ref[s][pos[s]][d-1]:
  * lp'_i = lp_i - c (i != r), lp'_r = lp_r + bias - c, c = log(1 + exp(lp_r)(e^bias - 1)).
  * The draw is a counter-based hash (splitmix64) of (seed, s, pos[s], d): no host input per
- * step, so the call can sit in a captured graph.  Rows whose position is outside the
- * reference are left as they are.
- *   logprobs [b][D][V] fp32 in/out;  ref [b][ref_len] int32 (prompt + greedy continuation);
- *   pos [b] int32: position of the block's row 0 (the target's cache length).
+ * step, so the call can sit in a captured graph.  Rows with no reference (pos[s] outside
+ * [0, n_pos) or a negative entry) are left as they are.
+ *   logprobs [b][D][V] fp32 in/out
+ *   ref      [b][n_pos][D] int32: the tokens expected at depths 1..D of a block whose row 0
+ *            (the bonus token) is at position p
+ *   pos      [b] int32: position of the block's row 0 (the target's cache length)
  * ------------------------------------------------------------------------------------ */
-int dflash_plant_logprobs(float* logprobs, int b, int D, int V, const int32_t* ref, int ref_len,
+int dflash_plant_logprobs(float* logprobs, int b, int D, int V, const int32_t* ref, int n_pos,
                           const int32_t* pos, float rate, float bias, unsigned long long seed,
                           df_stream stream);
 

@@ -97,25 +97,25 @@ def _splitmix64(x):
 def test_plant_logprobs_harness():
     # the benchmark's acceptance plant: the planted rows are a renormalised bias at the
     # reference token, drawn per (seed, sequence, position, depth); the others are unchanged
-    b, D, V, ref_len, rate, bias, seed = 3, 15, 5000, 400, 0.6, 16.0, 77
+    b, D, V, n_pos, rate, bias, seed = 3, 15, 5000, 400, 0.6, 16.0, 77
     lp = ddtree.log_softmax(np.random.default_rng(0).normal(0, 1.3, size=(b, D, V)))
-    ref = np.random.default_rng(1).integers(0, V, size=(b, ref_len)).astype(np.int32)
-    pos = np.array([10, 200, ref_len - 4], dtype=np.int32)   # the last one runs off the reference
+    ref = np.random.default_rng(1).integers(0, V, size=(b, n_pos, D)).astype(np.int32)
+    pos = np.array([10, 200, 250], dtype=np.int32)
+    ref[2, 250, 3:9] = -1                                     # no reference at these depths
     lp_t = torch.from_numpy(lp).cuda()
     _lib.plant_logprobs(lp_t, torch.from_numpy(ref).cuda(), torch.from_numpy(pos).cuda(), rate, bias, seed)
     got = lp_t.cpu().numpy().astype(np.float64)
     n_planted = 0
     for s in range(b):
         for d in range(1, D + 1):
-            p = int(pos[s]) + d
             h = _splitmix64(seed ^ _splitmix64((s << 40) ^ (int(pos[s]) << 8) ^ d))
-            planted = p < ref_len and (h >> 11) / 2.0 ** 53 < rate
+            r = int(ref[s, pos[s], d - 1])
+            planted = r >= 0 and (h >> 11) / 2.0 ** 53 < rate
             row = lp[s, d - 1].astype(np.float64)
             if not planted:
                 np.testing.assert_array_equal(got[s, d - 1], row)
                 continue
             n_planted += 1
-            r = ref[s, p]
             x = row.copy()
             x[r] += bias
             expect = x - np.log(np.sum(np.exp(x)))    # log-softmax of the biased logits
