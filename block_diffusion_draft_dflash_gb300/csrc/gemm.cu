@@ -22,8 +22,12 @@
 // Every mbarrier wait is bounded (common.cuh); a timeout is recorded in the status word.
 #include <stdio.h>
 
+#include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <unordered_map>
+#include <vector>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -37,6 +41,11 @@ constexpr int kGemmThreads = 192;
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // k per stage (one 128-byte swizzle row)
 constexpr int kArgChunks = 16;  // argmax epilogue: running maxima of up to 16 x 32 token columns
+constexpr int kMaxGrid = 192;   // CTAs a launch may use (iteration ranges passed as parameters)
+#ifndef DF_GEMM_DRAIN_DELTA
+#define DF_GEMM_DRAIN_DELTA -1
+#endif
+constexpr int kDrainDelta = DF_GEMM_DRAIN_DELTA;  // drain cost in k-steps (-1: BN / 64 when not double-buffered)
 
 struct GemmParams {
   int M, N, K;
@@ -57,6 +66,7 @@ struct GemmParams {
   int n_stats;               // = 4 * number of weight tiles
   int* status;
   int stages;
+  int starts[kMaxGrid + 1];  // CTA c owns iterations [starts[c], starts[c + 1])
 };
 
 struct Segment {
@@ -64,17 +74,20 @@ struct Segment {
   int k0, k1;
 };
 
-// Iteration range of CTA c and its decomposition into per-tile segments.
+// Iteration range of CTA c (chosen on the host, see gemm_partition) and its decomposition
+// into per-tile segments.
 DF_DEV void cta_range(const GemmParams& p, long long& it0, long long& it1) {
-  const long long G = gridDim.x, c = blockIdx.x;
-  if (p.whole_tiles) {
-    const long long tiles = p.total_iters / p.k_iters;
-    it0 = (tiles * c / G) * p.k_iters;
-    it1 = (tiles * (c + 1) / G) * p.k_iters;
-  } else {
-    it0 = p.total_iters * c / G;
-    it1 = p.total_iters * (c + 1) / G;
+  it0 = p.starts[blockIdx.x];
+  it1 = p.starts[blockIdx.x + 1];
+}
+// The CTA whose range holds iteration `it` (the ranges are contiguous and ascending).
+DF_DEV int cta_of(const GemmParams& p, long long it) {
+  int lo = 0, hi = (int)gridDim.x - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.starts[mid] <= it) lo = mid; else hi = mid - 1;
   }
+  return lo;
 }
 DF_DEV bool next_segment(const GemmParams& p, long long& it, long long it1, Segment& s) {
   if (it >= it1) return false;
@@ -281,15 +294,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (MODE == kGemmPartial && threadIdx.x == 64 && it1 > it0) {
       // Register this CTA's segments in the per-tile slot lists.  The CTA's place among a
       // tile's contributors is its distance from the CTA that owns the tile's first k-step.
-      const long long G = gridDim.x, k = p.k_iters;
+      const long long k = p.k_iters;
       const long long t_first = it0 / k, t_last = (it1 - 1) / k;
       for (long long t = t_first; t <= t_last; ++t) {
         int pos = 0;
-        if (t * k < it0) {
-          long long cf = (t * k * G) / p.total_iters;  // CTA holding iteration t*k
-          while (cf + 1 < G && p.total_iters * (cf + 1) / G <= t * k) ++cf;
-          pos = (int)(blockIdx.x - cf);
-        }
+        if (t * k < it0) pos = (int)blockIdx.x - cta_of(p, t * k);  // CTA holding iteration t*k is first
         p.meta[t * p.meta_stride + 1 + pos] = (int)(blockIdx.x * p.max_seg + (t - t_first));
         if ((t + 1) * k <= it1) p.meta[t * p.meta_stride] = pos + 1;  // this CTA holds the tile's last k-step
       }
@@ -451,6 +460,97 @@ int gemm_token_tile(int M) {
   return (bn + 15) / 16 * 16;
 }
 
+// Split of a launch's iteration space over its CTAs.
+//
+// Whole-tile epilogues: tiles spread evenly.  Partial-tile epilogue (stream-K): contiguous
+// iteration ranges of equal *cost*, where a range that crosses a tile boundary is charged
+// `delta` extra iterations per crossing when the accumulator is not double-buffered (its MMA
+// waits for the previous tile's drain; delta = the drain time in k-steps, about BN / 64).
+// The smallest feasible maximum cost is found by bisection with a greedy fill; CTAs left
+// without work are not launched.
+struct Partition {
+  int G;                      // CTAs launched
+  int starts[kMaxGrid + 1];
+  int max_seg, maxc;          // most segments of one CTA, most pieces of one tile
+};
+
+static void make_partition(long long total, long long k_iters, int G, bool whole_tiles, int delta, Partition& P) {
+  P.G = 0;
+  if (whole_tiles) {
+    const long long tiles = total / k_iters;
+    for (int c = 0; c <= G; ++c) P.starts[c] = (int)((tiles * c / G) * k_iters);
+    P.G = G;
+  } else {
+    // furthest end of a range that starts at s and may cost C
+    auto reach = [&](long long s, long long C) {
+      long long end = s, budget = C;
+      while (end < total) {
+        const long long lim = std::min((end / k_iters + 1) * k_iters, total);
+        if (end + budget <= lim) return end + budget;
+        budget -= lim - end;
+        end = lim;
+        if (end >= total) break;
+        budget -= delta;  // going on past a tile boundary costs a drain
+        if (budget <= 0) break;
+      }
+      return end;
+    };
+    auto ranges = [&](long long C) {  // greedy fill: ranges needed at cost C (G + 1 = too many)
+      int n = 0;
+      for (long long s = 0; s < total;) {
+        const long long e = reach(s, C);
+        if (e <= s || ++n > G) return G + 1;
+        s = e;
+      }
+      return n;
+    };
+    long long lo = (total + G - 1) / G, hi = lo;
+    while (ranges(hi) > G) hi *= 2;
+    while (lo < hi) {
+      const long long mid = (lo + hi) / 2;
+      if (ranges(mid) <= G) hi = mid; else lo = mid + 1;
+    }
+    long long s = 0;
+    P.starts[0] = 0;
+    while (s < total) {
+      s = reach(s, lo);
+      P.starts[++P.G] = (int)s;
+    }
+  }
+  P.max_seg = 1;
+  P.maxc = 1;
+  std::vector<int> pieces(total / k_iters, 0);
+  for (int c = 0; c < P.G; ++c) {
+    if (P.starts[c + 1] <= P.starts[c]) continue;
+    const long long t0 = P.starts[c] / k_iters, t1 = (P.starts[c + 1] - 1) / k_iters;
+    P.max_seg = std::max(P.max_seg, (int)(t1 - t0 + 1));
+    for (long long t = t0; t <= t1; ++t) P.maxc = std::max(P.maxc, ++pieces[t]);
+  }
+}
+
+// The partition of a launch of this shape (cached: it depends on the shape and the SM count only).
+static const Partition& gemm_partition(int M, int N, int K, bool whole_tiles) {
+  const int BN = gemm_token_tile(M);
+  const long long n_tt = (M + BN - 1) / BN, k_iters = K / kBK;
+  const long long tiles = (long long)((N + kBM - 1) / kBM) * n_tt;
+  const long long total = tiles * k_iters;
+  long long G = std::min<long long>(num_sms(), kMaxGrid);
+  G = std::min(G, whole_tiles ? tiles : total);
+  const int nbuf = 2 * BN <= 512 ? 2 : 1;
+  const int delta = kDrainDelta >= 0 ? kDrainDelta : (nbuf == 2 ? 0 : (BN + 63) / 64);
+  static std::mutex mu;
+  static std::map<std::tuple<long long, long long, long long, bool, int>, Partition> cache;
+  std::lock_guard<std::mutex> g(mu);
+  auto key = std::make_tuple(total, k_iters, G, whole_tiles, delta);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    Partition P;
+    make_partition(total, k_iters, (int)G, whole_tiles, delta, P);
+    it = cache.emplace(key, P).first;
+  }
+  return it->second;
+}
+
 // Layout of a partial buffer: slots [grid * max_seg][BN][128] fp32, then per tile its piece
 // count and slot list, meta[tiles][meta_stride] (meta_stride >= maxc + 1, a multiple of 4).
 struct PartialLayout {
@@ -458,17 +558,13 @@ struct PartialLayout {
   long long tiles;
   int max_seg, maxc, meta_stride;
 };
-static PartialLayout partial_layout(int M, int N, int K, long long grid) {
+static PartialLayout partial_layout(int M, int N, int K, const Partition& P) {
   PartialLayout L;
   const int BN = gemm_token_tile(M);
-  const long long n_tt = (M + BN - 1) / BN;
-  const long long k_iters = K / kBK;
-  L.tiles = (long long)((N + kBM - 1) / kBM) * n_tt;
-  const long long total = L.tiles * k_iters;
-  const long long range_max = (total + grid - 1) / grid, range_min = total / grid;
-  L.max_seg = (int)((range_max + k_iters - 1) / k_iters + 1);
-  L.maxc = (int)((k_iters + range_min - 1) / (range_min > 0 ? range_min : 1) + 2);
-  L.slots_bytes = (size_t)grid * L.max_seg * BN * 128 * 4;
+  L.tiles = (long long)((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  L.max_seg = P.max_seg;
+  L.maxc = P.maxc;
+  L.slots_bytes = (size_t)P.G * L.max_seg * BN * 128 * 4;
   L.meta_stride = (L.maxc + 1 + 3) / 4 * 4;
   L.total_bytes = L.slots_bytes + (size_t)L.tiles * 4 * L.meta_stride + 64;
   return L;
@@ -476,11 +572,7 @@ static PartialLayout partial_layout(int M, int N, int K, long long grid) {
 
 size_t gemm_partial_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  const int BN = gemm_token_tile(M);
-  const long long total = (long long)((N + kBM - 1) / kBM) * ((M + BN - 1) / BN) * (K / kBK);
-  long long grid = num_sms();
-  if (grid > total) grid = total;
-  return partial_layout(M, N, K, grid).total_bytes;
+  return partial_layout(M, N, K, gemm_partition(M, N, K, false)).total_bytes;
 }
 
 int launch_gemm(const GemmDesc& g, cudaStream_t st) {
@@ -532,13 +624,12 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
     default: return DF_ERR_ARG;
   }
   if (attr_err != cudaSuccess) return DF_ERR_CUDA;
-  long long grid = num_sms();
-  const long long work = p.whole_tiles ? tiles : p.total_iters;
-  if (grid > work) grid = work;
-  if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;
+  const Partition& P = gemm_partition(g.M, g.N, g.K, p.whole_tiles);
+  const long long grid = P.G;
+  for (int c = 0; c <= P.G; ++c) p.starts[c] = P.starts[c];
   if (g.mode == kGemmPartial) {
     if (!g.part || !g.view) return DF_ERR_ARG;
-    const PartialLayout L = partial_layout(g.M, g.N, g.K, grid);
+    const PartialLayout L = partial_layout(g.M, g.N, g.K, P);
     unsigned char* base = reinterpret_cast<unsigned char*>(g.part);
     p.part = g.part;
     p.max_seg = L.max_seg;

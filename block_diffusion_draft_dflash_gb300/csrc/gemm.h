@@ -20,7 +20,6 @@ struct GemmDesc {
   unsigned long long* amax;  // kGemmArgmax: per-token packed (value key << 32 | ~index), max-reduced
   float* stats;    // kGemmStore, optional: [M][4 * ceil(N/128)] float2 (max, sum exp(x - max)) partials
   int* status;
-  int max_ctas;    // 0 = one CTA per SM
   float* part;     // kGemmPartial: slot buffer (size from gemm_partial_bytes)
   PartialView* view;  // kGemmPartial: filled with what consumers need to read the slots
 };
