@@ -214,64 +214,54 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
   topk_row_full<kVec4>(lp, blockIdx.x, V, K, out_id, out_val, status);
 }
 
-// ----------------------------------------------------------------------------- chunked top-K
-// Pass A: per (chunk, row) CTA, histogram of the top 12 key bits into hist[row][4096].
-// Pass B: per (chunk, row) CTA, threshold bin t from hist (the bin holding the K-th
-//         largest key); keys in bins above t go to hi[row] (all of them are selected),
-//         keys in bin t to eq[row] (candidates), with per-row counters.
-// Pass C: per row, the K - |hi| best candidates of eq by (key desc, id asc) join hi and
-//         the K winners are sorted.  If eq overflowed, the row is redone by topk_row_full.
-constexpr int kChunk = 8192;
-constexpr int kCapEq = 4096;
+// ----------------------------------------------------------------------------- sampled top-K
+// One read of the log-probs per row when scratch is available:
+//   topk_sample:  a 1/16 sample of the row (every 16th line of 32 floats) and histograms of
+//                 its top 12 key bits, then of the next 12 bits inside the chosen bin, give
+//                 a threshold key t at or below the K-th largest key with high probability
+//                 (where the sample's count from the top reaches K/16 plus a 4-sigma margin);
+//   topk_collect: every key >= t is appended to the row's candidate list (gathered per
+//                 block in shared memory, one global reservation per block), NaN reported;
+//   topk_final:   if K <= candidates <= capacity, a bitonic sort by (key desc, id asc) of
+//                 the candidates gives the top K exactly (every key above the K-th largest
+//                 is at least t).  Otherwise the row is redone by the whole-row select.
+constexpr int kChunk = 8192;          // keys per collect block
 constexpr int kChunkThreads = 512;
+constexpr int kSampleLines = 16;      // one line of 32 keys in 16 is sampled
+constexpr int kCapCand = 8192;        // candidates kept per row
+constexpr int kLocCand = 2048;        // candidates one collect block holds (more: the row falls back)
 
-struct TopkScratch {     // per row
-  uint32_t cnt_hi, cnt_eq, thr_bin, above;
+struct TopkRow {     // per row, in the workspace
+  uint32_t thr, count, pad0, pad1;
 };
 
-__global__ void __launch_bounds__(kChunkThreads) topk_hist_kernel(const float* __restrict__ lp, int V,
-                                                                  uint32_t* __restrict__ ghist, int* status) {
+__global__ void __launch_bounds__(256) topk_sample_kernel(const float* __restrict__ lp, int V, int K,
+                                                          TopkRow* __restrict__ sc) {
   pdl_wait();
   pdl_trigger();
   __shared__ uint32_t hist[4096];
-  __shared__ uint32_t sh_nan;
-  const size_t row = blockIdx.y;
+  __shared__ uint32_t warp_tmp[8];
+  __shared__ uint32_t sh_bin, sh_found;
+  const size_t row = blockIdx.x;
   const float* x = lp + row * (size_t)V;
   for (int i = threadIdx.x; i < 4096; i += blockDim.x) hist[i] = 0;
-  if (threadIdx.x == 0) sh_nan = 0;
+  if (threadIdx.x == 0) { sh_bin = 0; sh_found = 0; }
   __syncthreads();
-  const int i0 = blockIdx.x * kChunk, i1 = min(V, i0 + kChunk);
-  for (int base = i0; base < i1; base += blockDim.x) {
-    const int i = base + threadIdx.x;
-    const bool ok = i < i1;
-    const float f = ok ? __ldg(x + i) : 0.f;
-    const bool nan = ok && isnan(f);
-    if (nan) sh_nan = 1;
-    hist_add(hist, float_key(f) >> 20, ok && !nan);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int n_lines = V / 32;
+  int n_sample = 0;
+  for (int l = warp * kSampleLines; l < n_lines; l += nw * kSampleLines) {
+    const float f = __ldg(x + (size_t)l * 32 + lane);
+    if (!isnan(f)) atomicAdd(&hist[float_key(f) >> 20], 1u);
   }
+  n_sample = ((n_lines + kSampleLines - 1) / kSampleLines) * 32;
   __syncthreads();
-  if (sh_nan && threadIdx.x == 0) set_status(status, DF_ERR_NAN, (int)row);
-  uint32_t* g = ghist + row * 4096;
-  for (int i = threadIdx.x; i < 4096; i += blockDim.x)
-    if (hist[i]) atomicAdd(g + i, hist[i]);
-}
-
-__global__ void __launch_bounds__(kChunkThreads) topk_collect_kernel(const float* __restrict__ lp, int V, int K,
-                                                                     const uint32_t* __restrict__ ghist,
-                                                                     TopkScratch* __restrict__ sc,
-                                                                     unsigned long long* __restrict__ hi,
-                                                                     unsigned long long* __restrict__ eq) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ uint32_t warp_tmp[32];
-  __shared__ uint32_t sh_bin, sh_above;
-  const size_t row = blockIdx.y;
-  const uint32_t* h = ghist + row * 4096;
-  // descending bins, 8 per thread (512 threads x 8 = 4096)
+  // the sample rank to reach: K / 16 plus a margin of 4 standard deviations
+  const float kr = (float)K / kSampleLines;
+  const uint32_t r = (uint32_t)ceilf(kr + 4.f * sqrtf(kr) + 4.f);
+  // bins in descending order, 16 per thread; inclusive scan of the per-thread sums
   uint32_t local = 0;
-  for (int j = 0; j < 8; ++j) local += h[4095 - (threadIdx.x * 8 + j)];
-  // inclusive scan over 512 threads
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j = 0; j < 16; ++j) local += hist[4095 - (threadIdx.x * 16 + j)];
   uint32_t v = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -280,44 +270,131 @@ __global__ void __launch_bounds__(kChunkThreads) topk_collect_kernel(const float
   }
   if (lane == 31) warp_tmp[warp] = v;
   __syncthreads();
-  if (warp == 0) {
-    uint32_t w = lane < (kChunkThreads >> 5) ? warp_tmp[lane] : 0u;
+  uint32_t off = 0;
+  for (int w = 0; w < warp; ++w) off += warp_tmp[w];
+  const uint32_t incl = v + off, excl = incl - local;
+  if (excl < r && r <= incl) {
+    uint32_t acc = excl;
+    for (int j = 0; j < 16; ++j) {
+      const int bin = 4095 - (threadIdx.x * 16 + j);
+      acc += hist[bin];
+      if (acc >= r) { sh_bin = bin; sh_found = 1; break; }
+    }
+  }
+  __syncthreads();
+  // second level: the next 12 key bits of the sampled keys inside that bin, counted from the
+  // top; the rank still to reach inside the bin is r minus the sample count above it
+  const uint32_t hi_bin = sh_bin;
+  const bool found = sh_found != 0;
+  uint32_t above = 0;
+  if (found) {
+    // count of sampled keys in bins above hi_bin (warp-strided sum, then block sum)
+    uint32_t a = 0;
+    for (int b2 = (int)hi_bin + 1 + threadIdx.x; b2 < 4096; b2 += blockDim.x) a += hist[b2];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    __syncthreads();
+    if (lane == 0) warp_tmp[warp] = a;
+    __syncthreads();
+    for (int w = 0; w < nw; ++w) above += warp_tmp[w];
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4096; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int l = warp * kSampleLines; l < n_lines; l += nw * kSampleLines) {
+      const float f = __ldg(x + (size_t)l * 32 + lane);
+      const uint32_t k = float_key(f);
+      if (!isnan(f) && (k >> 20) == hi_bin) atomicAdd(&hist[(k >> 8) & 0xFFF], 1u);
+    }
+    __syncthreads();
+    const uint32_t r2 = r - above;  // >= 1: the bin holds the r-th sampled key
+    if (threadIdx.x == 0) sh_bin = hi_bin << 12;  // (the whole bin, should the search below miss)
+    __syncthreads();
+    local = 0;
+    for (int j = 0; j < 16; ++j) local += hist[4095 - (threadIdx.x * 16 + j)];
+    v = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += n;
+      const uint32_t nn = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += nn;
     }
-    if (lane < (kChunkThreads >> 5)) warp_tmp[lane] = w;
-  }
-  __syncthreads();
-  const uint32_t incl = v + (warp ? warp_tmp[warp - 1] : 0u);
-  const uint32_t excl = incl - local;
-  if (excl < (uint32_t)K && (uint32_t)K <= incl) {
-    uint32_t acc = excl;
-    for (int j = 0; j < 8; ++j) {
-      const int bin = 4095 - (threadIdx.x * 8 + j);
-      if (acc + h[bin] >= (uint32_t)K) { sh_bin = bin; sh_above = acc; break; }
-      acc += h[bin];
+    __syncthreads();
+    if (lane == 31) warp_tmp[warp] = v;
+    __syncthreads();
+    uint32_t off2 = 0;
+    for (int w = 0; w < warp; ++w) off2 += warp_tmp[w];
+    const uint32_t incl2 = v + off2, excl2 = incl2 - local;
+    if (excl2 < r2 && r2 <= incl2) {
+      uint32_t acc = excl2;
+      for (int j = 0; j < 16; ++j) {
+        const int bin = 4095 - (threadIdx.x * 16 + j);
+        acc += hist[bin];
+        if (acc >= r2) { sh_bin = (hi_bin << 12) | (uint32_t)bin; break; }
+      }
     }
+    __syncthreads();
   }
-  __syncthreads();
-  const uint32_t tb = sh_bin;
-  if (blockIdx.x == 0 && threadIdx.x == 0) { sc[row].thr_bin = tb; sc[row].above = sh_above; }
+  if (threadIdx.x == 0) {
+    // too small a sample for the rank: take every key (the count check then decides)
+    sc[row].thr = (found && (uint32_t)n_sample >= r) ? (sh_bin << 8) : 0u;
+    sc[row].count = 0;
+  }
+}
+
+template <bool kVec4>
+__global__ void __launch_bounds__(kChunkThreads) topk_collect_kernel(const float* __restrict__ lp, int V,
+                                                                     TopkRow* __restrict__ sc,
+                                                                     unsigned long long* __restrict__ cand,
+                                                                     int* status) {
+  pdl_wait();
+  pdl_trigger();
+  // candidates of this chunk gather in shared memory first; one global reservation per block
+  __shared__ unsigned long long loc[kLocCand];
+  __shared__ uint32_t n_loc, base;
+  const size_t row = blockIdx.y;
   const float* x = lp + row * (size_t)V;
+  if (threadIdx.x == 0) n_loc = 0;
+  __syncthreads();
+  const uint32_t t = sc[row].thr;
+  const int lane = threadIdx.x & 31;
   const int i0 = blockIdx.x * kChunk, i1 = min(V, i0 + kChunk);
-  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-    const uint32_t k = float_key(__ldg(x + i));
-    const uint32_t d = k >> 20;
-    if (d < tb) continue;
-    const unsigned long long c = ((unsigned long long)k << 32) | (uint32_t)(~(uint32_t)i);
-    if (d > tb) {
-      const uint32_t pos = atomicAdd(&sc[row].cnt_hi, 1u);
-      if (pos < (uint32_t)kMaxK) hi[row * kMaxK + pos] = c;
-    } else {
-      const uint32_t pos = atomicAdd(&sc[row].cnt_eq, 1u);
-      if (pos < (uint32_t)kCapEq) eq[row * kCapEq + pos] = c;
+  bool nan = false;
+  auto put = [&](float f, int i, bool valid) {
+    nan |= valid && isnan(f);
+    const uint32_t k = float_key(f);
+    const bool take = valid && k >= t;
+    const uint32_t m = __ballot_sync(0xffffffffu, take);
+    if (!m) return;
+    uint32_t b0 = 0;
+    if (lane == __ffs(m) - 1) b0 = atomicAdd(&n_loc, (uint32_t)__popc(m));
+    b0 = __shfl_sync(0xffffffffu, b0, __ffs(m) - 1);
+    const uint32_t pos = b0 + __popc(m & ((1u << lane) - 1u));
+    if (take && pos < (uint32_t)kLocCand) loc[pos] = ((unsigned long long)k << 32) | (uint32_t)(~(uint32_t)i);
+  };
+  if (kVec4) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (int b4 = i0 / 4; b4 < (i1 + 3) / 4; b4 += blockDim.x) {
+      const int q = b4 + threadIdx.x;
+      const bool ok = q * 4 < i1;
+      const float4 f = ok ? __ldg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      put(f.x, 4 * q, ok); put(f.y, 4 * q + 1, ok); put(f.z, 4 * q + 2, ok); put(f.w, 4 * q + 3, ok);
+    }
+  } else {
+    for (int b = i0; b < i1; b += blockDim.x) {
+      const int i = b + threadIdx.x;
+      const bool ok = i < i1;
+      put(ok ? __ldg(x + i) : 0.f, i, ok);
     }
   }
+  if (__any_sync(0xffffffffu, nan) && lane == 0) set_status(status, DF_ERR_NAN, (int)row);
+  __syncthreads();
+  const uint32_t n = n_loc;
+  // a block holding more than kLocCand candidates pushes the row's count past the capacity,
+  // so the row is redone by the whole-row select
+  if (threadIdx.x == 0) base = atomicAdd(&sc[row].count, n > (uint32_t)kLocCand ? (uint32_t)kCapCand + 1 : n);
+  __syncthreads();
+  if (n <= (uint32_t)kLocCand)
+    for (uint32_t j = threadIdx.x; j < n; j += blockDim.x)
+      if (base + j < (uint32_t)kCapCand) cand[row * kCapCand + base + j] = loc[j];
 }
 
 DF_DEV void bitonic_desc(unsigned long long* a, int n) {  // n power of two, block-wide
@@ -338,44 +415,34 @@ DF_DEV void bitonic_desc(unsigned long long* a, int n) {  // n power of two, blo
 
 template <bool kVec4>
 __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(const float* __restrict__ lp, int V, int K,
-                                                                  const TopkScratch* __restrict__ sc,
-                                                                  const unsigned long long* __restrict__ hi,
-                                                                  const unsigned long long* __restrict__ eq,
+                                                                  const TopkRow* __restrict__ sc,
+                                                                  const unsigned long long* __restrict__ cand,
                                                                   int32_t* __restrict__ out_id,
                                                                   float* __restrict__ out_val, int* status) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ unsigned long long cand[];  // [kCapEq] then [kMaxK]
+  extern __shared__ unsigned long long keys[];  // [kCapCand]
   const size_t row = blockIdx.x;
   if (status && *(volatile int*)status == DF_ERR_NAN) return;
-  const uint32_t n_eq = sc[row].cnt_eq, n_hi = sc[row].above;
-  if (n_eq > (uint32_t)kCapEq) {  // threshold bin too crowded: whole-row path
+  const uint32_t n_c = sc[row].count;
+  if (n_c < (uint32_t)K || n_c > (uint32_t)kCapCand) {  // the threshold missed: whole-row select
     topk_row_full<kVec4>(lp, row, V, K, out_id, out_val, status);
     return;
   }
-  unsigned long long* e = cand;
-  unsigned long long* w = cand + kCapEq;
   int n = 1;
-  while (n < (int)n_eq) n <<= 1;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) e[i] = i < (int)n_eq ? eq[row * kCapEq + i] : 0ull;
-  int nk = 1;
-  while (nk < K) nk <<= 1;
-  for (int i = threadIdx.x; i < nk; i += blockDim.x) w[i] = i < (int)n_hi ? hi[row * kMaxK + i] : 0ull;
+  while (n < (int)n_c) n <<= 1;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = i < (int)n_c ? cand[row * kCapCand + i] : 0ull;
   __syncthreads();
-  bitonic_desc(e, n);
-  const int need = K - (int)n_hi;
-  for (int i = threadIdx.x; i < need; i += blockDim.x) w[n_hi + i] = e[i];
-  __syncthreads();
-  bitonic_desc(w, nk);
+  bitonic_desc(keys, n);
   for (int r = threadIdx.x; r < K; r += blockDim.x) {
-    const unsigned long long c = w[r];
+    const unsigned long long c = keys[r];
     out_id[row * K + r] = (int32_t)(~(uint32_t)(c & 0xFFFFFFFFull));
     out_val[row * K + r] = key_float((uint32_t)(c >> 32));
   }
 }
 
 size_t topk_chunked_scratch_bytes(int rows) {
-  return (size_t)rows * (4096 * 4 + sizeof(TopkScratch) + kMaxK * 8 + kCapEq * 8) + 1024;
+  return (size_t)rows * (sizeof(TopkRow) + (size_t)kCapCand * 8) + 1024;
 }
 
 // ----------------------------------------------------------------------------- heap
@@ -432,29 +499,30 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
     n_par[0] = -1; n_dep[0] = 0; n_rank[0] = -1; n_score[0] = 0.f;
     if (B > 0) append(heap_key(0.f + val[0], 1, 0, 0));
     for (int idx = 1; idx <= B; ++idx) {
-      unsigned long long best = cand[0];
-      int bi = 0;
+      // lane maximum as a tree (depth log2 NREG, not a chain through every register)
+      unsigned long long t[NREG];
 #pragma unroll
-      for (int i = 1; i < NREG; ++i)
-        if (cand[i] > best) { best = cand[i]; bi = i; }
+      for (int i = 0; i < NREG; ++i) t[i] = cand[i];
+#pragma unroll
+      for (int st = 1; st < NREG; st <<= 1)
+#pragma unroll
+        for (int i = 0; i + st < NREG; i += 2 * st) t[i] = t[i] > t[i + st] ? t[i] : t[i + st];
+      const unsigned long long best = t[0];
       // warp maximum of the 64-bit lane maxima: the high words with one redux, then the low
       // words among the lanes that hold the top high word
       const uint32_t top_hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
       const bool at_hi = (uint32_t)(best >> 32) == top_hi;
       const uint32_t top_lo = __reduce_max_sync(0xffffffffu, at_hi ? (uint32_t)best : 0u);
       const unsigned long long top = ((unsigned long long)top_hi << 32) | top_lo;
-      const int owner = __ffs(__ballot_sync(0xffffffffu, best == top)) - 1;
-      const int hole = __shfl_sync(0xffffffffu, bi, owner);
-      // the last candidate moves into the hole (or the hole is the last one)
+      // the last candidate moves into the popped one's place (keys are unique, so exactly one
+      // register of one lane equals `top`); then the last place is cleared
       const int last = cnt - 1, ll = last & 31, lr = last >> 5;
       unsigned long long lv = 0ull;
 #pragma unroll
-      for (int i = 0; i < NREG; ++i)
-        if (i == lr) lv = cand[i];
+      for (int i = 0; i < NREG; ++i) lv |= (i == lr) ? cand[i] : 0ull;
       lv = __shfl_sync(0xffffffffu, lv, ll);
 #pragma unroll
-      for (int i = 0; i < NREG; ++i)
-        if (lane == owner && i == hole) cand[i] = lv;
+      for (int i = 0; i < NREG; ++i) cand[i] = cand[i] == top ? lv : cand[i];
 #pragma unroll
       for (int i = 0; i < NREG; ++i)
         if (lane == ll && i == lr) cand[i] = 0ull;
@@ -513,33 +581,39 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
                   float* topk_val, int* status, cudaStream_t st, void* chunk_scratch) {
   const int K = B < V ? B : V;
   if (B > 0) {
-    DF_TRACE("topk", st);
     const int rows = b * D;
-    if (chunk_scratch) {
-      // chunked path: histogram, collect, final select (falls back per row when needed)
+    if (chunk_scratch && V >= 4 * kChunk) {
+      // sampled threshold, one collecting read, exact select (whole-row select per row as fallback)
       unsigned char* base = static_cast<unsigned char*>(chunk_scratch);
-      uint32_t* ghist = reinterpret_cast<uint32_t*>(base);
-      TopkScratch* sc = reinterpret_cast<TopkScratch*>(ghist + (size_t)rows * 4096);
-      unsigned long long* hi = reinterpret_cast<unsigned long long*>(
+      TopkRow* sc = reinterpret_cast<TopkRow*>(base);
+      unsigned long long* cand = reinterpret_cast<unsigned long long*>(
           (reinterpret_cast<uintptr_t>(sc + rows) + 255) & ~uintptr_t(255));
-      unsigned long long* eq = hi + (size_t)rows * kMaxK;
-      const size_t nzero = (size_t)rows * 4096 + (size_t)rows * (sizeof(TopkScratch) / 4);
-      launch_k(zero_u32_kernel, dim3((unsigned)((nzero + 1023) / 1024 < 1024 ? (nzero + 1023) / 1024 : 1024)), dim3(1024), 0, st, 
-          ghist, nzero);
+      {
+        DF_TRACE("topk_sample", st);
+        launch_k(topk_sample_kernel, dim3(rows), dim3(256), 0, st, lp, V, K, sc);
+      }
       const dim3 grid((V + kChunk - 1) / kChunk, rows);
-      launch_k(topk_hist_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, ghist, status);
-      launch_k(topk_collect_kernel, dim3(grid), dim3(kChunkThreads), 0, st, lp, V, K, ghist, sc, hi, eq);
-      const size_t smem = (size_t)(kCapEq + kMaxK) * 8;
+      const size_t smem = (size_t)kCapCand * 8;
       if (ensure_dynamic_smem(topk_final_kernel<true>, smem) != cudaSuccess ||
           ensure_dynamic_smem(topk_final_kernel<false>, smem) != cudaSuccess)
         return DF_ERR_CUDA;
+      {
+        DF_TRACE("topk_collect", st);
+        if ((V & 3) == 0) launch_k(topk_collect_kernel<true>, grid, dim3(kChunkThreads), 0, st, lp, V, sc, cand, status);
+        else launch_k(topk_collect_kernel<false>, grid, dim3(kChunkThreads), 0, st, lp, V, sc, cand, status);
+      }
+      DF_TRACE("topk_select", st);
       if ((V & 3) == 0)
-        launch_k(topk_final_kernel<true>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, hi, eq, topk_id, topk_val, status);
+        launch_k(topk_final_kernel<true>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, cand, topk_id,
+                 topk_val, status);
       else
-        launch_k(topk_final_kernel<false>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, hi, eq, topk_id, topk_val, status);
+        launch_k(topk_final_kernel<false>, dim3(rows), dim3(kTopkThreads), smem, st, lp, V, K, sc, cand, topk_id,
+                 topk_val, status);
     } else if ((V & 3) == 0) {
+      DF_TRACE("topk", st);
       launch_k(topk_rows_kernel<true>, dim3(rows), dim3(kTopkThreads), 0, st, lp, V, K, topk_id, topk_val, status);
     } else {
+      DF_TRACE("topk", st);
       launch_k(topk_rows_kernel<false>, dim3(rows), dim3(kTopkThreads), 0, st, lp, V, K, topk_id, topk_val, status);
     }
   }

@@ -140,3 +140,31 @@ def test_chain_nan_is_reported():
     lp[1, 2, 499] = np.nan
     _, st = _gpu_chain(lp)
     assert st == -6
+
+
+@pytest.mark.parametrize("mode", ["ties", "equal_rows", "neginf"])
+def test_sampled_topk_paths_bit_exact(mode):
+    # vocabularies of 32768 and more use the sampled-threshold top-K; rows where the sampled
+    # threshold cannot hold (all keys equal, heavy ties, -inf mass) must still be exact
+    g = np.random.default_rng(11)
+    b, D, V, B = 2, 4, 40000, 300
+    x = g.normal(0, 3, size=(b, D, V))
+    if mode == "ties":
+        x = np.round(x)                       # large groups of exactly equal keys at the threshold
+    lp = ddtree.log_softmax(x)
+    if mode == "equal_rows":
+        lp[0, 1, :] = np.float32(-np.log(float(V)))   # every key equal: more candidates than the cap
+        lp[1, 3, :V // 2] = np.float32(-30.0)
+    if mode == "neginf":
+        lp[g.random(lp.shape) < 0.7] = -np.inf
+        lp[1, 2, :] = -np.inf                 # a row with no finite key
+    out, st = gpu_ddtree(lp, B)
+    assert st == 0
+    _check_same(out, lp, B)
+
+
+def test_sampled_topk_nan_is_reported():
+    lp = ddtree.log_softmax(np.random.default_rng(4).normal(size=(2, 3, 40000)))
+    lp[1, 2, 39999] = np.nan
+    _, st = gpu_ddtree(lp, 64)
+    assert st == -6
