@@ -30,6 +30,10 @@ Parity pins (see tests/test_oracle_*.py):
   verify.tree_attention   equals causal attention over each root path. PINNED
   verify.greedy_walk/compact  hand-built trees.                        PINNED
   step.spec_generate      token-identical to step.greedy_generate (losslessness). PINNED
+  model.moe_route / moe_block  (mixture-of-experts target) reduction to the dense layer
+                          with one expert, brute force over expert subsets, relabelling
+                          invariance, a torch-library formulation, tree rows = sequential
+                          decode.                                      PINNED
   model.layer_forward     pinned only through the invariants above: the pages
                           print no layer equations or values (a Qwen3-style
                           pre-norm layer is the stated reading).

@@ -14,6 +14,10 @@ Readings taken here (Qwen3 family, the target the pages evaluate):
   embedding in rotate-half form with base theta; grouped-query attention (q head h uses
   kv head h // (Hq/Hkv)); softmax scale 1/sqrt(head_dim); SwiGLU MLP
   down(silu(gate) * up); a final RMSNorm before the tied LM head.
+  The pages also evaluate Qwen3-Coder-30B-A3B-Instruct ([DFlash] SGLang results; [DDTree]
+  "실험 결과"), a mixture-of-experts target; its feed-forward is read as the Qwen3-MoE one:
+  a router softmax over the experts, the top-k experts per token with weights renormalised
+  to sum 1, each expert a SwiGLU feed-forward, no shared expert.
 
 Rows never interact except through attention, and every row is computed with the same
 routine in the same order, so a tree row and the same token decoded alone give bitwise
@@ -103,6 +107,46 @@ def mlp_block(layer, shape, h):
     gu = linear(x, layer.w_gate_up)
     act = silu(gu[:, :F]) * gu[:, F:]
     return h + linear(act, layer.w_down)
+
+
+def moe_route(layer, shape, x):
+    """Router of a mixture-of-experts layer: a softmax over the experts' logits, the top_k
+    experts by probability (lower expert id first among equal probabilities), their weights
+    renormalised to sum to 1.  Returns (ids [n, k], weights [n, k], logits [n, E])."""
+    logits = linear(x, layer.w_router)
+    E, k = logits.shape[1], shape.top_k
+    p = np.exp(logits - logits.max(axis=-1, keepdims=True))
+    p /= p.sum(axis=-1, keepdims=True)
+    ids = np.zeros((len(p), k), dtype=np.int64)
+    w = np.zeros((len(p), k))
+    for i in range(len(p)):
+        order = np.lexsort((np.arange(E), -p[i]))[:k]
+        ids[i] = order
+        w[i] = p[i][order] / np.sum(p[i][order])
+    return ids, w, logits
+
+
+def expert_ffn(layer, e, x_row):
+    """Expert e's SwiGLU feed-forward of one normed row: down(silu(gate x) * up x)."""
+    Fe = layer.w_experts_down.shape[2]
+    gu = np.asarray(layer.w_experts_gate_up[e], np.float64) @ np.asarray(x_row, np.float64)
+    return np.asarray(layer.w_experts_down[e], np.float64) @ (silu(gu[:Fe]) * gu[Fe:])
+
+
+def moe_block(layer, shape, h):
+    """h + sum over the chosen experts of weight * expert(x), x the post-attention-normed rows."""
+    x = rms_norm(h, layer.mlp_norm, shape.rms_eps)
+    ids, w, _ = moe_route(layer, shape, x)
+    y = np.zeros_like(x)
+    for i in range(len(x)):
+        for j in range(shape.top_k):
+            y[i] += w[i, j] * expert_ffn(layer, int(ids[i, j]), x[i])
+    return h + y
+
+
+def ffn_block(layer, shape, h):
+    """The layer's feed-forward half: dense SwiGLU or mixture of experts."""
+    return moe_block(layer, shape, h) if shape.n_experts else mlp_block(layer, shape, h)
 
 
 def lm_head(weights, h):

@@ -59,7 +59,7 @@ def target_tree_forward(tw, tok, parent, depth, cache: KVCache, N):
         cache.v[li][N:N + T] = v
         o = verify.tree_attention(shape, q, cache.k[li], cache.v[li], N, parent)
         h = h + model.linear(o, layer.w_o)
-        h = model.mlp_block(layer, shape, h)
+        h = model.ffn_block(layer, shape, h)
         if li + 1 in shape.feat_layers:
             feats.append(h.copy())
     logits = model.lm_head(tw, h)

@@ -42,6 +42,11 @@ class ModelShape:
     feat_layers: tuple = ()
     block_size: int = 16
     mask_id: int = -1  # -1 means vocab-1
+    # mixture-of-experts feed-forward (n_experts > 0): n_experts SwiGLU experts of width
+    # d_expert, top_k of them per token; d_ff is then unused
+    n_experts: int = 0
+    top_k: int = 0
+    d_expert: int = 0
 
     @property
     def q_dim(self):
@@ -68,6 +73,12 @@ TOY_DRAFTER = ModelShape(1, 128, 4, 4, 32, 512, 512, block_size=4)
 QWEN3_8B_TARGET = ModelShape(36, 4096, 32, 8, 128, 12288, 151936,
                              feat_layers=(2, 10, 18, 26, 34), block_size=16)
 DFLASH_QWEN3_8B_DRAFTER = ModelShape(5, 4096, 32, 8, 128, 12288, 151936, block_size=16)
+
+# Qwen3-Coder-30B-A3B-shaped target (mixture of experts): 48 layers, d 2048, 32 q / 4 kv heads
+# x 128, 128 experts of width 768, 8 per token.
+QWEN3_30B_A3B_TARGET = ModelShape(48, 2048, 32, 4, 128, 768, 151936, feat_layers=(2, 14, 26, 38, 46),
+                                  block_size=16, n_experts=128, top_k=8, d_expert=768)
+DFLASH_QWEN3_30B_A3B_DRAFTER = ModelShape(5, 2048, 32, 4, 128, 6144, 151936, block_size=16)
 
 # Small head_dim-128 shapes for GPU parity: several tiles in every GEMM dimension,
 # ragged vocab tail, GQA group 4, two feature layers.
@@ -110,8 +121,11 @@ class LayerWeights:
     k_norm: np.ndarray      # [hd]
     w_o: np.ndarray         # [d, Hq*hd]
     mlp_norm: np.ndarray    # [d]
-    w_gate_up: np.ndarray   # [2F, d]  rows 0..F-1 gate, F..2F-1 up
+    w_gate_up: np.ndarray   # [2F, d]  rows 0..F-1 gate, F..2F-1 up (dense layers)
     w_down: np.ndarray      # [d, F]
+    w_router: np.ndarray = None        # mixture of experts: [E, d]
+    w_experts_gate_up: np.ndarray = None  # [E, 2 Fe, d]  per expert: gate rows, then up rows
+    w_experts_down: np.ndarray = None     # [E, d, Fe]
 
 
 @dataclass
@@ -132,6 +146,8 @@ def _norm_w(seed, name, n):
 def layer_weights(shape: ModelShape, seed: int, prefix: str, std=0.02) -> LayerWeights:
     d, hd, F = shape.d_model, shape.head_dim, shape.d_ff
     nqkv = (shape.n_q_heads + 2 * shape.n_kv_heads) * hd
+    moe = shape.n_experts > 0
+    E, Fe = shape.n_experts, shape.d_expert
     return LayerWeights(
         attn_norm=_norm_w(seed, prefix + ".attn_norm", d),
         w_qkv=normal(seed, prefix + ".w_qkv", (nqkv, d), std),
@@ -139,8 +155,11 @@ def layer_weights(shape: ModelShape, seed: int, prefix: str, std=0.02) -> LayerW
         k_norm=_norm_w(seed, prefix + ".k_norm", hd),
         w_o=normal(seed, prefix + ".w_o", (d, shape.q_dim), std),
         mlp_norm=_norm_w(seed, prefix + ".mlp_norm", d),
-        w_gate_up=normal(seed, prefix + ".w_gate_up", (2 * F, d), std),
-        w_down=normal(seed, prefix + ".w_down", (d, F), std),
+        w_gate_up=None if moe else normal(seed, prefix + ".w_gate_up", (2 * F, d), std),
+        w_down=None if moe else normal(seed, prefix + ".w_down", (d, F), std),
+        w_router=normal(seed, prefix + ".w_router", (E, d), std) if moe else None,
+        w_experts_gate_up=normal(seed, prefix + ".w_experts_gate_up", (E, 2 * Fe, d), std) if moe else None,
+        w_experts_down=normal(seed, prefix + ".w_experts_down", (E, d, Fe), std) if moe else None,
     )
 
 
