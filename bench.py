@@ -218,7 +218,7 @@ class Clocks:
 
 
 # kernels launched per traced call of each class (the rest launch one kernel per call)
-KERNELS_PER_CALL = {"accept_compact": 3, "logsoftmax": 2, "chain": 3}
+KERNELS_PER_CALL = {"accept_compact": 3, "logsoftmax": 2, "chain": 3, "moe_dispatch": 2}
 
 
 def gemm_algorithmic(b, B, nd_ctx_rows=16):

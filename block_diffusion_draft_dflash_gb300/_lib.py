@@ -27,12 +27,14 @@ class ModelCfg(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_q_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
                 ("n_feat_layers", C.c_int32), ("feat_layers", C.c_int32 * 8), ("block_size", C.c_int32),
-                ("mask_id", C.c_int32), ("rms_eps", C.c_float), ("rope_theta", C.c_float)]
+                ("mask_id", C.c_int32), ("rms_eps", C.c_float), ("rope_theta", C.c_float),
+                ("n_experts", C.c_int32), ("top_k", C.c_int32), ("d_expert", C.c_int32)]
 
 
 class LayerWeights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm",
-                                          "w_gate_up", "w_down")]
+                                          "w_gate_up", "w_down", "w_router", "w_experts_gate_up",
+                                          "w_experts_down")]
 
 
 class ModelWeights(C.Structure):

@@ -16,7 +16,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdflash.so")
 
 SOURCES = ["api.cu", "gemm.cu", "attention.cu", "layers.cu", "ddtree.cu", "ddtree_static.cu", "accept.cu", "trace.cu",
-           "runtime.cu", "plant.cu"]
+           "runtime.cu", "plant.cu", "moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

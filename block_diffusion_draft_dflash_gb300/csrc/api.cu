@@ -9,6 +9,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "layers.h"
+#include "moe.h"
 
 namespace df {
 int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
@@ -53,9 +54,14 @@ inline int* status_of(void* ws) { return reinterpret_cast<int*>(ws); }
   } while (0)
 
 bool cfg_ok(const df_model_cfg* c) {
-  return c && c->n_layers > 0 && c->d_model > 0 && c->d_model % 64 == 0 && c->head_dim == 128 && c->n_kv_heads > 0 &&
+  if (!c || c->n_experts < 0) return false;
+  const bool moe = c->n_experts > 0;
+  if (moe && (c->n_experts % 32 || c->n_experts > 256 || c->top_k < 1 || c->top_k > 32 || c->top_k > c->n_experts ||
+              c->d_expert <= 0 || c->d_expert % 64 || c->d_model % 256))
+    return false;
+  return c->n_layers > 0 && c->d_model > 0 && c->d_model % 64 == 0 && c->head_dim == 128 && c->n_kv_heads > 0 &&
          c->n_q_heads % c->n_kv_heads == 0 && (128 % (c->n_q_heads / c->n_kv_heads)) == 0 &&
-         (c->n_q_heads / c->n_kv_heads) <= 8 && c->d_ff > 0 && c->d_ff % 64 == 0 && c->vocab >= 2 &&
+         (c->n_q_heads / c->n_kv_heads) <= 8 && (moe || (c->d_ff > 0 && c->d_ff % 64 == 0)) && c->vocab >= 2 &&
          c->n_feat_layers >= 0 && c->n_feat_layers <= 8;
 }
 
@@ -69,6 +75,7 @@ struct LayerBufs {
   float* o_part;    // attention split-KV partials
   float* ml_part;
   float2* rope;     // [Rx][64] rotary (cos, sin) of every q/k/v row, filled once per forward
+  MoeBufs moe;      // mixture-of-experts layers only
 };
 
 int nsplit_for(int b, int T, int Hq, int Hkv, int max_keys) {
@@ -81,8 +88,12 @@ size_t layer_partial_bytes(const df_model_cfg* c, int R, int Rx) {
   const int d = c->d_model, F = c->d_ff, qd = c->n_q_heads * 128, nqkv = (c->n_q_heads + 2 * c->n_kv_heads) * 128;
   size_t m = gemm_partial_bytes(Rx, nqkv, d);
   m = std::max(m, gemm_partial_bytes(R, d, qd));
-  m = std::max(m, gemm_partial_bytes(R, 2 * F, d));
-  m = std::max(m, gemm_partial_bytes(R, d, F));
+  if (c->n_experts > 0) {
+    m = std::max(m, gemm_partial_bytes(R, c->n_experts, d));  // router logits
+  } else {
+    m = std::max(m, gemm_partial_bytes(R, 2 * F, d));
+    m = std::max(m, gemm_partial_bytes(R, d, F));
+  }
   return m;
 }
 
@@ -128,6 +139,22 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
   rn.pv = pv; rn.h = B.h; rn.d = d; rn.gain = L.w->mlp_norm; rn.eps = c.rms_eps; rn.out = B.x; rn.ld_out = d;
   rn.rows = R; rn.group_out = 1; rn.group_in = 1; rn.in_off = 0;
   DF_TRY(launch_res_norm(rn, st));
+  if (c.n_experts > 0) {
+    // mixture of experts: router logits -> top-k routing -> expert order -> grouped expert
+    // products (SwiGLU fused into the gate/up one) -> weighted combine + residual + next norm
+    g = GemmDesc{};
+    g.X = B.x; g.W = L.w->w_router; g.M = R; g.N = c.n_experts; g.K = d; g.ldx = d; g.ldw = d;
+    g.mode = kGemmPartial; g.part = B.part; g.view = &pv; g.status = L.status;
+    DF_TRY(launch_gemm(g, st));
+    MoeBufs m = B.moe;
+    DF_TRY(launch_moe_route(pv, R, c.n_experts, c.top_k, m, st));
+    DF_TRY(launch_moe_dispatch(B.x, R, d, c.n_experts, c.top_k, m, st));
+    DF_TRY(launch_moe_experts(L.w->w_experts_gate_up, L.w->w_experts_down, R, d, c.n_experts, c.top_k, c.d_expert,
+                              m, L.status, st));
+    rn = L.out;
+    rn.h = B.h; rn.d = d; rn.eps = c.rms_eps;
+    return launch_moe_combine(m, c.top_k, rn, st);
+  }
   g = GemmDesc{};
   g.X = B.x; g.W = L.w->w_gate_up; g.M = R; g.N = 2 * F; g.K = d; g.ldx = d; g.ldw = d;
   g.mode = kGemmPartial; g.part = B.part; g.view = &pv; g.status = L.status;
@@ -159,9 +186,23 @@ size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs*
   w.B.x = cv.take<df_bf16>(R * d);
   w.B.q = cv.take<df_bf16>(R * Hq * 128);
   w.B.attn = cv.take<df_bf16>(R * Hq * 128);
-  w.B.act = cv.take<df_bf16>(R * F);
+  w.B.act = cv.take<df_bf16>(R * (c->n_experts > 0 ? 1 : F));
   w.B.part = cv.take<float>(layer_partial_bytes(c, (int)R, (int)R) / 4 + 1);
   w.amax = cv.take<unsigned long long>(R);
+  if (c->n_experts > 0) {
+    size_t sz[9];
+    moe_buf_elems((int)R, c->top_k, c->n_experts, d, c->d_expert, sz);
+    MoeBufs& m = w.B.moe;
+    m.topk_id = cv.take<int32_t>(sz[0] / 4);
+    m.topk_w = cv.take<float>(sz[1] / 4);
+    m.counts = cv.take<int32_t>(sz[2] / 4);
+    m.offsets = cv.take<int32_t>(sz[3] / 4);
+    m.pos_of = cv.take<int32_t>(sz[4] / 4);
+    m.pair_token = cv.take<int32_t>(sz[5] / 4);
+    m.xp = cv.take<df_bf16>(sz[6] / 2);
+    m.act = cv.take<df_bf16>(sz[7] / 2);
+    m.out = cv.take<float>(sz[8] / 4);
+  }
   w.B.rope = cv.take<float2>(R * 64);
   // split-KV partials sized for the largest split this call could choose (cache up to 2^20 keys)
   const int ns = nsplit_for(b, n_tree, Hq, Hkv, 1 << 20);
@@ -385,12 +426,29 @@ size_t dflash_target_tree_forward_workspace_size(const df_model_cfg* tcfg, int b
   return target_ws(tcfg, b, n_tree, nullptr, nullptr);
 }
 
+// Every layer carries the weights its feed-forward kind needs, 16-byte aligned (TMA).
+int layers_ok(const df_model_cfg* c, const df_model_weights* w) {
+  for (int i = 0; i < c->n_layers; ++i) {
+    const df_layer_weights& L = w->layers[i];
+    const void* need[] = {L.attn_norm, L.w_qkv, L.q_norm, L.k_norm, L.w_o, L.mlp_norm,
+                          c->n_experts > 0 ? (const void*)L.w_router : (const void*)L.w_gate_up,
+                          c->n_experts > 0 ? (const void*)L.w_experts_gate_up : (const void*)L.w_down,
+                          c->n_experts > 0 ? (const void*)L.w_experts_down : (const void*)L.w_down};
+    for (const void* q : need) {
+      if (!q) return DF_ERR_ARG;
+      if (!al16(q)) return DF_ERR_ALIGN;
+    }
+  }
+  return DF_OK;
+}
+
 int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w, int b, int n_tree, const int32_t* tok,
                                const int32_t* depth, const uint32_t* anc, df_bf16* k_cache, df_bf16* v_cache, int cap,
                                const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat, void* ws,
                                size_t ws_bytes, df_stream stream) {
   if (!cfg_ok(c)) return DF_ERR_SHAPE;
   if (!w || !w->layers || !w->embed || !w->final_norm || b < 0 || n_tree < 1 || cap <= 0) return DF_ERR_ARG;
+  DF_TRY(layers_ok(c, w));
   if (cap % 8) return DF_ERR_SHAPE;
   if (b == 0) return DF_OK;
   if (!tok || !k_cache || !v_cache || !cache_len || !choice) return DF_ERR_ARG;
@@ -448,16 +506,17 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
 
 // ------------------------------------------------------------------------ draft block
 size_t dflash_draft_block_workspace_size(const df_model_cfg* dcfg, int b, int max_new) {
-  if (!cfg_ok(dcfg) || b < 0 || max_new < 0 || dcfg->block_size < 2) return kAlign;
+  if (!cfg_ok(dcfg) || b < 0 || max_new < 0 || dcfg->block_size < 2 || dcfg->n_experts != 0) return kAlign;
   return draft_ws(dcfg, b, max_new, nullptr, nullptr);
 }
 
 int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, const df_bf16* new_feat, int max_new,
                        const int32_t* n_new, df_bf16* ctx_k, df_bf16* ctx_v, int32_t* ctx_len, int cap,
                        const int32_t* bonus, float* logprobs, void* ws, size_t ws_bytes, df_stream stream) {
-  if (!cfg_ok(c) || c->block_size < 2 || c->n_feat_layers < 1) return DF_ERR_SHAPE;
+  if (!cfg_ok(c) || c->block_size < 2 || c->n_feat_layers < 1 || c->n_experts != 0) return DF_ERR_SHAPE;
   if (!w || !w->layers || !w->embed || !w->final_norm || !w->fc || !w->fc_norm) return DF_ERR_ARG;
   if (b < 0 || max_new < 0 || cap <= 0) return DF_ERR_ARG;
+  DF_TRY(layers_ok(c, w));
   if (cap % 8) return DF_ERR_SHAPE;
   if (b == 0) return DF_OK;
   if ((max_new > 0 && (!new_feat || !n_new)) || !ctx_k || !ctx_v || !ctx_len || !bonus || !logprobs) return DF_ERR_ARG;

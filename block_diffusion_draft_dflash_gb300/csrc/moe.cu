@@ -1,0 +1,463 @@
+// Mixture-of-experts feed-forward of the target, for the mixture-of-experts target the
+// pages evaluate (Qwen3-Coder-30B-A3B: [DFlash] SGLang results, summary of "Accelerating
+// Speculative Decoding with Block Diffusion Draft Trees", section "실험 결과").  Reading of
+// its feed-forward (Qwen3-MoE): a router softmax over the experts, the top-k experts per
+// token with weights renormalised to sum 1, each expert a SwiGLU feed-forward.
+//
+//   moe_route_kernel    one warp per token: sums the router logits' partial tiles, fp32
+//                       softmax, k rounds of a warp maximum (lower expert id first among
+//                       equal probabilities), renormalised weights
+//   moe_permute_kernel  one warp: stable counting sort of the (token, choice) pairs by
+//                       expert (ties by token, then choice), expert offsets and counts
+//   moe_gather_kernel   normed rows copied into expert order
+//   moe_gemm_kernel     grouped weight-streaming GEMM on tcgen05 over the stacked expert
+//                       weights: persistent CTAs take work items (token tile of 64 rows,
+//                       expert, 128 output rows) round robin, token tiles outermost, so the
+//                       empty items (token tiles past an expert's count, read on the device)
+//                       are spread evenly and skipped; gate/up items load 64 gate rows and
+//                       the matching 64 up rows, and the epilogue writes silu(g) * u
+//   moe_combine_kernel  h += sum_j w_j expert_out_j, then RMSNorm (as res_norm)
+// No host synchronisation: the routing stays on the device, so a step is graph-capturable.
+#include "common.cuh"
+#include "gemm.h"
+#include "moe.h"
+#include "runtime.h"
+#include "trace.h"
+
+namespace df {
+
+constexpr int kMoeThreads = 192;
+constexpr int kMoeBN = 64;      // token rows per work item (MMA N)
+constexpr int kMoeBK = 64;
+constexpr int kMoeStages = 8;
+constexpr uint32_t kMoeWBytes = 128 * kMoeBK * 2, kMoeXBytes = kMoeBN * kMoeBK * 2;
+constexpr uint32_t kMoeStageBytes = kMoeWBytes + kMoeXBytes;
+enum { kMoeGateUp = 0, kMoeDown = 1 };
+
+// ------------------------------------------------------------------------------ routing
+// grid: ceil(R / 8); block 256: one warp per token.  E a multiple of 32, at most 256.
+__global__ void __launch_bounds__(256) moe_route_kernel(PartialView pv, int R, int E, int k,
+                                                        int32_t* __restrict__ topk_id, float* __restrict__ topk_w) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= R) return;
+  constexpr int kMaxPer = 8;  // E / 32 <= 8
+  const int per = E / 32;
+  float lg[kMaxPer];
+#pragma unroll
+  for (int w = 0; w < kMaxPer / 4; ++w)
+    if (4 * w < per) partial_sum_strided4(pv, w, t, lane, lg + 4 * w);  // experts 128 w + lane + 32 i
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i)
+    if (i < per) m = fmaxf(m, lg[i]);
+  m = warp_max(m);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i)
+    if (i < per) { lg[i] = __expf(lg[i] - m); s += lg[i]; }
+  s = warp_sum(s);
+  const float inv = 1.f / s;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) lg[i] = i < per ? lg[i] * inv : -1.f;  // probabilities; -1 = taken / absent
+  float wsum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    // this lane's best (probability desc, expert id asc), then the warp's
+    unsigned long long best = 0ull;
+    int bi = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+      const int e = (i / 4) * 128 + (i % 4) * 32 + lane;
+      const unsigned long long key =
+          lg[i] >= 0.f ? (((unsigned long long)float_key(lg[i]) << 32) | (uint32_t)(~(uint32_t)e)) : 0ull;
+      if (key > best) { best = key; bi = i; }
+    }
+    const uint32_t top_hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+    const uint32_t top_lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == top_hi ? (uint32_t)best : 0u);
+    const int e = (int)(~top_lo);
+    const float pe = key_float(top_hi);
+    if (best == (((unsigned long long)top_hi << 32) | top_lo)) lg[bi] = -1.f;  // the owner drops it
+    if (lane == 0) {
+      topk_id[(size_t)t * k + j] = e;
+      topk_w[(size_t)t * k + j] = pe;
+    }
+    wsum += pe;
+  }
+  __syncwarp();
+  if (lane < k) topk_w[(size_t)t * k + lane] = topk_w[(size_t)t * k + lane] / wsum;
+}
+
+// one warp: pairs p = t k + j in order; a stable counting sort by expert
+__global__ void __launch_bounds__(32) moe_permute_kernel(int P, int E, int k, const int32_t* __restrict__ topk_id,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ pos_of, int32_t* __restrict__ pair_token) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int cnt[256];
+  __shared__ int off[256];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    const int p = p0 + lane;
+    const bool valid = p < P;
+    const int id = valid ? topk_id[p] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, id);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int base = valid ? cnt[id] : 0;
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) cnt[id] = base + __popc(peers);
+    __syncwarp();
+    if (valid) pos_of[p] = base + rank;  // rank among the expert's pairs, for now
+  }
+  __syncwarp();
+  if (lane == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) { off[e] = acc; acc += cnt[e]; }
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) { counts[e] = cnt[e]; offsets[e] = off[e]; }
+  for (int p = lane; p < P; p += 32) {
+    const int pos = off[topk_id[p]] + pos_of[p];
+    pos_of[p] = pos;
+    pair_token[pos] = p / k;
+  }
+}
+
+// grid: P; block 128: row pos of xp <- row pair_token[pos] of x (d / 8 uint4 per row)
+__global__ void __launch_bounds__(128) moe_gather_kernel(const df_bf16* __restrict__ x, int d,
+                                                         const int32_t* __restrict__ pair_token,
+                                                         df_bf16* __restrict__ xp) {
+  pdl_wait();
+  pdl_trigger();
+  const int pos = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)pair_token[pos] * d);
+  uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+// ------------------------------------------------------------------------- grouped GEMM
+struct MoeGemmParams {
+  int E, n_wt, n_tt, k_iters;   // work items n_tt x E x n_wt
+  const int32_t* counts;
+  const int32_t* offsets;
+  int Fe, d;
+  df_bf16* act;                 // gate/up: [P][Fe]
+  float* out;                   // down: [P][d]
+  int* status;
+};
+
+DF_DEV void moe_item(const MoeGemmParams& p, int it, int& tt, int& e, int& wt) {
+  tt = it / (p.E * p.n_wt);
+  const int r = it - tt * p.E * p.n_wt;
+  e = r / p.n_wt;
+  wt = r - e * p.n_wt;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kMoeThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    const MoeGemmParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int S = kMoeStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * kMoeStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 2;
+  uint64_t* mma_drain = bars + 2 * S + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  float* xbuf = reinterpret_cast<float*>(bars + 2 * S + 8);  // gate/up epilogue: [64 rows][64 tokens] of up values
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&tfull[i], 1); mbar_init(&tempty[i], 128); }
+    mbar_init(mma_drain, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, 2 * kMoeBN); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // counts, offsets and the expert-ordered rows come from the previous kernels
+  pdl_trigger();
+  const int n_items = p.n_tt * p.E * p.n_wt;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      int tt, e, wt;
+      moe_item(p, it, tt, e, wt);
+      if (tt * kMoeBN >= p.counts[e]) continue;
+      const int xrow = p.offsets[e] + tt * kMoeBN;
+      for (int k = 0; k < p.k_iters; ++k) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 21)) { ok = false; break; }
+        unsigned char* sb = smem + (size_t)stage * kMoeStageBytes;
+        mbar_arrive_expect_tx(&full[stage], kMoeStageBytes);
+        if (MODE == kMoeGateUp) {
+          const int g0 = e * 2 * p.Fe + wt * 64;  // 64 gate rows, then the matching 64 up rows
+          tma_load_2d(sb, &tmW, &full[stage], k * kMoeBK, g0, pol_w);
+          tma_load_2d(sb + kMoeWBytes / 2, &tmW, &full[stage], k * kMoeBK, g0 + p.Fe, pol_w);
+        } else {
+          tma_load_2d(sb, &tmW, &full[stage], k * kMoeBK, e * p.d + wt * 128, pol_w);
+        }
+        tma_load_2d(sb + kMoeWBytes, &tmX, &full[stage], k * kMoeBK, xrow, pol_x);
+        ++issued;
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+    }
+    // every load issued has landed before the CTA may exit (bounded waits)
+    const long long n = issued < S ? issued : S;
+    int st = stage;
+    uint32_t ph = phase;
+    for (long long i = 0; i < n; ++i) {
+      if (--st < 0) { st = S - 1; ph ^= 1; }
+      mbar_wait(&full[st], ph, nullptr, 0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, kMoeBN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int si = 0;
+    bool ok = true, issued_any = false;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      int tt, e, wt;
+      moe_item(p, it, tt, e, wt);
+      if (tt * kMoeBN >= p.counts[e]) continue;
+      const int acc = si & 1, use = si >> 1;
+      if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 22)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * kMoeBN;
+      for (int k = 0; k < p.k_iters; ++k) {
+        if (!mbar_wait(&full[stage], phase, p.status, 23)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + (size_t)stage * kMoeStageBytes);
+        const uint64_t adesc = sdesc_kmajor_sw128(sa), bdesc = sdesc_kmajor_sw128(sa + kMoeWBytes);
+#pragma unroll
+        for (int kk = 0; kk < kMoeBK / 16; ++kk)
+          mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+        issued_any = true;
+        mma_commit(&empty[stage]);
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      mma_commit(&tfull[acc]);
+      ++si;
+    }
+    if (issued_any && !ok) {
+      // giving up: the MMAs already issued must finish before TMEM is freed
+      mma_commit(mma_drain);
+      mbar_wait(mma_drain, 0, nullptr, 0);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;      // TMEM lane quarter: rows 32 q .. 32 q + 31
+    const int r = q * 32 + lane;
+    int si = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      int tt, e, wt;
+      moe_item(p, it, tt, e, wt);
+      const int cnt = p.counts[e];
+      if (tt * kMoeBN >= cnt) continue;
+      const int acc = si & 1, use = si >> 1;
+      // the four epilogue warps leave together (they meet at named barriers below)
+      const bool ok = mbar_wait(&tfull[acc], use & 1, p.status, 24);
+      uint32_t all_ok;
+      asm volatile("{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.and.pred b, 1, 128, a;\n"
+                   " selp.u32 %0, 1, 0, b;\n}" : "=r"(all_ok) : "r"((uint32_t)ok) : "memory");
+      if (!all_ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kMoeBN;
+      float v[kMoeBN];
+#pragma unroll
+      for (int c = 0; c < kMoeBN; c += 16) tmem_ld16(taddr + c, v + c);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);  // the accumulator may be reused while the values are written out
+      const int n_ok = min(kMoeBN, cnt - tt * kMoeBN);
+      const size_t row0 = (size_t)p.offsets[e] + (size_t)tt * kMoeBN;
+      if (MODE == kMoeGateUp) {
+        // rows 0..63: gate of features 64 wt + r; rows 64..127: the matching up
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the previous item's readers are done
+        if (r >= 64)
+#pragma unroll
+          for (int c = 0; c < kMoeBN; ++c) xbuf[(r - 64) * kMoeBN + c] = v[c];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (r < 64) {
+          df_bf16* dst = p.act + row0 * p.Fe + wt * 64 + r;
+          for (int c = 0; c < n_ok; ++c) {
+            const float g = v[c], u = xbuf[r * kMoeBN + c];
+            dst[(size_t)c * p.Fe] = f_to_bf16(g / (1.f + __expf(-g)) * u);
+          }
+        }
+      } else {
+        float* dst = p.out + row0 * p.d + wt * 128 + r;
+        for (int c = 0; c < n_ok; ++c) dst[(size_t)c * p.d] = v[c];
+      }
+      ++si;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, 2 * kMoeBN);
+  }
+}
+
+// ----------------------------------------------------------------------------- combine
+// grid: output rows; block d / 8 threads (two float4 each), d a multiple of 256, <= 8192.
+__global__ void __launch_bounds__(1024) moe_combine_kernel(ResNormArgs a, const float* __restrict__ out,
+                                                           const float* __restrict__ topk_w,
+                                                           const int32_t* __restrict__ pos_of, int k) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[32];
+  const int o = blockIdx.x;
+  const int t = (o / a.group_out) * a.group_in + a.in_off + (o % a.group_out);
+  float4 v[2];
+  const int per = blockDim.x * 4;
+  float ss = 0.f;
+  float* hrow = a.h + (size_t)t * a.d;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int n = i * per + threadIdx.x * 4;
+    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n >= a.d) continue;
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {  // choices in order: a fixed summation order
+      const float w = topk_w[(size_t)t * k + j];
+      const float4 e = *reinterpret_cast<const float4*>(out + (size_t)pos_of[(size_t)t * k + j] * a.d + n);
+      y.x += w * e.x; y.y += w * e.y; y.z += w * e.z; y.w += w * e.w;
+    }
+    const float4 hv = *reinterpret_cast<const float4*>(hrow + n);
+    y.x += hv.x; y.y += hv.y; y.z += hv.z; y.w += hv.w;
+    *reinterpret_cast<float4*>(hrow + n) = y;
+    v[i] = y;
+    ss += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+  }
+  ss = warp_sum(ss);
+  const int nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < nw; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / a.d + a.eps);
+  const uint2* g = reinterpret_cast<const uint2*>(a.gain);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int n = i * per + threadIdx.x * 4;
+    if (n >= a.d) continue;
+    const float4 y = v[i];
+    const uint2 gw = g[n / 4];
+    uint2 r;
+    r.x = (uint32_t)f_to_bf16(y.x * inv * bf16_to_f(gw.x & 0xFFFF)) |
+          ((uint32_t)f_to_bf16(y.y * inv * bf16_to_f(gw.x >> 16)) << 16);
+    r.y = (uint32_t)f_to_bf16(y.z * inv * bf16_to_f(gw.y & 0xFFFF)) |
+          ((uint32_t)f_to_bf16(y.w * inv * bf16_to_f(gw.y >> 16)) << 16);
+    *reinterpret_cast<uint2*>(a.out + (size_t)o * a.ld_out + n) = r;
+    if (a.capture) {
+      uint2 c;
+      c.x = (uint32_t)f_to_bf16(y.x) | ((uint32_t)f_to_bf16(y.y) << 16);
+      c.y = (uint32_t)f_to_bf16(y.z) | ((uint32_t)f_to_bf16(y.w) << 16);
+      *reinterpret_cast<uint2*>(a.capture + (size_t)t * a.ld_capture + n) = c;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- host
+size_t moe_buf_elems(int R, int k, int E, int d, int Fe, size_t* sz) {
+  const size_t P = (size_t)R * k;
+  sz[0] = P * 4;            // topk_id
+  sz[1] = P * 4;            // topk_w
+  sz[2] = (size_t)E * 4;    // counts
+  sz[3] = (size_t)E * 4;    // offsets
+  sz[4] = P * 4;            // pos_of
+  sz[5] = P * 4;            // pair_token
+  sz[6] = P * d * 2;        // xp
+  sz[7] = P * Fe * 2;       // act
+  sz[8] = P * d * 4;        // out
+  size_t t = 0;
+  for (int i = 0; i < 9; ++i) t += sz[i];
+  return t;
+}
+
+int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, cudaStream_t st) {
+  if (E % 32 || E > 256 || k < 1 || k > 32 || k > E) return DF_ERR_SHAPE;
+  DF_TRACE("moe_route", st);
+  launch_k(moe_route_kernel, dim3((R + 7) / 8), dim3(256), 0, st, pv, R, E, k, m.topk_id, m.topk_w);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, MoeBufs& m, cudaStream_t st) {
+  DF_TRACE("moe_dispatch", st);
+  const int P = R * k;
+  launch_k(moe_permute_kernel, dim3(1), dim3(32), 0, st, P, E, k, m.topk_id, m.counts, m.offsets, m.pos_of,
+           m.pair_token);
+  launch_k(moe_gather_kernel, dim3(P), dim3(128), 0, st, x, d, m.pair_token, m.xp);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_moe_experts(const df_bf16* w_gate_up, const df_bf16* w_down, int R, int d, int E, int k, int Fe,
+                       MoeBufs& m, int* status, cudaStream_t st) {
+  if (Fe % 64 || d % 128) return DF_ERR_SHAPE;
+  const int P = R * k;
+  const size_t smem = 1024 + (size_t)kMoeStages * kMoeStageBytes + (2 * kMoeStages + 8) * 8 + 64 * kMoeBN * 4;
+  if (ensure_dynamic_smem(moe_gemm_kernel<kMoeGateUp>, smem) != cudaSuccess ||
+      ensure_dynamic_smem(moe_gemm_kernel<kMoeDown>, smem) != cudaSuccess)
+    return DF_ERR_CUDA;
+  CUtensorMap tw1, tx1, tw2, tx2;
+  // gate/up: stacked [E * 2 Fe][d] weights in 64-row boxes; token rows xp [P][d]
+  if (make_tmap_2d(&tw1, w_gate_up, (long long)E * 2 * Fe, d, d, 64) || make_tmap_2d(&tx1, m.xp, P, d, d, kMoeBN))
+    return DF_ERR_CUDA;
+  // down: stacked [E * d][Fe] weights in 128-row boxes; token rows act [P][Fe]
+  if (make_tmap_2d(&tw2, w_down, (long long)E * d, Fe, Fe, 128) || make_tmap_2d(&tx2, m.act, P, Fe, Fe, kMoeBN))
+    return DF_ERR_CUDA;
+  MoeGemmParams p{};
+  p.E = E;
+  p.n_tt = (R + kMoeBN - 1) / kMoeBN;  // an expert gets each token at most once
+  p.counts = m.counts;
+  p.offsets = m.offsets;
+  p.Fe = Fe;
+  p.d = d;
+  p.act = m.act;
+  p.out = m.out;
+  p.status = status;
+  const int grid = num_sms();
+  {
+    DF_TRACE("moe_gemm_gate_up", st);
+    p.n_wt = Fe / 64;
+    p.k_iters = d / kMoeBK;
+    launch_k(moe_gemm_kernel<kMoeGateUp>, dim3(grid), dim3(kMoeThreads), smem, st, tw1, tx1, p);
+  }
+  {
+    DF_TRACE("moe_gemm_down", st);
+    p.n_wt = d / 128;
+    p.k_iters = Fe / kMoeBK;
+    launch_k(moe_gemm_kernel<kMoeDown>, dim3(grid), dim3(kMoeThreads), smem, st, tw2, tx2, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_moe_combine(const MoeBufs& m, int k, const ResNormArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return DF_OK;
+  if (a.d % 256 || a.d > 8192 || !a.h) return DF_ERR_SHAPE;
+  DF_TRACE("moe_combine", st);
+  launch_k(moe_combine_kernel, dim3(a.rows), dim3(a.d / 8), 0, st, a, m.out, m.topk_w, m.pos_of, k);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+}  // namespace df

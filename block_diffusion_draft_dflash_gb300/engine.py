@@ -21,6 +21,10 @@ import torch
 from . import _lib
 
 
+_LAYER_KEYS = ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down", "w_router",
+               "w_experts_gate_up", "w_experts_down")
+
+
 def _bf16(x, device):
     return torch.as_tensor(np.ascontiguousarray(x), dtype=torch.float32).to(device=device, dtype=torch.bfloat16).contiguous()
 
@@ -48,11 +52,13 @@ class DeviceModel:
         cfg.block_size = shape.block_size
         cfg.mask_id = shape.mask_token
         cfg.rms_eps, cfg.rope_theta = shape.rms_eps, shape.rope_theta
+        cfg.n_experts, cfg.top_k, cfg.d_expert = shape.n_experts, shape.top_k, shape.d_expert
         self.cfg = cfg
         arr = (_lib.LayerWeights * shape.n_layers)()
         for i, L in enumerate(layers):
-            for k in ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down"):
-                setattr(arr[i], k, L[k].data_ptr())
+            for k in _LAYER_KEYS:
+                if L.get(k) is not None:
+                    setattr(arr[i], k, L[k].data_ptr())
         self._layer_arr = arr
         w = _lib.ModelWeights()
         w.layers = C.cast(arr, C.POINTER(_lib.LayerWeights))
@@ -67,8 +73,7 @@ class DeviceModel:
         """From synth.ModelWeights (numpy, bf16-representable values)."""
         layers = []
         for L in mw.layers:
-            layers.append({k: _bf16(getattr(L, k), device) for k in
-                           ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down")})
+            layers.append({k: _bf16(getattr(L, k), device) for k in _LAYER_KEYS if getattr(L, k) is not None})
         emb = embed if embed is not None else _bf16(mw.embed, device)
         fc = _bf16(mw.fc, device) if mw.fc is not None else None
         fcn = _bf16(mw.fc_norm, device) if mw.fc_norm is not None else None
@@ -82,15 +87,22 @@ class DeviceModel:
         nqkv = (shape.n_q_heads + 2 * shape.n_kv_heads) * hd
         gain = lambda name, n: device_normal((n,), 0.1, seed, name, device, mean=1.0)
         layers = []
+        E, Fe = shape.n_experts, shape.d_expert
         for i in range(shape.n_layers):
             p = f"{role}.{i}"
-            layers.append(dict(
+            L = dict(
                 attn_norm=gain(p + ".attn_norm", d), w_qkv=device_normal((nqkv, d), std, seed, p + ".w_qkv", device),
                 q_norm=gain(p + ".q_norm", hd), k_norm=gain(p + ".k_norm", hd),
                 w_o=device_normal((d, shape.q_dim), std, seed, p + ".w_o", device),
-                mlp_norm=gain(p + ".mlp_norm", d),
-                w_gate_up=device_normal((2 * F, d), std, seed, p + ".w_gate_up", device),
-                w_down=device_normal((d, F), std, seed, p + ".w_down", device)))
+                mlp_norm=gain(p + ".mlp_norm", d))
+            if E:
+                L.update(w_router=device_normal((E, d), std, seed, p + ".w_router", device),
+                         w_experts_gate_up=device_normal((E, 2 * Fe, d), std, seed, p + ".w_experts_gate_up", device),
+                         w_experts_down=device_normal((E, d, Fe), std, seed, p + ".w_experts_down", device))
+            else:
+                L.update(w_gate_up=device_normal((2 * F, d), std, seed, p + ".w_gate_up", device),
+                         w_down=device_normal((d, F), std, seed, p + ".w_down", device))
+            layers.append(L)
         emb = embed if embed is not None else device_normal((shape.vocab, d), std, seed, "embed", device)
         fc = fcn = None
         if n_feat is not None:

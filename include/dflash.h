@@ -75,6 +75,10 @@ typedef struct {
   int32_t block_size;          /* drafter: L (row 0 bonus, rows 1..L-1 mask)         */
   int32_t mask_id;             /* drafter: mask token id                             */
   float rms_eps, rope_theta;
+  int32_t n_experts;           /* target: 0 = dense feed-forward; else a mixture of   */
+  int32_t top_k;               /*   n_experts SwiGLU experts of width d_expert, top_k  */
+  int32_t d_expert;            /*   per token (n_experts a multiple of 32, <= 256;     */
+                               /*   d_expert a multiple of 64; d_model of 256)         */
 } df_model_cfg;
 
 /* One decoder layer's weights (all bf16, row-major [out][in]). */
@@ -87,6 +91,10 @@ typedef struct {
   const df_bf16* mlp_norm;     /* [d]                                                */
   const df_bf16* w_gate_up;    /* [2 F][d]: gate rows 0..F-1, up rows F..2F-1        */
   const df_bf16* w_down;       /* [d][F]                                             */
+  /* mixture-of-experts layers (n_experts > 0; w_gate_up and w_down unused):          */
+  const df_bf16* w_router;     /* [E][d]                                             */
+  const df_bf16* w_experts_gate_up;  /* [E][2 Fe][d]: per expert gate rows, then up  */
+  const df_bf16* w_experts_down;     /* [E][d][Fe]                                   */
 } df_layer_weights;
 
 typedef struct {
@@ -115,7 +123,8 @@ typedef struct {
  * runs through the layers, each row attending to every context slot and every block
  * row (no mask).  Rows 1..L-1 give log-probs (fp32 log-softmax of the logits).
  *
- *   dcfg, dw      drafter shape / weights (dw->embed is the shared embedding)
+ *   dcfg, dw      drafter shape / weights (dw->embed is the shared embedding); a dense
+ *                 feed-forward (n_experts = 0)
  *   new_feat      [b][max_new][n_feat * d] bf16; rows >= n_new[s] are ignored
  *   n_new         [b] int32, 0 <= n_new <= max_new
  *   ctx_k         [n_layers][b][Hkv][cap][hd] bf16, in/out
@@ -236,6 +245,11 @@ int tree_verify_attention(int b, int n_tree, int Hq, int Hkv, int hd,
  *
  * [DDTree] "핵심 아이디어" / "방법론 자세히 보기": the tree is verified in one target
  * forward pass under the ancestor-only mask.
+ *
+ * The target's feed-forward may be a mixture of experts (tcfg->n_experts > 0: [DFlash]
+ * and [DDTree] "실험 결과" evaluate Qwen3-Coder-30B-A3B; read as the Qwen3-MoE layer: a
+ * router softmax over the experts, the top_k experts per token, weights renormalised to
+ * sum 1, SwiGLU experts).  Routing stays on the device (no host synchronisation).
  *
  * Node i of sequence s (token tok[s][i]) is rotated at position cache_len[s] + depth[s][i];
  * its K/V go to slot cache_len[s] + i of every layer; attention is tree_verify_attention.

@@ -1,0 +1,111 @@
+"""The mixture-of-experts target on the GPU vs the oracle: the target tree forward with
+router, top-k routing, expert-ordered grouped expert products and the weighted combine.
+
+Routing is a discrete decision on slightly different inputs (bf16 activations on the GPU,
+float64 in the oracle), so with a random router rows are compared where the oracle's k-th
+and (k+1)-th router logits are clear of that noise; elsewhere the GPU may have picked the
+other expert.  An all-zero router makes every probability equal, so the lower-id rule sends
+every token to experts 0 .. k-1 with weight 1/k on both sides: every row is compared, the
+routed experts hold all rows (several token tiles, a ragged last one) and the rest are empty.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from block_diffusion_draft_dflash_gb300 import _lib, engine
+from oracle import ddtree, model, step, verify
+
+from gpu_util import bf16_dev, cache_to_oracle, rel_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+N_CTX, CAP = 37, 512
+
+
+def _shape(E, k):
+    return synth.ModelShape(1, 512, 8, 2, 128, 0, 4000, feat_layers=(1,), block_size=8, n_experts=E, top_k=k,
+                            d_expert=128)
+
+
+def _tree(shape, B, seed):
+    rng = np.random.default_rng(seed)
+    t = ddtree.build_tree(ddtree.log_softmax(rng.normal(0, 2, size=(5, shape.vocab))), B)
+    t["tok"][0] = 9
+    return t
+
+
+def _cache(shape, seed):
+    kc = synth.normal(seed, "mk", (1, 1, shape.n_kv_heads, CAP, 128))
+    vc = synth.normal(seed, "mv", (1, 1, shape.n_kv_heads, CAP, 128))
+    kc[..., N_CTX:, :] = 0
+    vc[..., N_CTX:, :] = 0
+    return kc, vc
+
+
+def _oracle_cache(kc, vc):
+    return cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), 0)
+
+
+def _gpu_forward(tw, t, kc, vc):
+    shape = tw.shape
+    tm = engine.DeviceModel.from_host(tw)
+    T = len(t["tok"])
+    k_t = bf16_dev(kc)
+    v_t = bf16_dev(vc).transpose(-1, -2).contiguous()
+    st = lambda key: torch.from_numpy(t[key][None].astype(np.int32)).cuda()
+    anc = torch.from_numpy(ddtree.ancestor_mask(t["parent"])[None].view(np.int32)).cuda()
+    clen = torch.tensor([N_CTX], dtype=torch.int32, device="cuda")
+    choice = torch.zeros(1, T, dtype=torch.int32, device="cuda")
+    feat = torch.zeros(1, T, shape.d_model, dtype=torch.bfloat16, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, 1, T))
+    _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k_t, v_t, clen, choice, feat, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    return choice[0].cpu().numpy(), to_np(feat[0])
+
+
+def _router_margin(tw, t, kc, vc):
+    """Per tree row, the gap between the oracle's k-th and (k+1)-th router logits."""
+    shape, L = tw.shape, tw.layers[0]
+    pos = N_CTX + t["depth"]
+    h = np.asarray(tw.embed, np.float64)[t["tok"]]
+    q, k, v = model.qkv_rows(L, shape, model.rms_norm(h, L.attn_norm, shape.rms_eps))
+    q, k = model.qk_finish(L, shape, q, k, pos)
+    c = _oracle_cache(kc, vc)
+    c.k[0][N_CTX:N_CTX + len(pos)] = k
+    c.v[0][N_CTX:N_CTX + len(pos)] = v
+    h = h + model.linear(verify.tree_attention(shape, q, c.k[0], c.v[0], N_CTX, t["parent"]), L.w_o)
+    lg = np.sort(model.linear(model.rms_norm(h, L.mlp_norm, shape.rms_eps), L.w_router), axis=-1)[:, ::-1]
+    return lg[:, shape.top_k - 1] - lg[:, shape.top_k]
+
+
+def _check(tw, t, kc, vc, rows):
+    choice, feat = _gpu_forward(tw, t, kc, vc)
+    och, ofeat, ologits = step.target_tree_forward(tw, t["tok"], t["parent"], t["depth"], _oracle_cache(kc, vc), N_CTX)
+    rel_close(feat[rows], ofeat[rows])
+    top2 = np.sort(ologits, axis=-1)[:, -2:]
+    sure = rows & ((top2[:, 1] - top2[:, 0]) > 0.02 * np.abs(ologits).max())
+    assert sure.mean() > 0.3
+    np.testing.assert_array_equal(choice[sure], och[sure])
+
+
+@pytest.mark.parametrize("E,k,B", [(32, 4, 64), (32, 8, 300), (64, 2, 40), (128, 8, 256)])
+def test_moe_target_tree_forward_matches_oracle(E, k, B):
+    tw = synth.target_weights(_shape(E, k), 5000 + E + B)
+    t = _tree(tw.shape, B, E + B)
+    kc, vc = _cache(tw.shape, E + B)
+    clear = _router_margin(tw, t, kc, vc) > 0.02
+    assert clear.mean() > 0.4
+    _check(tw, t, kc, vc, clear)
+
+
+@pytest.mark.parametrize("k,B", [(8, 300), (1, 130)])
+def test_moe_all_tokens_to_the_lowest_experts(k, B):
+    tw = synth.target_weights(_shape(32, k), 6000 + B)
+    tw.layers[0].w_router[:] = 0
+    t = _tree(tw.shape, B, B)
+    kc, vc = _cache(tw.shape, B)
+    ids, w, _ = model.moe_route(tw.layers[0], tw.shape, np.ones((1, tw.shape.d_model)))
+    assert ids[0].tolist() == list(range(k)) and np.all(w == 1.0 / k)
+    _check(tw, t, kc, vc, np.ones(B + 1, bool))
