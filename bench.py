@@ -18,6 +18,10 @@ accept_and_compact, captured once as a CUDA graph and replayed.
                                    8192), then walk + compaction over 36 layers
   python bench.py --mode prefill   prompt pass (target chain + drafter context), 512 and
                                    4096 tokens
+  python bench.py --target qwen3-coder-30b-a3b
+                                   the step with the mixture-of-experts target (48 layers,
+                                   d 2048, 128 experts of width 768, 8 per token) and its
+                                   5-layer d-2048 drafter
   python bench.py --impl reference (the CPU oracle, timed on a bounded sample)
 
 Several GPUs run independent replicas (the step has no cross-sequence exchange):
@@ -53,31 +57,68 @@ def parse():
                     help="probability per draft depth that the drafter's log-probs lean on the target's greedy "
                          "continuation (0 = no planting)")
     ap.add_argument("--plant-bias", type=float, default=16.0, help="logit bias of a planted token")
+    ap.add_argument("--target", default="qwen3-8b", choices=["qwen3-8b", "qwen3-coder-30b-a3b"],
+                    help="step mode: the dense Qwen3-8B-shaped target, or the mixture-of-experts "
+                         "Qwen3-Coder-30B-A3B-shaped one (48 layers, 128 experts, 8 per token)")
     ap.add_argument("--draft-mode", default="tree", choices=["tree", "chain"],
                     help="tree: DDTree of B nodes; chain: vanilla DFlash (argmax chain of 15)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample-json", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree", "draft", "layer"],
+    ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree", "draft", "layer", "moe"],
                     help="run one small isolated case of a kernel a few times (for ncu captures), no JSON")
     ap.add_argument("--case-n", type=int, default=24576, help="gemm case: weight rows (output features)")
     ap.add_argument("--case-k", type=int, default=4096, help="gemm case: reduction length")
     return ap.parse_args()
 
 
+def shapes(a):
+    """(target, drafter) model shapes of the step."""
+    import synth
+    if getattr(a, "target", "qwen3-8b") == "qwen3-coder-30b-a3b":
+        return synth.QWEN3_30B_A3B_TARGET, synth.DFLASH_QWEN3_30B_A3B_DRAFTER
+    return synth.QWEN3_8B_TARGET, synth.DFLASH_QWEN3_8B_DRAFTER
+
+
+def target_label(a):
+    return "Qwen3-Coder-30B-A3B" if getattr(a, "target", "qwen3-8b") == "qwen3-coder-30b-a3b" else "Qwen3-8B"
+
+
+def metric_of(a):
+    return METRIC if target_label(a) == "Qwen3-8B" else METRIC.replace("Qwen3-8B", target_label(a))
+
+
+def layer_params(S):
+    """Weight elements of one layer of shape S (all experts of a mixture-of-experts layer)."""
+    d, nq = S.d_model, S.n_q_heads * S.head_dim
+    attn = (nq + 2 * S.n_kv_heads * S.head_dim) * d + d * nq
+    if S.n_experts:
+        return attn + S.n_experts * d + S.n_experts * 3 * S.d_expert * d
+    return attn + 3 * S.d_ff * d
+
+
 def workload_name(a):
+    TS, DS = shapes(a)
+    moe = f", {TS.n_experts} experts x {TS.d_expert} (top {TS.top_k})" if TS.n_experts else ""
     draft = f"B={a.budget}" if a.draft_mode == "tree" else "DFlash chain of 15 (no tree)"
-    return (f"DFlash+DDTree spec step, Qwen3-8B-shaped target (36L) + 5L drafter, block 16, "
-            f"{draft}, ctx {a.ctx}, b={a.batch}, acceptance planted at {a.accept_rate}")
+    return (f"DFlash+DDTree spec step, {target_label(a)}-shaped target ({TS.n_layers}L{moe}) + {DS.n_layers}L "
+            f"drafter, block 16, {draft}, ctx {a.ctx}, b={a.batch}, acceptance planted at {a.accept_rate}")
 
 
 def config(a, impl="gb300"):
     timing = ("CUDA graph replay of whole steps, CUDA events on the launching stream" if impl == "gb300" else
               "oracle on the host cores: wall-clock of a bounded sample of one step, scaled to the whole step")
-    return {"workload": workload_name(a), "global_batch": a.batch * a.gpus, "block": 16,
-            "budget": a.budget if a.draft_mode == "tree" else 15, "draft_mode": a.draft_mode,
-            "accept_rate": a.accept_rate, "ctx": a.ctx, "target_layers": 36, "drafter_layers": 5, "vocab": 151936,
-            "l2": "inputs larger than L2 (about 17 GB of weights streamed per step)",
-            "timing": timing, "parallelism": f"replicas x{a.gpus}"}
+    TS, DS = shapes(a)
+    gb = 2 * (TS.n_layers * layer_params(TS) + DS.n_layers * layer_params(DS) + TS.vocab * TS.d_model) / 1e9
+    cfg = {"workload": workload_name(a), "global_batch": a.batch * a.gpus, "block": 16,
+           "budget": a.budget if a.draft_mode == "tree" else 15, "draft_mode": a.draft_mode,
+           "accept_rate": a.accept_rate, "ctx": a.ctx, "target_layers": TS.n_layers,
+           "drafter_layers": DS.n_layers, "vocab": TS.vocab,
+           "l2": f"inputs larger than L2 (about {gb:.0f} GB of weights streamed per step)",
+           "timing": timing, "parallelism": f"replicas x{a.gpus}"}
+    if TS.n_experts:
+        cfg.update(target="Qwen3-Coder-30B-A3B shape", n_experts=TS.n_experts, top_k=TS.top_k,
+                   d_expert=TS.d_expert)
+    return cfg
 
 
 # ------------------------------------------------------------------------ oracle timing
@@ -93,16 +134,20 @@ def oracle_sample(a, budget_s=25.0):
     import synth
     from oracle import ddtree, model, verify
 
+    import dataclasses
+
     t_all = time.perf_counter()
-    TS, DS = synth.QWEN3_8B_TARGET, synth.DFLASH_QWEN3_8B_DRAFTER
+    TS, DS = shapes(a)
     B, N, T = a.budget, a.ctx, a.budget + 1
     # DDTree on config-style log-probs
     lp = ddtree.log_softmax(synth.ddtree_logits(1002, 1, 15, TS.vocab)[0])
     t0 = time.perf_counter()
     tree = ddtree.build_tree(lp, B)
     t_tree = time.perf_counter() - t0
-    # one target layer, 8 tree rows
-    lw = synth.layer_weights(TS, 1005, "bench.layer")
+    # one target layer, 8 tree rows (a mixture-of-experts layer holds 16 of its experts: a
+    # row's cost is its top_k experts' products whatever the expert count)
+    TSs = dataclasses.replace(TS, n_experts=16) if TS.n_experts else TS
+    lw = synth.layer_weights(TSs, 1005, "bench.layer")
     rows = 8
     h = synth.normal(1005, "bench.h", (rows, TS.d_model))
     kc = synth.normal(1005, "bench.k", (N + T, TS.n_kv_heads, 128)).astype(np.float64)
@@ -114,19 +159,20 @@ def oracle_sample(a, budget_s=25.0):
     sub_parent = tree["parent"][:rows]
     o = verify.tree_attention(TS, q, kc, vc, N, sub_parent)
     hh = h + model.linear(o, lw.w_o)
-    hh = model.mlp_block(lw, TS, hh)
+    hh = model.ffn_block(lw, TSs, hh)
     t_layer = time.perf_counter() - t0
+    dlw = lw if (DS.d_ff == TS.d_ff and not TS.n_experts) else synth.layer_weights(DS, 1006, "bench.dlayer")
     # drafter layer on 16 rows (attention over ctx + block)
     t0 = time.perf_counter()
     hd = synth.normal(1006, "bench.hd", (16, DS.d_model))
-    x = model.rms_norm(hd, lw.attn_norm, DS.rms_eps)
-    q, k, v = model.qkv_rows(lw, DS, x)
-    q, k = model.qk_finish(lw, DS, q, k, N + np.arange(16))
+    x = model.rms_norm(hd, dlw.attn_norm, DS.rms_eps)
+    q, k, v = model.qkv_rows(dlw, DS, x)
+    q, k = model.qk_finish(dlw, DS, q, k, N + np.arange(16))
     K = np.concatenate([kc[:N], k])
     V = np.concatenate([vc[:N], v])
     o = model.attention_rows(DS, q, lambda i: (K, V))
-    hd = hd + model.linear(o, lw.w_o)
-    model.mlp_block(lw, DS, hd)
+    hd = hd + model.linear(o, dlw.w_o)
+    model.mlp_block(dlw, DS, hd)
     t_dlayer = time.perf_counter() - t0
     # LM-head rows against a 16384-row slice of the embedding, scaled to the full vocab
     Vs = 16384
@@ -140,8 +186,10 @@ def oracle_sample(a, budget_s=25.0):
     return {"value": 1.0 / est, "unit": "spec steps/s", "cores": threads, "kind": "oracle",
             "sample": (f"oracle (numpy fp64, BLAS on {threads} thread(s), Python loops on one) timed on: DDTree "
                        f"build B={B}; 1 target layer x {rows} of {T} tree rows (ctx {N}); 1 drafter layer x 16 rows; "
-                       f"2 LM-head rows x {Vs} vocab; scaled to 36+5 layers, {T} tree rows, {T + 15} full LM-head "
-                       f"rows, b=1 (sample wall {wall:.1f}s)"),
+                       f"2 LM-head rows x {Vs} vocab; scaled to {TS.n_layers}+{DS.n_layers} layers, {T} tree rows, "
+                       f"{T + 15} full LM-head rows, b=1 (sample wall {wall:.1f}s)"
+                       + (f"; {target_label(a)} target: the sampled layer holds 16 of its {TS.n_experts} experts, "
+                          f"each row runs its top {TS.top_k}" if TS.n_experts else "")),
             "est_s_per_step": est, "sample_wall_s": wall}
 
 
@@ -151,7 +199,8 @@ def oracle_sample_threads(a, threads):
     for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(threads)
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--oracle-sample-json",
-                        "--budget", str(a.budget), "--ctx", str(a.ctx)], env=env, capture_output=True, text=True,
+                        "--budget", str(a.budget), "--ctx", str(a.ctx), "--target", a.target], env=env,
+                       capture_output=True, text=True,
                        timeout=900)
     if r.returncode != 0:
         return None
@@ -221,14 +270,22 @@ class Clocks:
 KERNELS_PER_CALL = {"accept_compact": 3, "logsoftmax": 2, "chain": 3, "moe_dispatch": 2}
 
 
-def gemm_algorithmic(b, B, nd_ctx_rows=16):
+def proj_shapes(S):
+    """(N, K) of one layer's projection GEMMs: q/k/v, o, then gate/up + down (dense) or the
+    router (mixture of experts; its expert products are a kernel of their own)."""
+    d, nq = S.d_model, S.n_q_heads * S.head_dim
+    out = [(nq + 2 * S.n_kv_heads * S.head_dim, d), (d, nq)]
+    out += [(S.n_experts, d)] if S.n_experts else [(2 * S.d_ff, d), (d, S.d_ff)]
+    return out
+
+
+def gemm_algorithmic(b, B, TS, DS, nd_ctx_rows=16):
     """Algorithmic bytes and flops of one step's projection GEMMs (class "gemm").
 
     Per launch: weights N*K*2 + input rows M*K*2 + output rows M*N*2 (bf16-sized);
-    flops 2*M*N*K.  Target: 36 layers on b*(B+1) tree rows.  Drafter: 5 layers on b*16
-    block rows (q/k/v also on b*16 context rows) and the context fusion (K = 5*4096).
+    flops 2*M*N*K.  Target: its layers on b*(B+1) tree rows.  Drafter: its layers on b*16
+    block rows (q/k/v also on b*16 context rows) and the context fusion (K = n_feat*d).
     """
-    d, F, nqkv = 4096, 12288, 6144
     byts = flops = 0
 
     def add(M, N, K, n=1):
@@ -236,14 +293,28 @@ def gemm_algorithmic(b, B, nd_ctx_rows=16):
         byts += n * (N * K * 2 + M * K * 2 + M * N * 2)
         flops += n * 2 * M * N * K
     Mt = b * (B + 1)
-    for (N, K) in ((nqkv, d), (d, d), (2 * F, d), (d, F)):
-        add(Mt, N, K, 36)
+    for (N, K) in proj_shapes(TS):
+        add(Mt, N, K, TS.n_layers)
     Md = b * 16
-    add(Md + b * nd_ctx_rows, nqkv, d, 5)
-    for (N, K) in ((d, d), (2 * F, d), (d, F)):
-        add(Md, N, K, 5)
-    add(b * nd_ctx_rows, d, 5 * d)
+    dsh = proj_shapes(DS)
+    add(Md + b * nd_ctx_rows, *dsh[0], DS.n_layers)
+    for (N, K) in dsh[1:]:
+        add(Md, N, K, DS.n_layers)
+    add(b * nd_ctx_rows, DS.d_model, TS.n_feat * TS.d_model)
     return byts, flops
+
+
+def moe_expert_algorithmic(b, B, TS, active):
+    """Algorithmic bytes and flops of the expert products of one step (both grouped GEMM
+    launches of every layer): the weights of every expert that received rows, once
+    (`active` = such (layer, expert) pairs in the step, from the library's routing counts),
+    the expert-ordered input rows, the bf16 activations written and read, the fp32 outputs
+    written."""
+    P, d, Fe, L = b * (B + 1) * TS.top_k, TS.d_model, TS.d_expert, TS.n_layers
+    gate_up = active * 2 * Fe * d * 2 + L * (P * d * 2 + P * Fe * 2)
+    down = active * d * Fe * 2 + L * (P * Fe * 2 + P * d * 4)
+    flops = L * 2 * P * 3 * Fe * d
+    return gate_up, down, flops
 
 
 # DRAM traffic of the target projection GEMMs, from one ncu capture of a 2-layer Qwen3-8B-width
@@ -285,7 +356,7 @@ def job_value(world, b, ms_per_step):
     return world * b * 1000.0 / ms_per_step
 
 
-def traced_breakdown(dec, n_steps):
+def traced_breakdown(dec, n_steps, after_step=None):
     """Per-class device time of eager steps, from the library's CUDA-event tracing."""
     import torch
 
@@ -295,6 +366,8 @@ def traced_breakdown(dec, n_steps):
     _lib.trace_enable(True)
     for _ in range(n_steps):
         dec.step()
+        if after_step is not None:
+            after_step()
     torch.cuda.synchronize()
     rec = _lib.trace_read()
     _lib.trace_enable(False)
@@ -310,25 +383,35 @@ def traced_breakdown(dec, n_steps):
     return per(cls), per(shapes)
 
 
-def step_roofline_ms(b, B, N, hbm_gbs, tc_tflops):
+def step_roofline_ms(b, B, N, hbm_gbs, tc_tflops, TS, DS, active=None):
     """T* for one step: sum over parts of max(bytes / BW, flops / tensor peak) (algorithmic)."""
-    d, F, V, Lt, Ld, Hq, Hkv, hd = 4096, 12288, 151936, 36, 5, 32, 8, 128
+    V, Lt, Ld, hd = TS.vocab, TS.n_layers, DS.n_layers, 128
+    d, dd = TS.d_model, DS.d_model
     T = B + 1
-    per_layer_w = 2 * (6144 * d + d * 4096 + 2 * F * d + d * F)
     parts = []
     # drafter: weights + fc + LM head, ctx KV reads, tiny flops
-    dr_bytes = Ld * per_layer_w + 2 * d * 5 * d + 2 * V * d + b * Ld * Hkv * hd * 2 * 2 * N
-    dr_flops = 2 * (16 * b) * (Ld * per_layer_w / 2 + V * d)
+    dr_w = Ld * layer_params(DS) + dd * TS.n_feat * d + V * dd
+    dr_bytes = 2 * dr_w + b * Ld * DS.n_kv_heads * hd * 2 * 2 * N
+    dr_flops = 2 * (16 * b) * dr_w
     parts.append((dr_bytes, dr_flops))
     # top-K read of log-probs
     parts.append((b * 15 * V * 4, 0))
-    # target projections + LM head
-    tg_bytes = Lt * per_layer_w + 2 * V * d
-    tg_flops = 2 * (b * T) * (Lt * per_layer_w / 2 + V * d)
+    # target projections (a mixture-of-experts layer: the weights of the experts that
+    # received rows, `active` (layer, expert) pairs in the step; each row multiplied by
+    # top_k of them) + LM head
+    tg_w = Lt * layer_params(TS) + V * d
+    if TS.n_experts and active is not None:
+        tg_w -= (Lt * TS.n_experts - active) * 3 * TS.d_expert * d
+    tg_bytes = 2 * tg_w
+    if TS.n_experts:
+        tg_flops = 2 * (b * T) * (Lt * (layer_params(TS) - TS.n_experts * 3 * TS.d_expert * d
+                                        + TS.top_k * 3 * TS.d_expert * d) + V * d)
+    else:
+        tg_flops = 2 * (b * T) * tg_w
     parts.append((tg_bytes, tg_flops))
     # tree attention: KV read once per (seq, kv head), flops over admitted keys only
-    att_bytes = b * Lt * Hkv * hd * 2 * 2 * (N + T)
-    att_flops = b * Lt * 4 * hd * Hq * (T * N + T * 8)
+    att_bytes = b * Lt * TS.n_kv_heads * hd * 2 * 2 * (N + T)
+    att_flops = b * Lt * 4 * hd * TS.n_q_heads * (T * N + T * 8)
     parts.append((att_bytes, att_flops))
     t = sum(max(by / (hbm_gbs * 1e9), fl / (tc_tflops * 1e12)) for by, fl in parts)
     return t * 1e3, sum(p[0] for p in parts)
@@ -343,14 +426,25 @@ def load_peaks():
             float(peaks.get("bf16_tflops_sustained", 1700.0)), "measured" if peaks else "fallback")
 
 
-def lookahead_table(dec, n_steps, table, dev):
-    """Untimed recording pass for the acceptance plant.  Before each of n_steps speculative
-    steps, the target's own greedy continuation of the current prefix (D single-node decodes
-    through the library) is written to table[s][pos][0..D-1], pos = the block's start;
-    then the step runs with the plant reading that table.  Every kernel of the library is
-    deterministic, so a later run from the same prefill replays exactly these steps, and
-    each of them finds its block's entry.  `table` [b][n_pos][D] int32 (all -1 on entry) is
-    filled in place; the decoder's plant must read this same tensor."""
+def lookahead_table(dec, n_steps, table, dev, max_fix=6):
+    """Untimed recording pass for the acceptance plant.  For each of n_steps speculative
+    steps, table[s][pos][0..D-1] (pos = the block's start) receives the target's greedy
+    continuation of the current prefix as the step's own verification computes it:
+
+      1. D single-node decodes through the library from the current prefix;
+      2. the step's draft, plant, tree build and tree verification are run, and the planted
+         path is walked on the host: where the verification's choice at one of its nodes
+         differs from the recorded token (with random-init weights the top two logits are
+         often within bf16 rounding of each other, and a tree of B+1 rows rounds differently
+         from a single row), the verification's choice is adopted and the deeper entries are
+         decoded again from that prefix;
+      3. repeated until the two agree (at most max_fix times), then the step is committed.
+
+    Every kernel of the library is deterministic, so a later run from the same prefill
+    replays exactly these steps and each finds its block's entry.  `table` [b][n_pos][D]
+    int32 (all -1 on entry) is filled in place; the decoder's plant must read this same
+    tensor.  Returns (entries adopted from the verification, steps left unresolved)."""
+    import numpy as np
     import torch
 
     from block_diffusion_draft_dflash_gb300 import _lib
@@ -362,20 +456,69 @@ def lookahead_table(dec, n_steps, table, dev):
     anc = torch.ones(b, 1, 1, dtype=torch.int32, device=dev)
     rows = torch.arange(b, device=dev)
     ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(dec.t.cfg, b, 1), dev)
-    for _ in range(n_steps):
+
+    def record(forced):
+        # decode writes go to slots the tree verification overwrites before reading them
         clen.copy_(dec.cache_len)
         tok.copy_(dec.bonus.view(b, 1))
         pos = dec.cache_len.long()
         for d in range(D):
-            # decode writes go to slots the next tree forward overwrites before reading them
             _lib.target_tree_forward(dec.t.cfg, dec.t.weights, tok, depth, anc, dec.k_cache, dec.v_cache, clen, ch,
                                      None, ws)
+            for s_, f in enumerate(forced):
+                if d in f:
+                    ch[s_, 0] = f[d]
             table[rows, pos, d] = ch[:, 0]
             clen.add_(1)
             tok.copy_(ch)
-        dec.step()
+
+    def walk(forced):
+        """Adopt the verification's choice at the first node of each planted path where it
+        differs from the table; True if any entry changed."""
+        tk = dec.tree["tok"].cpu().numpy()
+        par = dec.tree["parent"].cpu().numpy()
+        cho = dec.choice.cpu().numpy()
+        tab = table[rows, dec.cache_len.long()].cpu().numpy()  # [b][D]
+        changed = False
+        for s_ in range(b):
+            node = 0
+            for dd in range(D):
+                c = int(cho[s_, node])
+                if c != int(tab[s_, dd]):
+                    for k_ in [k_ for k_ in forced[s_] if k_ >= dd]:
+                        del forced[s_][k_]
+                    forced[s_][dd] = c
+                    changed = True
+                    break
+                kids = np.nonzero((par[s_] == node) & (tk[s_] == tab[s_, dd]))[0]
+                if len(kids) == 0:
+                    break  # the path leaves the tree: nothing deeper is verified
+                node = kids[0]
+        return changed
+
+    fixes = unresolved = 0
+    for _ in range(n_steps):
+        forced = [dict() for _ in range(b)]
+        ctx_len0, first0 = dec.ctx_len.clone(), dec.first
+        record(forced)
+        for it in range(max_fix + 1):
+            dec.ctx_len.copy_(ctx_len0)
+            dec.first = first0
+            dec.draft()
+            dec.plant(dec)
+            dec.build_tree()
+            dec.verify()
+            if not walk(forced):
+                break
+            fixes += 1
+            if it == max_fix:
+                unresolved += 1
+                break
+            record(forced)
+        dec.accept()
     torch.cuda.synchronize()
     assert ws.status() == 0 and dec.status() == 0
+    return fixes, unresolved
 
 
 def run_gpu(a, rank, world, local_rank):
@@ -391,7 +534,7 @@ def run_gpu(a, rank, world, local_rank):
     assert _lib.load().dflash_check_device() == 0, "needs a compute-capability 10.3 GPU"
     hbm, tc_burst, tc_sust, peak_src = load_peaks()
 
-    TS, DS = synth.QWEN3_8B_TARGET, synth.DFLASH_QWEN3_8B_DRAFTER
+    TS, DS = shapes(a)
     seed = 1000 + 5 + rank
     tm = engine.DeviceModel.random(TS, seed, "target", dev)
     dm = engine.DeviceModel.random(DS, seed, "drafter", dev, embed=tm.embed, n_feat=TS.n_feat)
@@ -402,6 +545,7 @@ def run_gpu(a, rank, world, local_rank):
     B, T = dec.B, dec.T
     prompt = torch.from_numpy(synth.uniform_ints(seed, "prompt", (b, N), 0, TS.vocab)).to(dev)
     ref = None
+    fixes = unresolved = 0
     if a.accept_rate > 0:
         # untimed: record, step by step, the target's greedy continuation the plant leans the
         # drafter on (the recorded run and the measured run below are the same steps)
@@ -409,7 +553,7 @@ def run_gpu(a, rank, world, local_rank):
         dec.plant = lambda d: _lib.plant_logprobs(d.logprobs, ref, d.cache_len, a.accept_rate, a.plant_bias,
                                                   seed)
         dec.prefill(prompt)
-        lookahead_table(dec, n_steps + 2, ref, dev)
+        fixes, unresolved = lookahead_table(dec, n_steps + 2, ref, dev)
     # prompt pass and the drafter's first context build, timed once each (untimed region)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     torch.cuda.synchronize()
@@ -493,54 +637,97 @@ def run_gpu(a, rank, world, local_rank):
                 disagree += want >= 0 and int(tk[s_, 0]) != want
                 pos_np[s_] += int(na[s_]) + 1
 
-    # live per-kernel breakdown (CUDA events around every library launch, eager steps)
-    kern, kern_shapes = traced_breakdown(dec, 3)
+    # live per-kernel breakdown (CUDA events around every library launch, eager steps); for
+    # a mixture-of-experts target also each step's routing counts
+    routed = []
+    grab = None
+    if TS.n_experts:
+        cbuf = torch.zeros(TS.n_layers, TS.n_experts, dtype=torch.int32, device=dev)
+
+        def grab():
+            _lib.target_expert_counts(dec.t.cfg, b, T, dec.ws_verify, cbuf)
+            routed.append(cbuf.clone())
+    kern, kern_shapes = traced_breakdown(dec, 3, grab)
     # dominant kernel: the target layers' projection GEMMs (gemm_bf16_tc_kernel, partial-tile
     # epilogue), 4 launches per layer; per-launch algorithmic bytes = weights + input rows +
     # output rows (bf16-sized)
-    Mt, d, F = b * T, 4096, 12288
-    t_bytes = t_flops = t_ms = t_launch = 0.0
-    for (Nn, Kk) in ((6144, d), (d, d), (2 * F, d), (d, F)):
-        sh = kern_shapes.get(f"gemm {Mt}x{Nn}x{Kk}")
-        if sh is None:
-            continue
-        t_bytes += sh["launches_per_step"] * (Nn * Kk * 2 + Mt * Kk * 2 + Mt * Nn * 2)
-        t_flops += sh["launches_per_step"] * 2 * Mt * Nn * Kk
-        t_ms += sh["ms_per_step"]
-        t_launch += sh["launches_per_step"]
-    achieved = t_bytes / (t_ms * 1e-3) / 1e9 if t_ms else 0.0
-    traffic = None
-    if b == 1 and T == 257 and gemm_src_hash() == GEMM_TRAFFIC["src_sha256_16"] and t_launch:
-        traffic = round(GEMM_TRAFFIC["bytes_per_layer"] / 4)  # per launch, averaged over the four shapes
+    Mt = b * T
     g_ms = kern["gemm"]["ms_per_step"]
-    g_bytes, g_flops = gemm_algorithmic(b, T - 1)
-    # the binding resource: HBM while the weights dominate (b = 1: 257 flop per byte, just
-    # under the ridge), the tensor cores once b * 257 token rows share each weight byte
-    tensor_bound = t_flops / (tc_sust * 1e12) > t_bytes / (hbm * 1e9)
-    if tensor_bound:
-        achieved = t_flops / (t_ms * 1e-3) / 1e12 if t_ms else 0.0
-    peak_r = tc_sust if tensor_bound else hbm
-    roof = {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(achieved, 1), "peak": peak_r,
-            "unit": "TFLOP/s" if tensor_bound else "GB/s",
-            "frac": round(achieved / peak_r, 4), "traffic": traffic,
-            "peak_source": f"{peak_src} ({'sustained bf16' if tensor_bound else 'HBM copy'})",
-            "kernel": "gemm_bf16_tc_kernel (partial-tile epilogue): the 4 projection launches of each of the "
-                      "36 target layers",
-            "algorithmic_bytes_per_launch": round(t_bytes / t_launch) if t_launch else None,
-            "launches_per_step": t_launch, "ms_per_step": round(t_ms, 4),
-            "timing": "CUDA events around each launch, in 3 eager traced steps after the timed replays",
-            "tflops": round(t_flops / (t_ms * 1e-3) / 1e12, 1) if t_ms else None,
-            "all_projection_gemms": {"ms_per_step": g_ms, "algorithmic_bytes_per_step": g_bytes,
-                                     "achieved_gbs": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
-                                     "launches_per_step": kern["gemm"]["launches_per_step"]}}
-    t_star_ms, step_bytes = step_roofline_ms(b, T - 1, N, hbm, tc_sust)
+    g_bytes, g_flops = gemm_algorithmic(b, T - 1, TS, DS)
+    all_proj = {"ms_per_step": g_ms, "algorithmic_bytes_per_step": g_bytes,
+                "achieved_gbs": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
+                "launches_per_step": kern["gemm"]["launches_per_step"]}
+    timing = "CUDA events around each launch, in 3 eager traced steps after the timed replays"
+    if TS.n_experts:
+        # dominant kernel: the grouped expert GEMM (gate/up with SwiGLU, then down), two
+        # launches per target layer
+        cnt = torch.stack(routed).cpu().numpy()  # [steps][layers][experts]
+        active = float((cnt > 0).sum(axis=(1, 2)).mean())
+        routing = {"active_experts_per_layer": round(active / TS.n_layers, 2),
+                   "token_tiles_per_layer": round(float(((cnt + 63) // 64).sum(axis=(1, 2)).mean()) / TS.n_layers, 2),
+                   "max_rows_per_expert": int(cnt.max()), "rows_per_layer": int(cnt[0, 0].sum()),
+                   "source": "dflash_target_expert_counts after each of the 3 traced steps"}
+        gu_b, dn_b, e_flops = moe_expert_algorithmic(b, T - 1, TS, active)
+        parts = [kern.get(k_, {"ms_per_step": 0.0, "launches_per_step": 0}) for k_ in
+                 ("moe_gemm_gate_up", "moe_gemm_down")]
+        t_ms = sum(p_["ms_per_step"] for p_ in parts)
+        t_launch = sum(p_["launches_per_step"] for p_ in parts)
+        achieved = (gu_b + dn_b) / (t_ms * 1e-3) / 1e9 if t_ms else 0.0
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": f"{peak_src} (HBM copy)",
+                "kernel": f"moe_gemm_kernel (grouped expert GEMM: gate/up + SwiGLU, down), 2 launches in each of "
+                          f"the {TS.n_layers} target layers",
+                "algorithmic_bytes_per_launch": round((gu_b + dn_b) / t_launch) if t_launch else None,
+                "algorithmic_bytes_per_layer": {"gate_up": gu_b // TS.n_layers, "down": dn_b // TS.n_layers},
+                "launches_per_step": t_launch, "ms_per_step": round(t_ms, 4), "timing": timing,
+                "gate_up_gbs": round(gu_b / (parts[0]["ms_per_step"] * 1e-3) / 1e9, 1) if parts[0]["ms_per_step"] else None,
+                "down_gbs": round(dn_b / (parts[1]["ms_per_step"] * 1e-3) / 1e9, 1) if parts[1]["ms_per_step"] else None,
+                "tflops": round(e_flops / (t_ms * 1e-3) / 1e12, 1) if t_ms else None,
+                "routing": routing, "all_projection_gemms": all_proj}
+    else:
+        active = None
+        # dominant kernel: the target layers' projection GEMMs (gemm_bf16_tc_kernel,
+        # partial-tile epilogue), 4 launches per layer; per-launch algorithmic bytes =
+        # weights + input rows + output rows (bf16-sized)
+        t_bytes = t_flops = t_ms = t_launch = 0.0
+        for (Nn, Kk) in proj_shapes(TS):
+            sh = kern_shapes.get(f"gemm {Mt}x{Nn}x{Kk}")
+            if sh is None:
+                continue
+            t_bytes += sh["launches_per_step"] * (Nn * Kk * 2 + Mt * Kk * 2 + Mt * Nn * 2)
+            t_flops += sh["launches_per_step"] * 2 * Mt * Nn * Kk
+            t_ms += sh["ms_per_step"]
+            t_launch += sh["launches_per_step"]
+        achieved = t_bytes / (t_ms * 1e-3) / 1e9 if t_ms else 0.0
+        traffic = None
+        if b == 1 and T == 257 and gemm_src_hash() == GEMM_TRAFFIC["src_sha256_16"] and t_launch:
+            traffic = round(GEMM_TRAFFIC["bytes_per_layer"] / 4)  # per launch, averaged over the four shapes
+        # the binding resource: HBM while the weights dominate (b = 1: 257 flop per byte, just
+        # under the ridge), the tensor cores once b * 257 token rows share each weight byte
+        tensor_bound = t_flops / (tc_sust * 1e12) > t_bytes / (hbm * 1e9)
+        if tensor_bound:
+            achieved = t_flops / (t_ms * 1e-3) / 1e12 if t_ms else 0.0
+        peak_r = tc_sust if tensor_bound else hbm
+        roof = {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(achieved, 1), "peak": peak_r,
+                "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                "frac": round(achieved / peak_r, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} ({'sustained bf16' if tensor_bound else 'HBM copy'})",
+                "kernel": f"gemm_bf16_tc_kernel (partial-tile epilogue): the 4 projection launches of each of the "
+                          f"{TS.n_layers} target layers",
+                "algorithmic_bytes_per_launch": round(t_bytes / t_launch) if t_launch else None,
+                "launches_per_step": t_launch, "ms_per_step": round(t_ms, 4), "timing": timing,
+                "tflops": round(t_flops / (t_ms * 1e-3) / 1e12, 1) if t_ms else None,
+                "all_projection_gemms": all_proj}
+    t_star_ms, step_bytes = step_roofline_ms(b, T - 1, N, hbm, tc_sust, TS, DS, active)
     clk = clocks.summary(local_rank)
     launches = sum(v["launches_per_step"] * KERNELS_PER_CALL.get(k, 1) for k, v in kern.items())
     acc = {"rate": a.accept_rate, "bias": a.plant_bias, "tokens_per_step": round(tau, 3),
            "tokens_per_step_e2e": round(emitted / (a.steps * b), 3),
-           "root_choice_vs_single_row_decode_disagreements": disagree, "steps_without_reference": unplanted,
-           "plant": "per step, the target's greedy continuation of the current prefix (recorded in an untimed "
-                    "pass of the same steps) is planted at each draft depth with probability rate"}
+           "root_choice_vs_reference_disagreements": disagree, "steps_without_reference": unplanted,
+           "reference_entries_adopted_from_verification": fixes, "recording_steps_unresolved": unresolved,
+           "plant": "per step, the target's greedy continuation of the current prefix, as the step's own tree "
+                    "verification computes it (recorded in an untimed pass of the same steps), is planted at each "
+                    "draft depth with probability rate"}
     return dict(ms=ms, e2e_s=e2e_s, emitted=emitted, roof=roof, t_star_ms=t_star_ms, step_bytes=step_bytes,
                 clocks=clk, peak_src=peak_src, hbm=hbm, tc=tc_sust, tau=tau, acc=acc, prefill=prefill,
                 launches=launches, kernels=kern, kernel_shapes=kern_shapes)
@@ -951,6 +1138,30 @@ def kernel_case(a):
             _lib.target_tree_forward(tm.cfg, tm.weights, tok, tr["depth"], tr["anc"], k, v, clen, choice, feat, ws)
         torch.cuda.synchronize()
         assert ws.status() == 0
+    elif a.kernel_case == "moe":
+        # the mixture-of-experts target (Qwen3-Coder-30B-A3B width) 2 layers deep (about 2.5 GB
+        # of weights) over the step's tree: router, dispatch, both grouped expert GEMMs, combine
+        import dataclasses
+        TS = dataclasses.replace(synth.QWEN3_30B_A3B_TARGET, n_layers=2, feat_layers=(1, 2))
+        tm = engine.DeviceModel.random(TS, 5, "target", dev)
+        b, T, N = a.batch, a.budget + 1, a.ctx
+        cap = (N + T + 127) // 128 * 128
+        k = synth.device_normal((2, b, TS.n_kv_heads, cap, 128), 1.0, 5, "case.k", dev)
+        v = synth.device_normal((2, b, TS.n_kv_heads, 128, cap), 1.0, 5, "case.v", dev)
+        tr = library_tree(b, T - 1, 2000, dev)
+        tok = tr["tok"].clone()
+        tok[:, 0] = 1
+        clen = torch.full((b,), N, dtype=torch.int32, device=dev)
+        choice = torch.zeros(b, T, dtype=torch.int32, device=dev)
+        ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T), dev)
+        for _ in range(4):
+            _lib.target_tree_forward(tm.cfg, tm.weights, tok, tr["depth"], tr["anc"], k, v, clen, choice, None, ws)
+        counts = torch.zeros(2, TS.n_experts, dtype=torch.int32, device=dev)
+        _lib.target_expert_counts(tm.cfg, b, T, ws, counts)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        c = counts.cpu().numpy()
+        print("experts with rows per layer", (c > 0).sum(axis=1).tolist(), "max rows", c.max(axis=1).tolist())
     torch.cuda.synchronize()
     print("kernel case", a.kernel_case, "done")
 
@@ -978,7 +1189,7 @@ def main():
         cb["est_s_per_step"] = 1.0 / cb["value"]
         cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
         cpu["nproc"] = os.cpu_count()
-        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "spec steps/s",
+        line = {"impl": "reference", "metric": metric_of(a), "value": cb["value"], "unit": "spec steps/s",
                 "n_gpus": a.gpus, "steps": n, "warmup": 0, "ms_per_step": cb["est_s_per_step"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config(a, impl="reference"),
@@ -1007,7 +1218,7 @@ def main():
     if not a.no_cpu_baseline and world == 1:
         cpu, _ = cpu_baseline(a)
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "spec steps/s", "n_gpus": world, "steps": a.steps,
+        "metric": metric_of(a), "value": round(value, 3), "unit": "spec steps/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(r["ms"], 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, random prompt)",
         "config": config(a),

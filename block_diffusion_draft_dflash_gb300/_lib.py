@@ -66,6 +66,8 @@ _SIGS = {
     "dflash_target_tree_forward_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
     "dflash_target_tree_forward": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int] + [C.c_void_p] * 5 +
                                    [C.c_int] + [C.c_void_p] * 4 + [C.c_size_t, C.c_void_p]),
+    "dflash_target_expert_counts": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p,
+                                              C.c_void_p]),
     "dflash_linear_workspace_size": (C.c_size_t, []),
     "dflash_linear_argmax_workspace_size": (C.c_size_t, [C.c_int]),
     "dflash_linear_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
@@ -249,6 +251,13 @@ def target_tree_forward(cfg: ModelCfg, weights: ModelWeights, tok, depth, anc, k
     _check("dflash_target_tree_forward", load().dflash_target_tree_forward(
         C.byref(cfg), C.byref(weights), b, T, _p(tok), _p(depth), _p(anc), _p(k_cache), _p(v_cache), cap,
         _p(cache_len), _p(choice), _p(tree_feat), ws.ptr, ws.nbytes, _stream()))
+
+
+def target_expert_counts(cfg: ModelCfg, b, n_tree, ws: Workspace, counts):
+    """counts [n_layers][n_experts] int32 <- the last mixture-of-experts tree forward's routing."""
+    _dev(counts, torch.int32, "counts")
+    _check("dflash_target_expert_counts", load().dflash_target_expert_counts(
+        C.byref(cfg), b, n_tree, ws.ptr, ws.nbytes, _p(counts), _stream()))
 
 
 def draft_block_workspace_size(cfg: ModelCfg, b, max_new):

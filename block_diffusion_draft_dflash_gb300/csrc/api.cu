@@ -53,6 +53,9 @@ inline int* status_of(void* ws) { return reinterpret_cast<int*>(ws); }
     if (_rc != DF_OK) return _rc; \
   } while (0)
 
+// Router GEMM (E <= 256 weight rows): each CTA takes at least this many k-steps.
+constexpr int kRouterMinK = 4;
+
 bool cfg_ok(const df_model_cfg* c) {
   if (!c || c->n_experts < 0) return false;
   const bool moe = c->n_experts > 0;
@@ -89,7 +92,7 @@ size_t layer_partial_bytes(const df_model_cfg* c, int R, int Rx) {
   size_t m = gemm_partial_bytes(Rx, nqkv, d);
   m = std::max(m, gemm_partial_bytes(R, d, qd));
   if (c->n_experts > 0) {
-    m = std::max(m, gemm_partial_bytes(R, c->n_experts, d));  // router logits
+    m = std::max(m, gemm_partial_bytes(R, c->n_experts, d, kRouterMinK));  // router logits
   } else {
     m = std::max(m, gemm_partial_bytes(R, 2 * F, d));
     m = std::max(m, gemm_partial_bytes(R, d, F));
@@ -105,6 +108,7 @@ size_t layer_partial_bytes(const df_model_cfg* c, int R, int Rx) {
 struct LayerRun {
   const df_model_cfg* cfg;
   const df_layer_weights* w;
+  int layer;           // index in the model
   int b, T;            // R = b*T query rows
   int Rx;              // rows of the q/k/v projection (R plus context rows)
   QkRopeArgs qk;       // filled except the layer-specific fields
@@ -145,9 +149,11 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
     g = GemmDesc{};
     g.X = B.x; g.W = L.w->w_router; g.M = R; g.N = c.n_experts; g.K = d; g.ldx = d; g.ldw = d;
     g.mode = kGemmPartial; g.part = B.part; g.view = &pv; g.status = L.status;
+    g.min_k_per_cta = kRouterMinK;  // a weight of E <= 256 rows: a few pieces per tile, not one per CTA
     DF_TRY(launch_gemm(g, st));
     MoeBufs m = B.moe;
-    DF_TRY(launch_moe_route(pv, R, c.n_experts, c.top_k, m, st));
+    m.counts += (size_t)L.layer * c.n_experts;  // each layer's expert counts are kept
+    DF_TRY(launch_moe_route(pv, R, c.n_experts, c.top_k, m, L.status, st));
     DF_TRY(launch_moe_dispatch(B.x, R, d, c.n_experts, c.top_k, m, st));
     DF_TRY(launch_moe_experts(L.w->w_experts_gate_up, L.w->w_experts_down, R, d, c.n_experts, c.top_k, c.d_expert,
                               m, L.status, st));
@@ -192,6 +198,7 @@ size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs*
   if (c->n_experts > 0) {
     size_t sz[9];
     moe_buf_elems((int)R, c->top_k, c->n_experts, d, c->d_expert, sz);
+    sz[2] *= c->n_layers;  // expert counts of every layer
     MoeBufs& m = w.B.moe;
     m.topk_id = cv.take<int32_t>(sz[0] / 4);
     m.topk_w = cv.take<float>(sz[1] / 4);
@@ -442,6 +449,19 @@ int layers_ok(const df_model_cfg* c, const df_model_weights* w) {
   return DF_OK;
 }
 
+int dflash_target_expert_counts(const df_model_cfg* c, int b, int n_tree, const void* ws, size_t ws_bytes,
+                                int32_t* counts, df_stream stream) {
+  if (!cfg_ok(c) || c->n_experts == 0) return DF_ERR_SHAPE;
+  if (b <= 0 || n_tree < 1 || !ws || !counts) return DF_ERR_ARG;
+  if (ws_bytes < dflash_target_tree_forward_workspace_size(c, b, n_tree)) return DF_ERR_WORKSPACE;
+  TargetWs W;
+  target_ws(c, b, n_tree, const_cast<void*>(ws), &W);
+  const size_t bytes = (size_t)c->n_layers * c->n_experts * sizeof(int32_t);
+  return cudaMemcpyAsync(counts, W.B.moe.counts, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream) == cudaSuccess
+             ? DF_OK
+             : DF_ERR_CUDA;
+}
+
 int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w, int b, int n_tree, const int32_t* tok,
                                const int32_t* depth, const uint32_t* anc, df_bf16* k_cache, df_bf16* v_cache, int cap,
                                const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat, void* ws,
@@ -476,7 +496,7 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
   }
   for (int li = 0; li < c->n_layers; ++li) {
     LayerRun L{};
-    L.cfg = c; L.w = &w->layers[li]; L.b = b; L.T = n_tree; L.Rx = R; L.status = status;
+    L.cfg = c; L.w = &w->layers[li]; L.layer = li; L.b = b; L.T = n_tree; L.Rx = R; L.status = status;
     QkRopeArgs& qk = L.qk;
     qk.b = b; qk.TA = n_tree; qk.TB = 0; qk.base = cache_len; qk.nnew = nullptr; qk.depth = depth;
     qk.Hq = c->n_q_heads; qk.Hkv = Hkv; qk.eps = c->rms_eps; qk.theta = c->rope_theta;

@@ -529,13 +529,14 @@ static void make_partition(long long total, long long k_iters, int G, bool whole
 }
 
 // The partition of a launch of this shape (cached: it depends on the shape and the SM count only).
-static const Partition& gemm_partition(int M, int N, int K, bool whole_tiles) {
+static const Partition& gemm_partition(int M, int N, int K, bool whole_tiles, int min_k_per_cta = 0) {
   const int BN = gemm_token_tile(M);
   const long long n_tt = (M + BN - 1) / BN, k_iters = K / kBK;
   const long long tiles = (long long)((N + kBM - 1) / kBM) * n_tt;
   const long long total = tiles * k_iters;
   long long G = std::min<long long>(num_sms(), kMaxGrid);
   G = std::min(G, whole_tiles ? tiles : total);
+  if (!whole_tiles && min_k_per_cta > 1) G = std::max(1LL, std::min(G, total / min_k_per_cta));
   const int nbuf = 2 * BN <= 512 ? 2 : 1;
   const int delta = kDrainDelta >= 0 ? kDrainDelta : (nbuf == 2 ? 0 : (BN + 63) / 64);
   static std::mutex mu;
@@ -570,9 +571,9 @@ static PartialLayout partial_layout(int M, int N, int K, const Partition& P) {
   return L;
 }
 
-size_t gemm_partial_bytes(int M, int N, int K) {
+size_t gemm_partial_bytes(int M, int N, int K, int min_k_per_cta) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  return partial_layout(M, N, K, gemm_partition(M, N, K, false)).total_bytes;
+  return partial_layout(M, N, K, gemm_partition(M, N, K, false, min_k_per_cta)).total_bytes;
 }
 
 int launch_gemm(const GemmDesc& g, cudaStream_t st) {
@@ -624,7 +625,7 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
     default: return DF_ERR_ARG;
   }
   if (attr_err != cudaSuccess) return DF_ERR_CUDA;
-  const Partition& P = gemm_partition(g.M, g.N, g.K, p.whole_tiles);
+  const Partition& P = gemm_partition(g.M, g.N, g.K, p.whole_tiles, g.mode == kGemmPartial ? g.min_k_per_cta : 0);
   const long long grid = P.G;
   for (int c = 0; c <= P.G; ++c) p.starts[c] = P.starts[c];
   if (g.mode == kGemmPartial) {

@@ -22,11 +22,13 @@ struct GemmDesc {
   int* status;
   float* part;     // kGemmPartial: slot buffer (size from gemm_partial_bytes)
   PartialView* view;  // kGemmPartial: filled with what consumers need to read the slots
+  int min_k_per_cta;  // kGemmPartial, optional: launch few enough CTAs that each takes at least
+                      // this many k-steps (fewer pieces per tile for a tiny weight; 0 = no limit)
 };
 
 int launch_gemm(const GemmDesc& g, cudaStream_t st);
 // Bytes of partial-tile slots a kGemmPartial launch of this shape writes.
-size_t gemm_partial_bytes(int M, int N, int K);
+size_t gemm_partial_bytes(int M, int N, int K, int min_k_per_cta = 0);
 int make_tmap_2d(struct CUtensorMap_st* out, const void* ptr, long long rows, long long cols, long long ld, int box_rows);
 
 }  // namespace df

@@ -7,7 +7,7 @@
 //   moe_route_kernel    one warp per token: sums the router logits' partial tiles, fp32
 //                       softmax, k rounds of a warp maximum (lower expert id first among
 //                       equal probabilities), renormalised weights
-//   moe_permute_kernel  one warp: stable counting sort of the (token, choice) pairs by
+//   moe_permute_kernel  one CTA: stable counting sort of the (token, choice) pairs by
 //                       expert (ties by token, then choice), expert offsets and counts
 //   moe_gather_kernel   normed rows copied into expert order
 //   moe_gemm_kernel     grouped weight-streaming GEMM on tcgen05 over the stacked expert
@@ -37,7 +37,8 @@ enum { kMoeGateUp = 0, kMoeDown = 1 };
 // ------------------------------------------------------------------------------ routing
 // grid: ceil(R / 8); block 256: one warp per token.  E a multiple of 32, at most 256.
 __global__ void __launch_bounds__(256) moe_route_kernel(PartialView pv, int R, int E, int k,
-                                                        int32_t* __restrict__ topk_id, float* __restrict__ topk_w) {
+                                                        int32_t* __restrict__ topk_id, float* __restrict__ topk_w,
+                                                        int* status) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -75,8 +76,11 @@ __global__ void __launch_bounds__(256) moe_route_kernel(PartialView pv, int R, i
     }
     const uint32_t top_hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
     const uint32_t top_lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == top_hi ? (uint32_t)best : 0u);
-    const int e = (int)(~top_lo);
-    const float pe = key_float(top_hi);
+    // no candidate left only when the logits were NaN: route to expert j with weight 0
+    const bool none = top_hi == 0u;
+    const int e = none ? j : (int)(~top_lo);
+    const float pe = none ? 0.f : key_float(top_hi);
+    if (none && lane == 0) set_status(status, DF_ERR_NAN, 30);
     if (best == (((unsigned long long)top_hi << 32) | top_lo)) lg[bi] = -1.f;  // the owner drops it
     if (lane == 0) {
       topk_id[(size_t)t * k + j] = e;
@@ -85,43 +89,79 @@ __global__ void __launch_bounds__(256) moe_route_kernel(PartialView pv, int R, i
     wsum += pe;
   }
   __syncwarp();
-  if (lane < k) topk_w[(size_t)t * k + lane] = topk_w[(size_t)t * k + lane] / wsum;
+  if (lane < k) topk_w[(size_t)t * k + lane] = wsum > 0.f ? topk_w[(size_t)t * k + lane] / wsum : 0.f;
 }
 
-// one warp: pairs p = t k + j in order; a stable counting sort by expert
-__global__ void __launch_bounds__(32) moe_permute_kernel(int P, int E, int k, const int32_t* __restrict__ topk_id,
-                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                         int32_t* __restrict__ pos_of, int32_t* __restrict__ pair_token) {
+// One CTA of 1024 threads: a stable counting sort of the pairs p = t k + j by expert.
+// Warp w takes the contiguous pairs [w c, (w + 1) c), c = ceil(P / 32): it counts them per
+// expert (lanes with equal experts found by a match), every expert's rows are then laid out
+// warp after warp, and each warp walks its pairs again to place them in order.
+constexpr int kPermWarps = 32;
+__global__ void __launch_bounds__(kPermWarps * 32) moe_permute_kernel(int P, int E, int k,
+                                                                     const int32_t* __restrict__ topk_id,
+                                                                     int32_t* __restrict__ counts,
+                                                                     int32_t* __restrict__ offsets,
+                                                                     int32_t* __restrict__ pos_of,
+                                                                     int32_t* __restrict__ pair_token) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int cnt[256];
-  __shared__ int off[256];
-  const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cnt[e] = 0;
-  __syncwarp();
-  for (int p0 = 0; p0 < P; p0 += 32) {
+  __shared__ int cnt[kPermWarps][256];  // per warp and expert: a count, then the warp's first row
+  __shared__ int base_e[256];           // per expert: its first row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kPermWarps * 256; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  __syncthreads();
+  const int chunk = (P + kPermWarps - 1) / kPermWarps;
+  const int p_lo = min(P, warp * chunk), p_hi = min(P, p_lo + chunk);
+  for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
     const int p = p0 + lane;
-    const bool valid = p < P;
-    const int id = valid ? topk_id[p] : -1;
+    int id = p < p_hi ? topk_id[p] : -1;
+    if (id >= E) id = -1;  // cannot come from the router; kept out of the tables
     const unsigned peers = __match_any_sync(0xffffffffu, id);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int base = valid ? cnt[id] : 0;
+    if (id >= 0 && lane == __ffs(peers) - 1) cnt[warp][id] += __popc(peers);
     __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) cnt[id] = base + __popc(peers);
-    __syncwarp();
-    if (valid) pos_of[p] = base + rank;  // rank among the expert's pairs, for now
   }
-  __syncwarp();
-  if (lane == 0) {
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int acc = 0;
-    for (int e = 0; e < E; ++e) { off[e] = acc; acc += cnt[e]; }
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = cnt[w][e];
+      cnt[w][e] = acc;
+      acc += c;
+    }
+    base_e[e] = acc;  // the expert's total, for now
   }
-  __syncwarp();
-  for (int e = lane; e < E; e += 32) { counts[e] = cnt[e]; offsets[e] = off[e]; }
-  for (int p = lane; p < P; p += 32) {
-    const int pos = off[topk_id[p]] + pos_of[p];
-    pos_of[p] = pos;
-    pair_token[pos] = p / k;
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the totals, 32 experts at a time (E is a multiple of 32)
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int v = base_e[e0 + lane];
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      counts[e0 + lane] = v;
+      offsets[e0 + lane] = run + x - v;
+      base_e[e0 + lane] = run + x - v;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+  __syncthreads();
+  for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
+    const int p = p0 + lane;
+    int id = p < p_hi ? topk_id[p] : -1;
+    if (id >= E) id = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, id);
+    const int before = id >= 0 ? cnt[warp][id] : 0;
+    __syncwarp();
+    if (id >= 0) {
+      const int pos = base_e[id] + before + __popc(peers & ((1u << lane) - 1u));
+      pos_of[p] = pos;
+      pair_token[pos] = p / k;
+      if (lane == __ffs(peers) - 1) cnt[warp][id] = before + __popc(peers);
+    }
+    __syncwarp();
   }
 }
 
@@ -320,33 +360,46 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
 
 // ----------------------------------------------------------------------------- combine
 // grid: output rows; block d / 8 threads (two float4 each), d a multiple of 256, <= 8192.
+// The row's k (weight, expert-ordered row) pairs are staged in shared memory first, so the
+// expert outputs' loads of several choices are in flight together.
 __global__ void __launch_bounds__(1024) moe_combine_kernel(ResNormArgs a, const float* __restrict__ out,
                                                            const float* __restrict__ topk_w,
                                                            const int32_t* __restrict__ pos_of, int k) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
+  __shared__ float w_sh[32];
+  __shared__ int pos_sh[32];
   const int o = blockIdx.x;
   const int t = (o / a.group_out) * a.group_in + a.in_off + (o % a.group_out);
-  float4 v[2];
+  if (threadIdx.x < k) {
+    w_sh[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+    pos_sh[threadIdx.x] = pos_of[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
   const int per = blockDim.x * 4;
+  const int n_[2] = {(int)threadIdx.x * 4, per + (int)threadIdx.x * 4};
+  float4 v[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+#pragma unroll 4
+  for (int j = 0; j < k; ++j) {  // choices in order: a fixed summation order
+    const float w = w_sh[j];
+    const float* row = out + (size_t)pos_sh[j] * a.d;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (n_[i] >= a.d) continue;
+      const float4 e = __ldcg(reinterpret_cast<const float4*>(row + n_[i]));
+      v[i].x += w * e.x; v[i].y += w * e.y; v[i].z += w * e.z; v[i].w += w * e.w;
+    }
+  }
   float ss = 0.f;
   float* hrow = a.h + (size_t)t * a.d;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const int n = i * per + threadIdx.x * 4;
-    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (n >= a.d) continue;
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {  // choices in order: a fixed summation order
-      const float w = topk_w[(size_t)t * k + j];
-      const float4 e = *reinterpret_cast<const float4*>(out + (size_t)pos_of[(size_t)t * k + j] * a.d + n);
-      y.x += w * e.x; y.y += w * e.y; y.z += w * e.z; y.w += w * e.w;
-    }
-    const float4 hv = *reinterpret_cast<const float4*>(hrow + n);
+    if (n_[i] >= a.d) continue;
+    const float4 hv = *reinterpret_cast<const float4*>(hrow + n_[i]);
+    float4& y = v[i];
     y.x += hv.x; y.y += hv.y; y.z += hv.z; y.w += hv.w;
-    *reinterpret_cast<float4*>(hrow + n) = y;
-    v[i] = y;
+    *reinterpret_cast<float4*>(hrow + n_[i]) = y;
     ss += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
   }
   ss = warp_sum(ss);
@@ -395,18 +448,18 @@ size_t moe_buf_elems(int R, int k, int E, int d, int Fe, size_t* sz) {
   return t;
 }
 
-int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, cudaStream_t st) {
+int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, int* status, cudaStream_t st) {
   if (E % 32 || E > 256 || k < 1 || k > 32 || k > E) return DF_ERR_SHAPE;
   DF_TRACE("moe_route", st);
-  launch_k(moe_route_kernel, dim3((R + 7) / 8), dim3(256), 0, st, pv, R, E, k, m.topk_id, m.topk_w);
+  launch_k(moe_route_kernel, dim3((R + 7) / 8), dim3(256), 0, st, pv, R, E, k, m.topk_id, m.topk_w, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
 int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, MoeBufs& m, cudaStream_t st) {
   DF_TRACE("moe_dispatch", st);
   const int P = R * k;
-  launch_k(moe_permute_kernel, dim3(1), dim3(32), 0, st, P, E, k, m.topk_id, m.counts, m.offsets, m.pos_of,
-           m.pair_token);
+  launch_k(moe_permute_kernel, dim3(1), dim3(kPermWarps * 32), 0, st, P, E, k, m.topk_id, m.counts, m.offsets,
+           m.pos_of, m.pair_token);
   launch_k(moe_gather_kernel, dim3(P), dim3(128), 0, st, x, d, m.pair_token, m.xp);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

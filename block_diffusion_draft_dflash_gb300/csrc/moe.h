@@ -24,8 +24,8 @@ struct MoeBufs {
 // Bytes of MoeBufs for R rows (each 256-byte aligned by the caller's carver).
 size_t moe_buf_elems(int R, int k, int E, int d, int Fe, size_t* sizes /* [9] */);
 
-// router logits (partial tiles of x . W_router^T) -> topk_id, topk_w
-int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, cudaStream_t st);
+// router logits (partial tiles of x . W_router^T) -> topk_id, topk_w; NaN logits -> DF_ERR_NAN
+int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, int* status, cudaStream_t st);
 // topk_id -> counts, offsets, pos_of, pair_token; then xp = x[pair_token]
 int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, MoeBufs& m, cudaStream_t st);
 // grouped expert products: act = SwiGLU(xp . W_gate_up[e]^T), out = act . W_down[e]^T

@@ -273,6 +273,15 @@ int dflash_target_tree_forward(const df_model_cfg* tcfg, const df_model_weights*
                                const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat,
                                void* ws, size_t ws_bytes, df_stream stream);
 
+/* dflash_target_expert_counts -- routing statistics of the last mixture-of-experts
+ * dflash_target_tree_forward run on this workspace (same tcfg, b, n_tree): per layer, the
+ * rows routed to each expert (each row goes to top_k distinct experts, so a layer's counts
+ * sum to b * n_tree * top_k).  Stream-ordered device-to-device copy.
+ *   counts [n_layers][n_experts] int32 out (device)
+ * Errors: DF_ERR_SHAPE for a dense target, DF_ERR_WORKSPACE for a smaller workspace.  */
+int dflash_target_expert_counts(const df_model_cfg* tcfg, int b, int n_tree, const void* ws,
+                                size_t ws_bytes, int32_t* counts, df_stream stream);
+
 /* ------------------------------------------------------------------------------------
  * accept_and_compact -- greedy acceptance and KV-cache compaction (DDTree).
  *

@@ -60,9 +60,11 @@ def _gpu_forward(tw, t, kc, vc):
     feat = torch.zeros(1, T, shape.d_model, dtype=torch.bfloat16, device="cuda")
     ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, 1, T))
     _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k_t, v_t, clen, choice, feat, ws)
+    counts = torch.full((shape.n_layers, shape.n_experts), -1, dtype=torch.int32, device="cuda")
+    _lib.target_expert_counts(tm.cfg, 1, T, ws, counts)
     torch.cuda.synchronize()
     assert ws.status() == 0
-    return choice[0].cpu().numpy(), to_np(feat[0])
+    return choice[0].cpu().numpy(), to_np(feat[0]), counts.cpu().numpy()
 
 
 def _router_margin(tw, t, kc, vc):
@@ -81,13 +83,17 @@ def _router_margin(tw, t, kc, vc):
 
 
 def _check(tw, t, kc, vc, rows):
-    choice, feat = _gpu_forward(tw, t, kc, vc)
+    choice, feat, counts = _gpu_forward(tw, t, kc, vc)
+    # every row goes to top_k distinct experts
+    assert counts.min() >= 0 and np.all(counts.sum(axis=1) == len(t["tok"]) * tw.shape.top_k)
+    assert counts.max() <= len(t["tok"])
     och, ofeat, ologits = step.target_tree_forward(tw, t["tok"], t["parent"], t["depth"], _oracle_cache(kc, vc), N_CTX)
     rel_close(feat[rows], ofeat[rows])
     top2 = np.sort(ologits, axis=-1)[:, -2:]
     sure = rows & ((top2[:, 1] - top2[:, 0]) > 0.02 * np.abs(ologits).max())
     assert sure.mean() > 0.3
     np.testing.assert_array_equal(choice[sure], och[sure])
+    return counts
 
 
 @pytest.mark.parametrize("E,k,B", [(32, 4, 64), (32, 8, 300), (64, 2, 40), (128, 8, 256)])
@@ -108,4 +114,5 @@ def test_moe_all_tokens_to_the_lowest_experts(k, B):
     kc, vc = _cache(tw.shape, B)
     ids, w, _ = model.moe_route(tw.layers[0], tw.shape, np.ones((1, tw.shape.d_model)))
     assert ids[0].tolist() == list(range(k)) and np.all(w == 1.0 / k)
-    _check(tw, t, kc, vc, np.ones(B + 1, bool))
+    counts = _check(tw, t, kc, vc, np.ones(B + 1, bool))
+    np.testing.assert_array_equal(counts[0], [B + 1] * k + [0] * (32 - k))
