@@ -68,6 +68,9 @@ def parse():
                     help="run one small isolated case of a kernel a few times (for ncu captures), no JSON")
     ap.add_argument("--case-n", type=int, default=24576, help="gemm case: weight rows (output features)")
     ap.add_argument("--case-k", type=int, default=4096, help="gemm case: reduction length")
+    ap.add_argument("--case-router", default="random", choices=["random", "zero", "few"],
+                    help="moe case: random router weights; all zero (every row to experts 0..k-1); or only "
+                         "12 experts with (large) router rows, so that rows crowd onto a few experts")
     return ap.parse_args()
 
 
@@ -1144,6 +1147,11 @@ def kernel_case(a):
         import dataclasses
         TS = dataclasses.replace(synth.QWEN3_30B_A3B_TARGET, n_layers=2, feat_layers=(1, 2))
         tm = engine.DeviceModel.random(TS, 5, "target", dev)
+        if a.case_router != "random":
+            for i, L in enumerate(tm.layers):
+                L["w_router"].zero_()
+                if a.case_router == "few":
+                    L["w_router"][:12] = synth.device_normal((12, TS.d_model), 0.2, 5, f"case.router{i}", dev)
         b, T, N = a.batch, a.budget + 1, a.ctx
         cap = (N + T + 127) // 128 * 128
         k = synth.device_normal((2, b, TS.n_kv_heads, cap, 128), 1.0, 5, "case.k", dev)
@@ -1156,6 +1164,8 @@ def kernel_case(a):
         ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T), dev)
         for _ in range(4):
             _lib.target_tree_forward(tm.cfg, tm.weights, tok, tr["depth"], tr["anc"], k, v, clen, choice, None, ws)
+        print("per call, eager traced (ms):", _traced(lambda: _lib.target_tree_forward(
+            tm.cfg, tm.weights, tok, tr["depth"], tr["anc"], k, v, clen, choice, None, ws), 3))
         counts = torch.zeros(2, TS.n_experts, dtype=torch.int32, device=dev)
         _lib.target_expert_counts(tm.cfg, b, T, ws, counts)
         torch.cuda.synchronize()

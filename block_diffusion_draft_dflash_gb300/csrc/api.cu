@@ -154,7 +154,7 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
     MoeBufs m = B.moe;
     m.counts += (size_t)L.layer * c.n_experts;  // each layer's expert counts are kept
     DF_TRY(launch_moe_route(pv, R, c.n_experts, c.top_k, m, L.status, st));
-    DF_TRY(launch_moe_dispatch(B.x, R, d, c.n_experts, c.top_k, m, st));
+    DF_TRY(launch_moe_dispatch(B.x, R, d, c.n_experts, c.top_k, c.d_expert, m, st));
     DF_TRY(launch_moe_experts(L.w->w_experts_gate_up, L.w->w_experts_down, R, d, c.n_experts, c.top_k, c.d_expert,
                               m, L.status, st));
     rn = L.out;
@@ -196,7 +196,7 @@ size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs*
   w.B.part = cv.take<float>(layer_partial_bytes(c, (int)R, (int)R) / 4 + 1);
   w.amax = cv.take<unsigned long long>(R);
   if (c->n_experts > 0) {
-    size_t sz[9];
+    size_t sz[kMoeBufCount];
     moe_buf_elems((int)R, c->top_k, c->n_experts, d, c->d_expert, sz);
     sz[2] *= c->n_layers;  // expert counts of every layer
     MoeBufs& m = w.B.moe;
@@ -209,6 +209,8 @@ size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs*
     m.xp = cv.take<df_bf16>(sz[6] / 2);
     m.act = cv.take<df_bf16>(sz[7] / 2);
     m.out = cv.take<float>(sz[8] / 4);
+    m.chunks = cv.take<int4>(sz[9] / 16);
+    m.n_chunks = cv.take<int32_t>(sz[10] / 4);
   }
   w.B.rope = cv.take<float2>(R * 64);
   // split-KV partials sized for the largest split this call could choose (cache up to 2^20 keys)

@@ -10,12 +10,15 @@
 //   moe_permute_kernel  one CTA: stable counting sort of the (token, choice) pairs by
 //                       expert (ties by token, then choice), expert offsets and counts
 //   moe_gather_kernel   normed rows copied into expert order
-//   moe_gemm_kernel     grouped weight-streaming GEMM on tcgen05 over the stacked expert
-//                       weights: persistent CTAs take work items (token tile of 64 rows,
-//                       expert, 128 output rows) round robin, token tiles outermost, so the
-//                       empty items (token tiles past an expert's count, read on the device)
-//                       are spread evenly and skipped; gate/up items load 64 gate rows and
-//                       the matching 64 up rows, and the epilogue writes silu(g) * u
+//   moe_gemm_kernel     grouped GEMM on tcgen05 over the stacked expert weights: the rows
+//                       of each expert in chunks of at most 256 (the chunk list is built by
+//                       the dispatch on the device), one work item per (chunk, 128 output
+//                       features), persistent CTAs taking items round robin; a k-step loads
+//                       the item's 128 x 64 weight tile once and the chunk's rows in 64-row
+//                       boxes, and one MMA of N = the chunk's rows (rounded up to 16) uses
+//                       them, so an expert's weights are streamed once per chunk however
+//                       many rows it holds; gate/up items load 64 gate rows and the matching
+//                       64 up rows, and the epilogue writes silu(g) * u
 //   moe_combine_kernel  h += sum_j w_j expert_out_j, then RMSNorm (as res_norm)
 // No host synchronisation: the routing stays on the device, so a step is graph-capturable.
 #include "common.cuh"
@@ -27,11 +30,15 @@
 namespace df {
 
 constexpr int kMoeThreads = 192;
-constexpr int kMoeBN = 64;      // token rows per work item (MMA N)
 constexpr int kMoeBK = 64;
-constexpr int kMoeStages = 8;
-constexpr uint32_t kMoeWBytes = 128 * kMoeBK * 2, kMoeXBytes = kMoeBN * kMoeBK * 2;
-constexpr uint32_t kMoeStageBytes = kMoeWBytes + kMoeXBytes;
+constexpr int kMoeChunk = 256;  // rows of one expert per work item at most (MMA N <= 256)
+constexpr uint32_t kMoeWBytes = 128 * kMoeBK * 2;  // 128 weight rows x 64
+constexpr uint32_t kMoeXBox = 64 * kMoeBK * 2;     // 64 token rows x 64
+// The k-steps' operands sit in a ring of bytes: a k-step takes its weight tile plus as many
+// 64-row boxes as its chunk needs (24 to 48 KB), so small chunks keep more k-steps in flight.
+constexpr uint32_t kMoeRing = 192 * 1024;
+constexpr int kMoeSlots = 8;    // k-steps in flight at most (kMoeRing / the smallest k-step)
+constexpr int kMoeXPitch = 33;  // gate/up exchange buffer: [64 features][32 tokens], padded
 enum { kMoeGateUp = 0, kMoeDown = 1 };
 
 // ------------------------------------------------------------------------------ routing
@@ -95,23 +102,34 @@ __global__ void __launch_bounds__(256) moe_route_kernel(PartialView pv, int R, i
 // One CTA of 1024 threads: a stable counting sort of the pairs p = t k + j by expert.
 // Warp w takes the contiguous pairs [w c, (w + 1) c), c = ceil(P / 32): it counts them per
 // expert (lanes with equal experts found by a match), every expert's rows are then laid out
-// warp after warp, and each warp walks its pairs again to place them in order.
+// warp after warp, and each warp walks its pairs again to place them in order.  Also the
+// grouped GEMM's work list: each expert's rows split evenly into chunks of at most m rows,
+// m in {256, 192, 128, 64} chosen to minimise the busiest CTA's bytes per k-step summed
+// over its items (ceil(items / ctas) x (the weight tile + the widest chunk's row boxes),
+// items = chunks x n_wt feature tiles): few experts holding many rows get smaller chunks,
+// so that the items spread over all CTAs.
 constexpr int kPermWarps = 32;
+__constant__ int kChunkCand[4] = {256, 192, 128, 64};
 __global__ void __launch_bounds__(kPermWarps * 32) moe_permute_kernel(int P, int E, int k,
                                                                      const int32_t* __restrict__ topk_id,
                                                                      int32_t* __restrict__ counts,
                                                                      int32_t* __restrict__ offsets,
                                                                      int32_t* __restrict__ pos_of,
-                                                                     int32_t* __restrict__ pair_token) {
+                                                                     int32_t* __restrict__ pair_token,
+                                                                     int4* __restrict__ chunks,
+                                                                     int32_t* __restrict__ n_chunks, int n_wt,
+                                                                     int ctas) {
   pdl_wait();
   pdl_trigger();
   __shared__ int cnt[kPermWarps][256];  // per warp and expert: a count, then the warp's first row
-  __shared__ int base_e[256];           // per expert: its first row
+  __shared__ int tot[256], first[256], nch[256], ch0[256];  // per expert
+  __shared__ int cand_chunks[4], cand_boxes[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kPermWarps * 256; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  if (threadIdx.x < 4) { cand_chunks[threadIdx.x] = 0; cand_boxes[threadIdx.x] = 0; }
   __syncthreads();
-  const int chunk = (P + kPermWarps - 1) / kPermWarps;
-  const int p_lo = min(P, warp * chunk), p_hi = min(P, p_lo + chunk);
+  const int per_warp = (P + kPermWarps - 1) / kPermWarps;
+  const int p_lo = min(P, warp * per_warp), p_hi = min(P, p_lo + per_warp);
   for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
     const int p = p0 + lane;
     int id = p < p_hi ? topk_id[p] : -1;
@@ -128,26 +146,55 @@ __global__ void __launch_bounds__(kPermWarps * 32) moe_permute_kernel(int P, int
       cnt[w][e] = acc;
       acc += c;
     }
-    base_e[e] = acc;  // the expert's total, for now
-  }
-  __syncthreads();
-  if (warp == 0) {  // exclusive scan of the totals, 32 experts at a time (E is a multiple of 32)
-    int run = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int v = base_e[e0 + lane];
-      int x = v;
+    tot[e] = acc;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+    for (int c = 0; c < 4; ++c) {
+      const int n = (acc + kChunkCand[c] - 1) / kChunkCand[c];
+      if (n) {
+        atomicAdd(&cand_chunks[c], n);
+        atomicMax(&cand_boxes[c], ((acc + n - 1) / n + 63) / 64);
       }
-      counts[e0 + lane] = v;
-      offsets[e0 + lane] = run + x - v;
-      base_e[e0 + lane] = run + x - v;
-      run += __shfl_sync(0xffffffffu, x, 31);
     }
   }
   __syncthreads();
+  int m = kChunkCand[0];
+  long long best = -1;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const long long cost = ((long long)cand_chunks[c] * n_wt + ctas - 1) / ctas * (2 + cand_boxes[c]);
+    if (best < 0 || cost < best) { best = cost; m = kChunkCand[c]; }
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) nch[e] = (tot[e] + m - 1) / m;
+  __syncthreads();
+  if (warp == 0) {  // exclusive scans of the rows and the chunks, 32 experts at a time (E % 32 == 0)
+    int run = 0, run_c = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int v = tot[e0 + lane], vc = nch[e0 + lane];
+      int x = v, xc = vc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o), yc = __shfl_up_sync(0xffffffffu, xc, o);
+        if (lane >= o) { x += y; xc += yc; }
+      }
+      counts[e0 + lane] = v;
+      offsets[e0 + lane] = run + x - v;
+      first[e0 + lane] = run + x - v;
+      ch0[e0 + lane] = run_c + xc - vc;
+      run += __shfl_sync(0xffffffffu, x, 31);
+      run_c += __shfl_sync(0xffffffffu, xc, 31);
+    }
+    if (lane == 0) *n_chunks = run_c;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = tot[e], n = nch[e];
+    int row = first[e];
+    for (int i = 0; i < n; ++i) {
+      const int rows = c / n + (i < c % n ? 1 : 0);
+      chunks[ch0[e] + i] = make_int4(e, row, rows, 0);
+      row += rows;
+    }
+  }
   for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
     const int p = p0 + lane;
     int id = p < p_hi ? topk_id[p] : -1;
@@ -156,7 +203,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) moe_permute_kernel(int P, int
     const int before = id >= 0 ? cnt[warp][id] : 0;
     __syncwarp();
     if (id >= 0) {
-      const int pos = base_e[id] + before + __popc(peers & ((1u << lane) - 1u));
+      const int pos = first[id] + before + __popc(peers & ((1u << lane) - 1u));
       pos_of[p] = pos;
       pair_token[pos] = p / k;
       if (lane == __ffs(peers) - 1) cnt[warp][id] = before + __popc(peers);
@@ -179,21 +226,14 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const df_bf16* __restri
 
 // ------------------------------------------------------------------------- grouped GEMM
 struct MoeGemmParams {
-  int E, n_wt, n_tt, k_iters;   // work items n_tt x E x n_wt
-  const int32_t* counts;
-  const int32_t* offsets;
+  int n_wt, k_iters;        // items: n_chunks x n_wt (feature tiles innermost)
+  const int4* chunks;       // {expert, first expert-ordered row, rows, 0}
+  const int32_t* n_chunks;
   int Fe, d;
-  df_bf16* act;                 // gate/up: [P][Fe]
-  float* out;                   // down: [P][d]
+  df_bf16* act;             // gate/up: [P][Fe]
+  float* out;               // down: [P][d]
   int* status;
 };
-
-DF_DEV void moe_item(const MoeGemmParams& p, int it, int& tt, int& e, int& wt) {
-  tt = it / (p.E * p.n_wt);
-  const int r = it - tt * p.E * p.n_wt;
-  e = r / p.n_wt;
-  wt = r - e * p.n_wt;
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(kMoeThreads, 1)
@@ -201,15 +241,16 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
                     const MoeGemmParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int S = kMoeStages;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * kMoeStageBytes);
+  constexpr int S = kMoeSlots;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMoeRing);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
   uint64_t* tempty = bars + 2 * S + 2;
   uint64_t* mma_drain = bars + 2 * S + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
-  float* xbuf = reinterpret_cast<float*>(bars + 2 * S + 8);  // gate/up epilogue: [64 rows][64 tokens] of up values
+  uint32_t* slot_off = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);  // [S] ring offset of each k-step
+  float* xbuf = reinterpret_cast<float*>(bars + 2 * S + 6 + S / 2);   // gate/up epilogue: up values
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -220,77 +261,82 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
-  if (warp == 1) { tmem_alloc(tmem_slot, 2 * kMoeBN); tmem_relinquish(); }
+  if (warp == 1) { tmem_alloc(tmem_slot, 2 * kMoeChunk); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();  // counts, offsets and the expert-ordered rows come from the previous kernels
+  pdl_wait();  // the chunk list and the expert-ordered rows come from the previous kernels
   pdl_trigger();
-  const int n_items = p.n_tt * p.E * p.n_wt;
+  const int n_items = *p.n_chunks * p.n_wt;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    long long issued = 0;
+    uint32_t head = 0, used = 0;  // next free byte of the ring; bytes held by k-steps in flight
+    uint32_t held[S];             // bytes each slot holds (a wrapped k-step also holds the skipped tail)
+    long long issued = 0, released = 0;
     bool ok = true;
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      int tt, e, wt;
-      moe_item(p, it, tt, e, wt);
-      if (tt * kMoeBN >= p.counts[e]) continue;
-      const int xrow = p.offsets[e] + tt * kMoeBN;
+      const int4 ch = p.chunks[it / p.n_wt];
+      const int wt = it % p.n_wt, nbox = (ch.z + 63) >> 6;
+      const uint32_t need = kMoeWBytes + nbox * kMoeXBox;
       for (int k = 0; k < p.k_iters; ++k) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 21)) { ok = false; break; }
-        unsigned char* sb = smem + (size_t)stage * kMoeStageBytes;
-        mbar_arrive_expect_tx(&full[stage], kMoeStageBytes);
-        if (MODE == kMoeGateUp) {
-          const int g0 = e * 2 * p.Fe + wt * 64;  // 64 gate rows, then the matching 64 up rows
-          tma_load_2d(sb, &tmW, &full[stage], k * kMoeBK, g0, pol_w);
-          tma_load_2d(sb + kMoeWBytes / 2, &tmW, &full[stage], k * kMoeBK, g0 + p.Fe, pol_w);
-        } else {
-          tma_load_2d(sb, &tmW, &full[stage], k * kMoeBK, e * p.d + wt * 128, pol_w);
+        uint32_t start = head, take = need;
+        if (head + need > kMoeRing) { start = 0; take = kMoeRing - head + need; }
+        // the oldest k-steps give their bytes back until this one fits and a slot is free
+        while (used + take > kMoeRing || issued - released == S) {
+          const int so = (int)(released % S);
+          if (!mbar_wait(&empty[so], (uint32_t)((released / S) & 1), p.status, 21)) { ok = false; break; }
+          used -= held[so];
+          ++released;
         }
-        tma_load_2d(sb + kMoeWBytes, &tmX, &full[stage], k * kMoeBK, xrow, pol_x);
+        if (!ok) break;
+        const int sl = (int)(issued % S);
+        held[sl] = take;
+        slot_off[sl] = start;
+        used += take;
+        head = start + need;
+        unsigned char* sb = smem + start;
+        mbar_arrive_expect_tx(&full[sl], need);
+        if (MODE == kMoeGateUp) {
+          const int g0 = ch.x * 2 * p.Fe + wt * 64;  // 64 gate rows, then the matching 64 up rows
+          tma_load_2d(sb, &tmW, &full[sl], k * kMoeBK, g0, pol_w);
+          tma_load_2d(sb + kMoeWBytes / 2, &tmW, &full[sl], k * kMoeBK, g0 + p.Fe, pol_w);
+        } else {
+          tma_load_2d(sb, &tmW, &full[sl], k * kMoeBK, ch.x * p.d + wt * 128, pol_w);
+        }
+        for (int j = 0; j < nbox; ++j)
+          tma_load_2d(sb + kMoeWBytes + j * kMoeXBox, &tmX, &full[sl], k * kMoeBK, ch.y + 64 * j, pol_x);
         ++issued;
-        if (++stage == S) { stage = 0; phase ^= 1; }
       }
     }
     // every load issued has landed before the CTA may exit (bounded waits)
-    const long long n = issued < S ? issued : S;
-    int st = stage;
-    uint32_t ph = phase;
-    for (long long i = 0; i < n; ++i) {
-      if (--st < 0) { st = S - 1; ph ^= 1; }
-      mbar_wait(&full[st], ph, nullptr, 0);
-    }
+    for (long long g = issued - S > released ? issued - S : released; g < issued; ++g)
+      mbar_wait(&full[g % S], (uint32_t)((g / S) & 1), nullptr, 0);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(128, kMoeBN);
-    int stage = 0;
-    uint32_t phase = 0;
+    long long g = 0;  // k-steps consumed
     int si = 0;
     bool ok = true, issued_any = false;
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      int tt, e, wt;
-      moe_item(p, it, tt, e, wt);
-      if (tt * kMoeBN >= p.counts[e]) continue;
+      const int4 ch = p.chunks[it / p.n_wt];
+      const uint32_t idesc = idesc_bf16_f32(128, (ch.z + 15) & ~15);
       const int acc = si & 1, use = si >> 1;
       if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 22)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * kMoeBN;
-      for (int k = 0; k < p.k_iters; ++k) {
-        if (!mbar_wait(&full[stage], phase, p.status, 23)) { ok = false; break; }
+      const uint32_t d_tmem = tmem_base + acc * kMoeChunk;
+      for (int k = 0; k < p.k_iters; ++k, ++g) {
+        const int sl = (int)(g % S);
+        if (!mbar_wait(&full[sl], (uint32_t)((g / S) & 1), p.status, 23)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + (size_t)stage * kMoeStageBytes);
+        const uint32_t sa = smem_u32(smem + slot_off[sl]);
         const uint64_t adesc = sdesc_kmajor_sw128(sa), bdesc = sdesc_kmajor_sw128(sa + kMoeWBytes);
 #pragma unroll
         for (int kk = 0; kk < kMoeBK / 16; ++kk)
           mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
         issued_any = true;
-        mma_commit(&empty[stage]);
-        if (++stage == S) { stage = 0; phase ^= 1; }
+        mma_commit(&empty[sl]);
       }
       if (!ok) break;
       mma_commit(&tfull[acc]);
@@ -303,14 +349,12 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;      // TMEM lane quarter: rows 32 q .. 32 q + 31
+    const int q = warp & 3;      // TMEM lane quarter: weight rows 32 q .. 32 q + 31
     const int r = q * 32 + lane;
     int si = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      int tt, e, wt;
-      moe_item(p, it, tt, e, wt);
-      const int cnt = p.counts[e];
-      if (tt * kMoeBN >= cnt) continue;
+      const int4 ch = p.chunks[it / p.n_wt];
+      const int wt = it % p.n_wt;
       const int acc = si & 1, use = si >> 1;
       // the four epilogue warps leave together (they meet at named barriers below)
       const bool ok = mbar_wait(&tfull[acc], use & 1, p.status, 24);
@@ -319,33 +363,40 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
                    " selp.u32 %0, 1, 0, b;\n}" : "=r"(all_ok) : "r"((uint32_t)ok) : "memory");
       if (!all_ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kMoeBN;
-      float v[kMoeBN];
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kMoeChunk;
+      for (int c0 = 0; c0 < ch.z; c0 += 32) {  // 32 token columns at a time
+        float v[32];
+        tmem_ld16(taddr + c0, v);
+        tmem_ld16(taddr + c0 + 16, v + 16);
+        tmem_ld_wait();
+        const int nc = min(32, ch.z - c0);
+        const size_t row0 = (size_t)ch.y + c0;
+        if (MODE == kMoeGateUp) {
+          // weight rows 0..63: gate of features 64 wt + r; rows 64..127: the matching up
+          asm volatile("bar.sync 1, 128;" ::: "memory");  // the previous columns' readers are done
+          if (r >= 64)
 #pragma unroll
-      for (int c = 0; c < kMoeBN; c += 16) tmem_ld16(taddr + c, v + c);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);  // the accumulator may be reused while the values are written out
-      const int n_ok = min(kMoeBN, cnt - tt * kMoeBN);
-      const size_t row0 = (size_t)p.offsets[e] + (size_t)tt * kMoeBN;
-      if (MODE == kMoeGateUp) {
-        // rows 0..63: gate of features 64 wt + r; rows 64..127: the matching up
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the previous item's readers are done
-        if (r >= 64)
+            for (int c = 0; c < 32; ++c) xbuf[(r - 64) * kMoeXPitch + c] = v[c];
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (r < 64) {
+            df_bf16* dst = p.act + row0 * p.Fe + wt * 64 + r;
 #pragma unroll
-          for (int c = 0; c < kMoeBN; ++c) xbuf[(r - 64) * kMoeBN + c] = v[c];
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (r < 64) {
-          df_bf16* dst = p.act + row0 * p.Fe + wt * 64 + r;
-          for (int c = 0; c < n_ok; ++c) {
-            const float g = v[c], u = xbuf[r * kMoeBN + c];
-            dst[(size_t)c * p.Fe] = f_to_bf16(g / (1.f + __expf(-g)) * u);
+            for (int c = 0; c < 32; ++c) {
+              if (c < nc) {
+                const float g = v[c], u = xbuf[r * kMoeXPitch + c];
+                dst[(size_t)c * p.Fe] = f_to_bf16(g / (1.f + __expf(-g)) * u);
+              }
+            }
           }
+        } else {
+          float* dst = p.out + row0 * p.d + wt * 128 + r;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < nc) dst[(size_t)c * p.d] = v[c];
         }
-      } else {
-        float* dst = p.out + row0 * p.d + wt * 128 + r;
-        for (int c = 0; c < n_ok; ++c) dst[(size_t)c * p.d] = v[c];
       }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);  // all of this accumulator's columns are read
       ++si;
     }
   }
@@ -354,7 +405,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, 2 * kMoeBN);
+    tmem_dealloc(tmem_base, 2 * kMoeChunk);
   }
 }
 
@@ -432,6 +483,10 @@ __global__ void __launch_bounds__(1024) moe_combine_kernel(ResNormArgs a, const 
 }
 
 // ----------------------------------------------------------------------------- host
+// chunks of at least 64 rows (the smallest chunk size the dispatch chooses): sum over the
+// experts of ceil(c_e / 64) <= E + R k / 64
+int moe_max_chunks(int R, int k, int E) { return E + R * k / 64 + 1; }
+
 size_t moe_buf_elems(int R, int k, int E, int d, int Fe, size_t* sz) {
   const size_t P = (size_t)R * k;
   sz[0] = P * 4;            // topk_id
@@ -443,8 +498,10 @@ size_t moe_buf_elems(int R, int k, int E, int d, int Fe, size_t* sz) {
   sz[6] = P * d * 2;        // xp
   sz[7] = P * Fe * 2;       // act
   sz[8] = P * d * 4;        // out
+  sz[9] = (size_t)moe_max_chunks(R, k, E) * 16;  // chunks
+  sz[10] = 16;              // n_chunks
   size_t t = 0;
-  for (int i = 0; i < 9; ++i) t += sz[i];
+  for (int i = 0; i < kMoeBufCount; ++i) t += sz[i];
   return t;
 }
 
@@ -455,11 +512,11 @@ int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, int
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
-int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, MoeBufs& m, cudaStream_t st) {
+int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, int Fe, MoeBufs& m, cudaStream_t st) {
   DF_TRACE("moe_dispatch", st);
   const int P = R * k;
   launch_k(moe_permute_kernel, dim3(1), dim3(kPermWarps * 32), 0, st, P, E, k, m.topk_id, m.counts, m.offsets,
-           m.pos_of, m.pair_token);
+           m.pos_of, m.pair_token, m.chunks, m.n_chunks, Fe / 64, num_sms());
   launch_k(moe_gather_kernel, dim3(P), dim3(128), 0, st, x, d, m.pair_token, m.xp);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
@@ -468,22 +525,20 @@ int launch_moe_experts(const df_bf16* w_gate_up, const df_bf16* w_down, int R, i
                        MoeBufs& m, int* status, cudaStream_t st) {
   if (Fe % 64 || d % 128) return DF_ERR_SHAPE;
   const int P = R * k;
-  const size_t smem = 1024 + (size_t)kMoeStages * kMoeStageBytes + (2 * kMoeStages + 8) * 8 + 64 * kMoeBN * 4;
+  const size_t smem = 1024 + kMoeRing + (2 * kMoeSlots + 6 + kMoeSlots / 2) * 8 + 64 * kMoeXPitch * 4;
   if (ensure_dynamic_smem(moe_gemm_kernel<kMoeGateUp>, smem) != cudaSuccess ||
       ensure_dynamic_smem(moe_gemm_kernel<kMoeDown>, smem) != cudaSuccess)
     return DF_ERR_CUDA;
   CUtensorMap tw1, tx1, tw2, tx2;
-  // gate/up: stacked [E * 2 Fe][d] weights in 64-row boxes; token rows xp [P][d]
-  if (make_tmap_2d(&tw1, w_gate_up, (long long)E * 2 * Fe, d, d, 64) || make_tmap_2d(&tx1, m.xp, P, d, d, kMoeBN))
+  // gate/up: stacked [E * 2 Fe][d] weights in 64-row boxes; token rows xp [P][d] in 64-row boxes
+  if (make_tmap_2d(&tw1, w_gate_up, (long long)E * 2 * Fe, d, d, 64) || make_tmap_2d(&tx1, m.xp, P, d, d, 64))
     return DF_ERR_CUDA;
   // down: stacked [E * d][Fe] weights in 128-row boxes; token rows act [P][Fe]
-  if (make_tmap_2d(&tw2, w_down, (long long)E * d, Fe, Fe, 128) || make_tmap_2d(&tx2, m.act, P, Fe, Fe, kMoeBN))
+  if (make_tmap_2d(&tw2, w_down, (long long)E * d, Fe, Fe, 128) || make_tmap_2d(&tx2, m.act, P, Fe, Fe, 64))
     return DF_ERR_CUDA;
   MoeGemmParams p{};
-  p.E = E;
-  p.n_tt = (R + kMoeBN - 1) / kMoeBN;  // an expert gets each token at most once
-  p.counts = m.counts;
-  p.offsets = m.offsets;
+  p.chunks = m.chunks;
+  p.n_chunks = m.n_chunks;
   p.Fe = Fe;
   p.d = d;
   p.act = m.act;
