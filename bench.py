@@ -57,6 +57,9 @@ def parse():
                     help="probability per draft depth that the drafter's log-probs lean on the target's greedy "
                          "continuation (0 = no planting)")
     ap.add_argument("--plant-bias", type=float, default=16.0, help="logit bias of a planted token")
+    ap.add_argument("--plant-miss-bias", type=float, default=0.0,
+                    help="near misses at the depths not drawn: the plant bias goes to a decoy and this bias to the "
+                         "reference token, the drafter's second choice (0: such depths are left alone)")
     ap.add_argument("--target", default="qwen3-8b", choices=["qwen3-8b", "qwen3-coder-30b-a3b"],
                     help="step mode: the dense Qwen3-8B-shaped target, or the mixture-of-experts "
                          "Qwen3-Coder-30B-A3B-shaped one (48 layers, 128 experts, 8 per token)")
@@ -104,7 +107,9 @@ def workload_name(a):
     moe = f", {TS.n_experts} experts x {TS.d_expert} (top {TS.top_k})" if TS.n_experts else ""
     draft = f"B={a.budget}" if a.draft_mode == "tree" else "DFlash chain of 15 (no tree)"
     return (f"DFlash+DDTree spec step, {target_label(a)}-shaped target ({TS.n_layers}L{moe}) + {DS.n_layers}L "
-            f"drafter, block 16, {draft}, ctx {a.ctx}, b={a.batch}, acceptance planted at {a.accept_rate}")
+            f"drafter, block 16, {draft}, ctx {a.ctx}, b={a.batch}, acceptance planted at {a.accept_rate}"
+            + (f" (near misses elsewhere: the target's token second at bias {a.plant_miss_bias:g})"
+               if getattr(a, "plant_miss_bias", 0) else ""))
 
 
 def config(a, impl="gb300"):
@@ -554,7 +559,7 @@ def run_gpu(a, rank, world, local_rank):
         # drafter on (the recorded run and the measured run below are the same steps)
         ref = torch.full((b, cap, dec.D), -1, dtype=torch.int32, device=dev)
         dec.plant = lambda d: _lib.plant_logprobs(d.logprobs, ref, d.cache_len, a.accept_rate, a.plant_bias,
-                                                  seed)
+                                                  seed, miss_bias=a.plant_miss_bias)
         dec.prefill(prompt)
         fixes, unresolved = lookahead_table(dec, n_steps + 2, ref, dev)
     # prompt pass and the drafter's first context build, timed once each (untimed region)
@@ -724,7 +729,7 @@ def run_gpu(a, rank, world, local_rank):
     t_star_ms, step_bytes = step_roofline_ms(b, T - 1, N, hbm, tc_sust, TS, DS, active)
     clk = clocks.summary(local_rank)
     launches = sum(v["launches_per_step"] * KERNELS_PER_CALL.get(k, 1) for k, v in kern.items())
-    acc = {"rate": a.accept_rate, "bias": a.plant_bias, "tokens_per_step": round(tau, 3),
+    acc = {"rate": a.accept_rate, "bias": a.plant_bias, "miss_bias": a.plant_miss_bias, "tokens_per_step": round(tau, 3),
            "tokens_per_step_e2e": round(emitted / (a.steps * b), 3),
            "root_choice_vs_reference_disagreements": disagree, "steps_without_reference": unplanted,
            "reference_entries_adopted_from_verification": fixes, "recording_steps_unresolved": unresolved,

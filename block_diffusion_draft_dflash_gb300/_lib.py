@@ -79,7 +79,7 @@ _SIGS = {
                                            C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_workspace_configure": (C.c_int, [C.c_void_p, C.c_ulonglong, C.c_int, C.c_void_p]),
     "dflash_plant_logprobs": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p,
-                                        C.c_float, C.c_float, C.c_ulonglong, C.c_void_p]),
+                                        C.c_float, C.c_float, C.c_float, C.c_ulonglong, C.c_void_p]),
     "dflash_draft_block_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
     "dflash_draft_block": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_int] + [C.c_void_p] * 4 +
                            [C.c_int] + [C.c_void_p] * 3 + [C.c_size_t, C.c_void_p]),
@@ -313,7 +313,7 @@ def linear_logsoftmax(X, W, out, ws: Workspace = None):
     return ws
 
 
-def plant_logprobs(logprobs, ref, pos, rate, bias, seed):
+def plant_logprobs(logprobs, ref, pos, rate, bias, seed, miss_bias=0.0):
     """Harness: plant agreement with reference tokens (see dflash_plant_logprobs).
     ref [b][n_pos][D] int32: tokens expected at depths 1..D of a block starting at position p."""
     _dev(logprobs, torch.float32, "logprobs")
@@ -322,7 +322,8 @@ def plant_logprobs(logprobs, ref, pos, rate, bias, seed):
     b, D, V = logprobs.shape
     assert ref.shape[0] == b and ref.shape[2] == D
     _check("dflash_plant_logprobs", load().dflash_plant_logprobs(
-        _p(logprobs), b, D, V, _p(ref), ref.shape[1], _p(pos), float(rate), float(bias), int(seed), _stream()))
+        _p(logprobs), b, D, V, _p(ref), ref.shape[1], _p(pos), float(rate), float(bias), float(miss_bias), int(seed),
+        _stream()))
 
 
 def trace_enable(on=True):

@@ -354,16 +354,20 @@ int dflash_linear_logsoftmax(const df_bf16* X, const df_bf16* W, int M, int N, i
  * log-softmax of its logits with `bias` added at the reference token r = ref[s][pos[s]][d-1]:
  * lp'_i = lp_i - c (i != r), lp'_r = lp_r + bias - c, c = log(1 + exp(lp_r)(e^bias - 1)).
  * The draw is a counter-based hash (splitmix64) of (seed, s, pos[s], d): no host input per
- * step, so the call can sit in a captured graph.  Rows with no reference (pos[s] outside
- * [0, n_pos) or a negative entry) are left as they are.
+ * step, so the call can sit in a captured graph.  With miss_bias > 0 a row not drawn is a
+ * near miss: `bias` goes to a decoy token d != r (picked by a second splitmix64 of the draw:
+ * d = (r + 1 + splitmix64(h) mod (V - 1)) mod V) and `miss_bias` to r, both renormalised as
+ * above: the decoy and r lead the row, r usually second (a drafter whose miss still holds
+ * the target's token); miss_bias = 0 leaves such rows as they are.  Rows with no reference (pos[s] outside [0, n_pos) or a negative
+ * entry) are left as they are.
  *   logprobs [b][D][V] fp32 in/out
  *   ref      [b][n_pos][D] int32: the tokens expected at depths 1..D of a block whose row 0
  *            (the bonus token) is at position p
  *   pos      [b] int32: position of the block's row 0 (the target's cache length)
  * ------------------------------------------------------------------------------------ */
 int dflash_plant_logprobs(float* logprobs, int b, int D, int V, const int32_t* ref, int n_pos,
-                          const int32_t* pos, float rate, float bias, unsigned long long seed,
-                          df_stream stream);
+                          const int32_t* pos, float rate, float bias, float miss_bias,
+                          unsigned long long seed, df_stream stream);
 
 /* ------------------------------------------------------------------------------------
  * Status and device queries.

@@ -94,16 +94,19 @@ def _splitmix64(x):
     return x ^ (x >> 31)
 
 
-def test_plant_logprobs_harness():
+@pytest.mark.parametrize("miss_bias", [0.0, 14.5])
+def test_plant_logprobs_harness(miss_bias):
     # the benchmark's acceptance plant: the planted rows are a renormalised bias at the
-    # reference token, drawn per (seed, sequence, position, depth); the others are unchanged
+    # reference token, drawn per (seed, sequence, position, depth); the others are unchanged,
+    # or near misses (the bias on a decoy, the miss bias on the reference)
     b, D, V, n_pos, rate, bias, seed = 3, 15, 5000, 400, 0.6, 16.0, 77
     lp = ddtree.log_softmax(np.random.default_rng(0).normal(0, 1.3, size=(b, D, V)))
     ref = np.random.default_rng(1).integers(0, V, size=(b, n_pos, D)).astype(np.int32)
     pos = np.array([10, 200, 250], dtype=np.int32)
     ref[2, 250, 3:9] = -1                                     # no reference at these depths
     lp_t = torch.from_numpy(lp).cuda()
-    _lib.plant_logprobs(lp_t, torch.from_numpy(ref).cuda(), torch.from_numpy(pos).cuda(), rate, bias, seed)
+    _lib.plant_logprobs(lp_t, torch.from_numpy(ref).cuda(), torch.from_numpy(pos).cuda(), rate, bias, seed,
+                        miss_bias=miss_bias)
     got = lp_t.cpu().numpy().astype(np.float64)
     n_planted = 0
     for s in range(b):
@@ -112,13 +115,23 @@ def test_plant_logprobs_harness():
             r = int(ref[s, pos[s], d - 1])
             planted = r >= 0 and (h >> 11) / 2.0 ** 53 < rate
             row = lp[s, d - 1].astype(np.float64)
-            if not planted:
+            if r < 0 or (not planted and miss_bias == 0.0):
                 np.testing.assert_array_equal(got[s, d - 1], row)
                 continue
-            n_planted += 1
+            n_planted += planted
             x = row.copy()
-            x[r] += bias
+            if planted:
+                x[r] += bias
+            else:
+                decoy = (r + 1 + _splitmix64(h) % (V - 1)) % V
+                assert decoy != r
+                x[decoy] += bias
+                x[r] += miss_bias
             expect = x - np.log(np.sum(np.exp(x)))    # log-softmax of the biased logits
             np.testing.assert_allclose(got[s, d - 1], expect, atol=2e-5)
-            assert int(np.argmax(got[s, d - 1])) == r
+            order = np.argsort(-got[s, d - 1])
+            if planted:
+                assert order[0] == r
+            else:  # the decoy and the reference lead (in either order, by their own logits)
+                assert set(order[:2].tolist()) == {decoy, r}
     assert 10 < n_planted < 3 * D
