@@ -327,10 +327,10 @@ def moe_expert_algorithmic(b, B, TS, active):
 
 # DRAM traffic of the target projection GEMMs, from one ncu capture of a 2-layer Qwen3-8B-width
 # target tree forward (B=256): the four projection launches of one layer read + wrote
-# 54.10 (q/k/v), 35.80 (o), 211.63 (gate/up) and 111.40 (down) MB.  Valid only for the GEMM
+# 53.14 (q/k/v), 35.72 (o), 210.23 (gate/up) and 108.79 (down) MB.  Valid only for the GEMM
 # code it was taken on (its hash below, comments aside); any other build reports traffic null.
-GEMM_TRAFFIC = {"src_sha256_16": "4006d7d03145f230", "bytes_per_layer": 412926720,
-                "capture": "profiles/gemm_attention_ncu_full_qwen3_8b_2layer_B256.md"}
+GEMM_TRAFFIC = {"src_sha256_16": "cbd0ed61cd72ff88", "bytes_per_layer": 407875328,
+                "capture": "profiles/gemm_traffic_ncu_qwen3_8b_2layer_B256.md"}
 GEMM_SOURCES = ("gemm.cu", "common.cuh", "partials.cuh")
 
 
