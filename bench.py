@@ -729,7 +729,12 @@ def run_gpu(a, rank, world, local_rank):
     t_star_ms, step_bytes = step_roofline_ms(b, T - 1, N, hbm, tc_sust, TS, DS, active)
     clk = clocks.summary(local_rank)
     launches = sum(v["launches_per_step"] * KERNELS_PER_CALL.get(k, 1) for k, v in kern.items())
+    hist = {}
+    for _, na in outs:  # tokens emitted per step and sequence in the end-to-end steps
+        for v in (na + 1).tolist():
+            hist[int(v)] = hist.get(int(v), 0) + 1
     acc = {"rate": a.accept_rate, "bias": a.plant_bias, "miss_bias": a.plant_miss_bias, "tokens_per_step": round(tau, 3),
+           "tau_histogram_e2e": {str(k_): hist[k_] for k_ in sorted(hist)},
            "tokens_per_step_e2e": round(emitted / (a.steps * b), 3),
            "root_choice_vs_reference_disagreements": disagree, "steps_without_reference": unplanted,
            "reference_entries_adopted_from_verification": fixes, "recording_steps_unresolved": unresolved,

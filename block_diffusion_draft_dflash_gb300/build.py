@@ -1,7 +1,8 @@
 """Builds the CUDA library (libdflash.so) in-tree for sm_103a with nvcc.
 
 Translation units are compiled in parallel and linked into one shared library under
-``_build/``.  The build is skipped when the library is newer than every source.
+``_build/`` (``_build_checked/`` with DFLASH_CHECKED=1: device-side index checks on).  The
+build is skipped when the library is newer than every source.
 """
 from __future__ import annotations
 
@@ -12,7 +13,10 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
-OUT_DIR = os.path.join(PKG, "_build")
+# DFLASH_CHECKED=1: the checked build (device-side index checks that record DF_ERR_BOUNDS),
+# kept apart from the default library
+CHECKED = os.environ.get("DFLASH_CHECKED", "0") not in ("", "0")
+OUT_DIR = os.path.join(PKG, "_build_checked" if CHECKED else "_build")
 LIB = os.path.join(OUT_DIR, "libdflash.so")
 
 SOURCES = ["api.cu", "gemm.cu", "attention.cu", "layers.cu", "ddtree.cu", "ddtree_static.cu", "accept.cu", "trace.cu",
@@ -50,7 +54,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        checked = ["-DDFLASH_CHECKED=1"] if CHECKED else []
+        cmd = [nvcc, *ARCH, *FLAGS, *checked, *extra_flags, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")

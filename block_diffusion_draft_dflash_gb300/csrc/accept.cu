@@ -15,6 +15,7 @@
 // gather_feat_kernel: copies the feature rows of the root and the accepted path into the
 //   drafter's pending-context buffer.
 #include "common.cuh"
+#include "checked.cuh"
 #include "trace.h"
 
 namespace df {
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(32) accept_walk_kernel(int n_tree, int max_new
 
 // grid: (n_layers * b * Hkv, 2): y = 0 moves K rows, y = 1 moves V columns.
 __global__ void __launch_bounds__(256) compact_kernel(df_bf16* k_cache, df_bf16* v_cache, int b, int Hkv, int cap,
-                                                      const AcceptScratch* __restrict__ scratch) {
+                                                      const AcceptScratch* __restrict__ scratch, int* status) {
   pdl_wait();
   pdl_trigger();
   constexpr int HD = 128;
@@ -102,8 +103,10 @@ __global__ void __launch_bounds__(256) compact_kernel(df_bf16* k_cache, df_bf16*
       if (c < total) {
         const int j = c >> 4, w = c & 15;
         const int src_slot = N + scratch[s].path[j];
-        buf[r] = base[(size_t)src_slot * 16 + w];
-        dst[r] = (N + 1 + j) * 16 + w;
+        if (DF_IN_BOUNDS(src_slot >= 0 && src_slot < cap && N + 1 + j < cap, status, 40)) {
+          buf[r] = base[(size_t)src_slot * 16 + w];
+          dst[r] = (N + 1 + j) * 16 + w;
+        }
       }
     }
     __syncthreads();
@@ -122,8 +125,11 @@ __global__ void __launch_bounds__(256) compact_kernel(df_bf16* k_cache, df_bf16*
       dst[r] = -1;
       if (c < total) {
         const int row = c / a, j = c % a;
-        buf[r] = base[(size_t)row * cap + N + scratch[s].path[j]];
-        dst[r] = row * cap + N + 1 + j;
+        const int src_slot = N + scratch[s].path[j];
+        if (DF_IN_BOUNDS(src_slot >= 0 && src_slot < cap && N + 1 + j < cap, status, 41)) {
+          buf[r] = base[(size_t)row * cap + src_slot];
+          dst[r] = row * cap + N + 1 + j;
+        }
       }
     }
     __syncthreads();
@@ -136,12 +142,13 @@ __global__ void __launch_bounds__(256) compact_kernel(df_bf16* k_cache, df_bf16*
 // grid: (b, max_new); copies feature row (root or path node) j of sequence s.
 __global__ void __launch_bounds__(256) gather_feat_kernel(const df_bf16* __restrict__ tree_feat, int n_tree,
                                                           int feat_dim, df_bf16* __restrict__ new_feat, int max_new,
-                                                          const AcceptScratch* __restrict__ scratch) {
+                                                          const AcceptScratch* __restrict__ scratch, int* status) {
   pdl_wait();
   pdl_trigger();
   const int s = blockIdx.x, j = blockIdx.y;
   if (j > scratch[s].a) return;
   const int node = j == 0 ? 0 : scratch[s].path[j - 1];
+  if (!DF_IN_BOUNDS(node >= 0 && node < n_tree, status, 42)) return;
   const uint4* src = reinterpret_cast<const uint4*>(tree_feat + ((size_t)s * n_tree + node) * feat_dim);
   uint4* dst = reinterpret_cast<uint4*>(new_feat + ((size_t)s * max_new + j) * feat_dim);
   for (int i = threadIdx.x; i < feat_dim / 8; i += blockDim.x) dst[i] = src[i];
@@ -159,9 +166,11 @@ int launch_accept(int b, int n_tree, const int32_t* choice, const int32_t* tok, 
   launch_k(accept_walk_kernel, dim3(b), dim3(32), 0, st, n_tree, max_new, choice, tok, parent, cache_len, cap, n_new, acc_tok, n_acc,
                                        new_bonus, src_slot, sc, status);
   if (k_cache && v_cache && n_layers > 0)
-    launch_k(compact_kernel, dim3(dim3(n_layers * b * Hkv, 2)), dim3(256), 0, st, k_cache, v_cache, b, Hkv, cap, sc);
+    launch_k(compact_kernel, dim3(dim3(n_layers * b * Hkv, 2)), dim3(256), 0, st, k_cache, v_cache, b, Hkv, cap, sc,
+             status);
   if (tree_feat && new_feat)
-    launch_k(gather_feat_kernel, dim3(dim3(b, max_new)), dim3(256), 0, st, tree_feat, n_tree, feat_dim, new_feat, max_new, sc);
+    launch_k(gather_feat_kernel, dim3(dim3(b, max_new)), dim3(256), 0, st, tree_feat, n_tree, feat_dim, new_feat, max_new, sc,
+             status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

@@ -10,6 +10,7 @@
 #include "gemm.h"
 #include "layers.h"
 #include "moe.h"
+#include "nvtx.h"
 
 namespace df {
 int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
@@ -154,12 +155,12 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
     MoeBufs m = B.moe;
     m.counts += (size_t)L.layer * c.n_experts;  // each layer's expert counts are kept
     DF_TRY(launch_moe_route(pv, R, c.n_experts, c.top_k, m, L.status, st));
-    DF_TRY(launch_moe_dispatch(B.x, R, d, c.n_experts, c.top_k, c.d_expert, m, st));
+    DF_TRY(launch_moe_dispatch(B.x, R, d, c.n_experts, c.top_k, c.d_expert, m, L.status, st));
     DF_TRY(launch_moe_experts(L.w->w_experts_gate_up, L.w->w_experts_down, R, d, c.n_experts, c.top_k, c.d_expert,
                               m, L.status, st));
     rn = L.out;
     rn.h = B.h; rn.d = d; rn.eps = c.rms_eps;
-    return launch_moe_combine(m, c.top_k, rn, st);
+    return launch_moe_combine(m, c.top_k, R * c.top_k, rn, L.status, st);
   }
   g = GemmDesc{};
   g.X = B.x; g.W = L.w->w_gate_up; g.M = R; g.N = 2 * F; g.K = d; g.ldx = d; g.ldw = d;
@@ -287,6 +288,7 @@ const char* dflash_status_string(int s) {
     case DF_ERR_NOT_IMPLEMENTED: return "not implemented";
     case DF_ERR_WORKSPACE: return "workspace missing or too small";
     case DF_ERR_DEVICE: return "device is not compute capability 10.3";
+    case DF_ERR_BOUNDS: return "device-side index check failed (checked build)";
     default: return "unknown status";
   }
 }
@@ -324,6 +326,7 @@ size_t ddtree_build_workspace_size(int b, int D, int V, int B) {
 int ddtree_build(const float* logprobs, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
                  int32_t* parent, int32_t* depth, float* score, uint32_t* anc, void* ws, size_t ws_bytes,
                  df_stream stream) {
+  DF_NVTX("ddtree_build");
   if (b < 0 || D < 1 || D > 31 || V < 2 || B < 0 || B > 2048) return DF_ERR_ARG;
   // B must not exceed the number of prefixes sum_{k<=D} V^k
   {
@@ -355,6 +358,7 @@ size_t dflash_chain_build_workspace_size(int b, int D) {
 int dflash_chain_build(const float* logprobs, int b, int D, int V, const int32_t* root_tok, int32_t* tok,
                        int32_t* parent, int32_t* depth, float* score, uint32_t* anc, void* ws, size_t ws_bytes,
                        df_stream stream) {
+  DF_NVTX("dflash_chain_build");
   if (b < 0 || D < 1 || D > 31 || V < 1) return DF_ERR_ARG;
   if (b == 0) return DF_OK;
   if (!logprobs || !tok || !parent || !depth || !score || !anc) return DF_ERR_ARG;
@@ -379,6 +383,7 @@ size_t tree_verify_attention_workspace_size(int b, int n_tree, int Hq, int Hkv, 
 int tree_verify_attention(int b, int n_tree, int Hq, int Hkv, int hd, const df_bf16* q, const df_bf16* k_cache,
                           const df_bf16* v_cache, int cap, const int32_t* cache_len, const uint32_t* anc, float scale,
                           df_bf16* out, void* ws, size_t ws_bytes, df_stream stream) {
+  DF_NVTX("tree_verify_attention");
   if (b < 0 || n_tree < 1 || Hkv <= 0 || Hq % Hkv || cap <= 0) return DF_ERR_ARG;
   const int G = Hq / Hkv;
   if (hd != 128 || G > 8 || (128 % G) || cap % 8) return DF_ERR_SHAPE;
@@ -412,6 +417,7 @@ int accept_and_compact(int b, int n_tree, const int32_t* choice, const int32_t* 
                        int32_t* cache_len, const df_bf16* tree_feat, int feat_dim, df_bf16* new_feat, int max_new,
                        int32_t* n_new, int32_t* acc_tok, int32_t* n_acc, int32_t* new_bonus, int32_t* src_slot,
                        void* ws, size_t ws_bytes, df_stream stream) {
+  DF_NVTX("accept_and_compact");
   if (b < 0 || n_tree < 1 || max_new < 1 || n_layers < 0 || cap <= 0) return DF_ERR_ARG;
   if (n_layers > 0 && (hd != 128 || Hkv <= 0)) return DF_ERR_SHAPE;
   if (b == 0) return DF_OK;
@@ -468,6 +474,7 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
                                const int32_t* depth, const uint32_t* anc, df_bf16* k_cache, df_bf16* v_cache, int cap,
                                const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat, void* ws,
                                size_t ws_bytes, df_stream stream) {
+  DF_NVTX("dflash_target_tree_forward");
   if (!cfg_ok(c)) return DF_ERR_SHAPE;
   if (!w || !w->layers || !w->embed || !w->final_norm || b < 0 || n_tree < 1 || cap <= 0) return DF_ERR_ARG;
   DF_TRY(layers_ok(c, w));
@@ -535,6 +542,7 @@ size_t dflash_draft_block_workspace_size(const df_model_cfg* dcfg, int b, int ma
 int dflash_draft_block(const df_model_cfg* c, const df_model_weights* w, int b, const df_bf16* new_feat, int max_new,
                        const int32_t* n_new, df_bf16* ctx_k, df_bf16* ctx_v, int32_t* ctx_len, int cap,
                        const int32_t* bonus, float* logprobs, void* ws, size_t ws_bytes, df_stream stream) {
+  DF_NVTX("dflash_draft_block");
   if (!cfg_ok(c) || c->block_size < 2 || c->n_feat_layers < 1 || c->n_experts != 0) return DF_ERR_SHAPE;
   if (!w || !w->layers || !w->embed || !w->final_norm || !w->fc || !w->fc_norm) return DF_ERR_ARG;
   if (b < 0 || max_new < 0 || cap <= 0) return DF_ERR_ARG;
@@ -621,6 +629,7 @@ size_t dflash_linear_argmax_workspace_size(int M) {
 
 int dflash_linear_argmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, int32_t* out, void* ws,
                          size_t ws_bytes, df_stream stream) {
+  DF_NVTX("dflash_linear_argmax");
   if (M < 0 || N <= 0 || K <= 0) return DF_ERR_ARG;
   if (K % 64) return DF_ERR_SHAPE;
   if (M == 0) return DF_OK;
@@ -648,6 +657,7 @@ size_t dflash_linear_logsoftmax_workspace_size(int M, int N) {
 
 int dflash_linear_logsoftmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out, void* ws,
                              size_t ws_bytes, df_stream stream) {
+  DF_NVTX("dflash_linear_logsoftmax");
   if (M < 0 || N <= 0 || K <= 0) return DF_ERR_ARG;
   if (K % 64) return DF_ERR_SHAPE;
   if (M == 0) return DF_OK;
@@ -686,6 +696,7 @@ int dflash_workspace_configure(void* ws, unsigned long long wait_limit_ns, int h
 
 int dflash_linear(const df_bf16* X, const df_bf16* W, int M, int N, int K, float* out, int accumulate, void* ws,
                   size_t ws_bytes, df_stream stream) {
+  DF_NVTX("dflash_linear");
   if (M < 0 || N < 0 || K <= 0) return DF_ERR_ARG;
   if (K % 64) return DF_ERR_SHAPE;
   if (M == 0 || N == 0) return DF_OK;

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "nvtx.h"
 
 namespace df {
 int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* root_tok, int32_t* tok,
@@ -52,6 +53,7 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 extern "C" int ddtree_build_static(const float* logprobs, int b, int D, int V, int B, const int32_t* root_tok,
                                    int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* anc,
                                    df_stream stream) {
+  DF_NVTX("ddtree_build_static");
   if (b < 0 || D < 1 || D > 31 || V < 2 || B < 0 || B > 2048) return DF_ERR_ARG;
   {
     double total = 0, p = 1;

@@ -22,6 +22,7 @@
 //   moe_combine_kernel  h += sum_j w_j expert_out_j, then RMSNorm (as res_norm)
 // No host synchronisation: the routing stays on the device, so a step is graph-capturable.
 #include "common.cuh"
+#include "checked.cuh"
 #include "gemm.h"
 #include "moe.h"
 #include "runtime.h"
@@ -213,13 +214,15 @@ __global__ void __launch_bounds__(kPermWarps * 32) moe_permute_kernel(int P, int
 }
 
 // grid: P; block 128: row pos of xp <- row pair_token[pos] of x (d / 8 uint4 per row)
-__global__ void __launch_bounds__(128) moe_gather_kernel(const df_bf16* __restrict__ x, int d,
+__global__ void __launch_bounds__(128) moe_gather_kernel(const df_bf16* __restrict__ x, int d, int R,
                                                          const int32_t* __restrict__ pair_token,
-                                                         df_bf16* __restrict__ xp) {
+                                                         df_bf16* __restrict__ xp, int* status) {
   pdl_wait();
   pdl_trigger();
   const int pos = blockIdx.x;
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)pair_token[pos] * d);
+  const int t = pair_token[pos];
+  if (!DF_IN_BOUNDS(t >= 0 && t < R, status, 50)) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
   uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * d);
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
 }
@@ -415,7 +418,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
 // expert outputs' loads of several choices are in flight together.
 __global__ void __launch_bounds__(1024) moe_combine_kernel(ResNormArgs a, const float* __restrict__ out,
                                                            const float* __restrict__ topk_w,
-                                                           const int32_t* __restrict__ pos_of, int k) {
+                                                           const int32_t* __restrict__ pos_of, int k, int P,
+                                                           int* status) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
@@ -424,8 +428,10 @@ __global__ void __launch_bounds__(1024) moe_combine_kernel(ResNormArgs a, const 
   const int o = blockIdx.x;
   const int t = (o / a.group_out) * a.group_in + a.in_off + (o % a.group_out);
   if (threadIdx.x < k) {
-    w_sh[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
-    pos_sh[threadIdx.x] = pos_of[(size_t)t * k + threadIdx.x];
+    const int pos = pos_of[(size_t)t * k + threadIdx.x];
+    const bool ok = DF_IN_BOUNDS(pos >= 0 && pos < P, status, 51);
+    w_sh[threadIdx.x] = ok ? topk_w[(size_t)t * k + threadIdx.x] : 0.f;
+    pos_sh[threadIdx.x] = ok ? pos : 0;
   }
   __syncthreads();
   const int per = blockDim.x * 4;
@@ -512,12 +518,13 @@ int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, int
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
-int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, int Fe, MoeBufs& m, cudaStream_t st) {
+int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, int Fe, MoeBufs& m, int* status,
+                        cudaStream_t st) {
   DF_TRACE("moe_dispatch", st);
   const int P = R * k;
   launch_k(moe_permute_kernel, dim3(1), dim3(kPermWarps * 32), 0, st, P, E, k, m.topk_id, m.counts, m.offsets,
            m.pos_of, m.pair_token, m.chunks, m.n_chunks, Fe / 64, num_sms());
-  launch_k(moe_gather_kernel, dim3(P), dim3(128), 0, st, x, d, m.pair_token, m.xp);
+  launch_k(moe_gather_kernel, dim3(P), dim3(128), 0, st, x, d, R, m.pair_token, m.xp, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
@@ -560,11 +567,11 @@ int launch_moe_experts(const df_bf16* w_gate_up, const df_bf16* w_down, int R, i
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
-int launch_moe_combine(const MoeBufs& m, int k, const ResNormArgs& a, cudaStream_t st) {
+int launch_moe_combine(const MoeBufs& m, int k, int P, const ResNormArgs& a, int* status, cudaStream_t st) {
   if (a.rows <= 0) return DF_OK;
   if (a.d % 256 || a.d > 8192 || !a.h) return DF_ERR_SHAPE;
   DF_TRACE("moe_combine", st);
-  launch_k(moe_combine_kernel, dim3(a.rows), dim3(a.d / 8), 0, st, a, m.out, m.topk_w, m.pos_of, k);
+  launch_k(moe_combine_kernel, dim3(a.rows), dim3(a.d / 8), 0, st, a, m.out, m.topk_w, m.pos_of, k, P, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

@@ -32,11 +32,12 @@ size_t moe_buf_elems(int R, int k, int E, int d, int Fe, size_t* sizes /* [kMoeB
 int launch_moe_route(const PartialView& pv, int R, int E, int k, MoeBufs& m, int* status, cudaStream_t st);
 // topk_id -> counts, offsets, pos_of, pair_token, the grouped GEMM's chunk list; then
 // xp = x[pair_token]
-int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, int Fe, MoeBufs& m, cudaStream_t st);
+int launch_moe_dispatch(const df_bf16* x, int R, int d, int E, int k, int Fe, MoeBufs& m, int* status,
+                        cudaStream_t st);
 // grouped expert products: act = SwiGLU(xp . W_gate_up[e]^T), out = act . W_down[e]^T
 int launch_moe_experts(const df_bf16* w_gate_up, const df_bf16* w_down, int R, int d, int E, int k, int Fe,
                        MoeBufs& m, int* status, cudaStream_t st);
-// h += sum_j w_j out[pos_of[t][j]];  then RMSNorm like res_norm (a.pv unused)
-int launch_moe_combine(const MoeBufs& m, int k, const ResNormArgs& a, cudaStream_t st);
+// h += sum_j w_j out[pos_of[t][j]];  then RMSNorm like res_norm (a.pv unused); P = R k rows of out
+int launch_moe_combine(const MoeBufs& m, int k, int P, const ResNormArgs& a, int* status, cudaStream_t st);
 
 }  // namespace df

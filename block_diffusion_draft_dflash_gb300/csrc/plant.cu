@@ -14,6 +14,7 @@
 // tree holds both branches, a single chain only the first.  miss_bias = 0 leaves such rows
 // as they are.
 #include "common.cuh"
+#include "nvtx.h"
 #include "trace.h"
 
 namespace df {
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(512) plant_logprobs_kernel(float* __restrict__
 extern "C" int dflash_plant_logprobs(float* logprobs, int b, int D, int V, const int32_t* ref, int n_pos,
                                      const int32_t* pos, float rate, float bias, float miss_bias,
                                      unsigned long long seed, df_stream stream) {
+  DF_NVTX("dflash_plant_logprobs");
   if (b < 0 || D < 1 || V < 1 || n_pos < 0) return DF_ERR_ARG;
   if (b == 0 || n_pos == 0) return DF_OK;
   if (!logprobs || !ref || !pos) return DF_ERR_ARG;

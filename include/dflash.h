@@ -63,7 +63,9 @@ enum {
   DF_ERR_TIMEOUT = -7,         /* a bounded device-side wait ran out                 */
   DF_ERR_NOT_IMPLEMENTED = -8,
   DF_ERR_WORKSPACE = -9,       /* workspace missing or smaller than required         */
-  DF_ERR_DEVICE = -10          /* current device is not compute capability 10.3      */
+  DF_ERR_DEVICE = -10,         /* current device is not compute capability 10.3      */
+  DF_ERR_BOUNDS = -11          /* a device-side index check failed (DFLASH_CHECKED builds
+                                  only; the access was skipped, detail = the check's id)   */
 };
 
 /* Shape of one decoder-only transformer (Qwen3 family layout). */

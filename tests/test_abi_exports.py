@@ -50,3 +50,28 @@ def test_host_argument_checks_without_gpu():
     assert lib.tree_verify_attention(1, 5, 8, 2, 64, None, None, None, 64, None, None, 1.0, None,
                                      None, 0, None) == -2                               # hd != 128
     assert lib.dflash_linear(None, None, 4, 4, 100, None, 0, None, 0, None) == -2      # K % 64
+
+
+def test_checked_build_is_separate_and_compiles():
+    # DFLASH_CHECKED=1 selects the checked build: its own output directory, and the index
+    # checks compile (one translation unit compiled here; the GPU tests run the whole library)
+    import subprocess
+    import sys
+    import tempfile
+    code = "import block_diffusion_draft_dflash_gb300.build as b; print(b.CHECKED, b.LIB)"
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                         env=dict(os.environ, DFLASH_CHECKED="1")).stdout.split()
+    assert out[0] == "True" and out[1].endswith(os.path.join("_build_checked", "libdflash.so"))
+    from block_diffusion_draft_dflash_gb300 import build
+    assert not build.CHECKED and build.LIB.endswith(os.path.join("_build", "libdflash.so"))
+    with tempfile.TemporaryDirectory() as d:
+        r = subprocess.run([build._nvcc(), *build.ARCH, *build.FLAGS, "-DDFLASH_CHECKED=1", "-I", build.INCLUDE, "-c",
+                            os.path.join(build.CSRC, "accept.cu"), "-o", os.path.join(d, "accept.o")],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
+def test_status_string_of_every_code():
+    from block_diffusion_draft_dflash_gb300 import _lib
+    for code in range(-11, 0):
+        assert _lib.status_string(code) != "unknown status", code

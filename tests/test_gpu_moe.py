@@ -116,3 +116,65 @@ def test_moe_all_tokens_to_the_lowest_experts(k, B):
     assert ids[0].tolist() == list(range(k)) and np.all(w == 1.0 / k)
     counts = _check(tw, t, kc, vc, np.ones(B + 1, bool))
     np.testing.assert_array_equal(counts[0], [B + 1] * k + [0] * (32 - k))
+
+
+def test_moe_target_two_sequences_share_the_experts():
+    # b = 2 with different cache lengths: the rows of both sequences are routed together
+    # (an expert's chunk may hold rows of both); each sequence is compared with the oracle.
+    # One layer, so a row's result depends on its own routing only (attention comes first).
+    shape = synth.ModelShape(1, 512, 8, 2, 128, 0, 4000, feat_layers=(1,), block_size=8, n_experts=32, top_k=4,
+                             d_expert=128)
+    tw = synth.target_weights(shape, 7001)
+    tm = engine.DeviceModel.from_host(tw)
+    b, B, Ns, cap = 2, 90, [37, 200], 512
+    T = B + 1
+    rng = np.random.default_rng(7)
+    kc = synth.normal(7001, "mk2", (1, b, 2, cap, 128))
+    vc = synth.normal(7001, "mv2", (1, b, 2, cap, 128))
+    trees = []
+    for s in range(b):
+        kc[:, s, :, Ns[s]:] = 0
+        vc[:, s, :, Ns[s]:] = 0
+        t = ddtree.build_tree(ddtree.log_softmax(rng.normal(0, 2, size=(7, shape.vocab))), B)
+        t["tok"][0] = 100 + s
+        trees.append(t)
+    k_t = bf16_dev(kc)
+    v_t = bf16_dev(vc).transpose(-1, -2).contiguous()
+    st = lambda key: torch.from_numpy(np.stack([t[key] for t in trees]).astype(np.int32)).cuda()
+    anc = torch.from_numpy(np.stack([ddtree.ancestor_mask(t["parent"]) for t in trees]).view(np.int32)).cuda()
+    clen = torch.tensor(Ns, dtype=torch.int32, device="cuda")
+    choice = torch.zeros(b, T, dtype=torch.int32, device="cuda")
+    feat = torch.zeros(b, T, shape.d_model, dtype=torch.bfloat16, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, b, T))
+    _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k_t, v_t, clen, choice, feat, ws)
+    counts = torch.zeros(1, 32, dtype=torch.int32, device="cuda")
+    _lib.target_expert_counts(tm.cfg, b, T, ws, counts)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert np.all(counts.cpu().numpy().sum(axis=1) == b * T * 4)
+    n_clear = 0
+    for s in range(b):
+        cache = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), s)
+        och, ofeat, ologits = step.target_tree_forward(tw, trees[s]["tok"], trees[s]["parent"], trees[s]["depth"],
+                                                       cache, Ns[s])
+        # rows whose routing is clear in both layers (oracle margins), as in the one-sequence test
+        clear = np.ones(T, bool)
+        h = np.asarray(tw.embed, np.float64)[trees[s]["tok"]]
+        c2 = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), s)
+        for li, L in enumerate(tw.layers):
+            pos = Ns[s] + trees[s]["depth"]
+            q, k_, v_ = model.qkv_rows(L, shape, model.rms_norm(h, L.attn_norm, shape.rms_eps))
+            q, k_ = model.qk_finish(L, shape, q, k_, pos)
+            c2.k[li][Ns[s]:Ns[s] + T] = k_
+            c2.v[li][Ns[s]:Ns[s] + T] = v_
+            h = h + model.linear(verify.tree_attention(shape, q, c2.k[li], c2.v[li], Ns[s], trees[s]["parent"]),
+                                 L.w_o)
+            lg = np.sort(model.linear(model.rms_norm(h, L.mlp_norm, shape.rms_eps), L.w_router), axis=-1)[:, ::-1]
+            clear &= (lg[:, shape.top_k - 1] - lg[:, shape.top_k]) > 0.02
+            h = model.moe_block(L, shape, h)
+        n_clear += clear.sum()
+        rel_close(to_np(feat[s])[clear], ofeat[clear])
+        top2 = np.sort(ologits, axis=-1)[:, -2:]
+        sure = clear & ((top2[:, 1] - top2[:, 0]) > 0.02 * np.abs(ologits).max())
+        np.testing.assert_array_equal(choice[s].cpu().numpy()[sure], och[sure])
+    assert n_clear > 0.4 * b * T
