@@ -15,12 +15,13 @@
 //     radix select (12 + 12 + 8 bit digits, MSB first, warp-aggregated shared-memory
 //     histograms) for the K-th largest key T, a gather of every key > T and the lowest-id
 //     keys == T, and the same sort.
-// Kernel 2 (ddtree_heap_kernel): one CTA per sequence.  One warp runs the best-first
-//   selection: each candidate is a single 64-bit key whose integer order is the tree's
-//   total order (score desc, depth asc, parent index asc, rank asc), the live candidates
-//   are held in the warp's registers and every pop is a warp-wide maximum.  The CTA then
-//   writes the node arrays and the ancestor bitsets (one warp per row; each lane owns a
-//   32-bit word).
+// Kernel 2 (ddtree_heap_kernel, or ddtree_tourney_kernel from 256 nodes on): one CTA per
+//   sequence.  One warp runs the best-first selection: each candidate is a single 64-bit key
+//   whose integer order is the tree's total order (score desc, depth asc, parent index asc,
+//   rank asc); the live candidates are held in the warp's registers (every pop a warp-wide
+//   maximum over them) or, for larger budgets, one per node in a three-level tournament in
+//   shared memory (every pop two slot updates and their group maxima).  The CTA then writes
+//   the node arrays and the ancestor bitsets (one warp per row; each lane owns a 32-bit word).
 #include "common.cuh"
 #include "runtime.h"
 #include "trace.h"
@@ -28,6 +29,10 @@
 namespace df {
 
 constexpr int kTopkThreads = 1024;
+#ifndef DF_TOURNEY_MIN_B
+#define DF_TOURNEY_MIN_B 256
+#endif
+constexpr int kTourneyMinB = DF_TOURNEY_MIN_B;  // budgets from which the selection runs as a tournament
 constexpr int kMaxK = 2048;
 
 DF_DEV void hist_add(uint32_t* hist, uint32_t digit, bool active) {
@@ -453,6 +458,35 @@ DF_DEV unsigned long long heap_key(float s, int depth, int parent, int rank) {
          ((uint32_t)(2047 - parent) << 16) | ((uint32_t)(2047 - rank) << 5);
 }
 
+// The selected nodes (shared memory) -> the tree's arrays and ancestor bitsets (whole CTA).
+DF_DEV void write_tree(int s, int n, int D, int K, const int32_t* __restrict__ topk_id,
+                       const int32_t* __restrict__ root_tok, const int32_t* n_par, const int32_t* n_dep,
+                       const int32_t* n_rank, const float* n_score, int32_t* __restrict__ tok,
+                       int32_t* __restrict__ parent, int32_t* __restrict__ depth, float* __restrict__ score,
+                       uint32_t* __restrict__ anc) {
+  const int tid = threadIdx.x, W = (n + 31) / 32;
+  const size_t o = (size_t)s * n;
+  const int32_t* gid = topk_id + (size_t)s * D * K;
+  for (int i = tid; i < n; i += blockDim.x) {
+    tok[o + i] = i == 0 ? (root_tok ? root_tok[s] : -1) : gid[(n_dep[i] - 1) * K + n_rank[i]];
+    parent[o + i] = n_par[i];
+    depth[o + i] = n_dep[i];
+    score[o + i] = n_score[i];
+  }
+  // Ancestor bitsets: one warp per row, lane w owns words w, w+32, ...
+  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  uint32_t* arow = anc + (size_t)s * n * W;
+  for (int i = warp; i < n; i += nwarps) {
+    for (int w0 = 0; w0 < W; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t bits = 0;
+      for (int j = i; j >= 0; j = n_par[j])
+        if ((j >> 5) == w) bits |= 1u << (j & 31);
+      if (w < W) arow[(size_t)i * W + w] = bits;
+    }
+  }
+}
+
 // One CTA per sequence; warp 0 runs the best-first selection.  The live candidates (at most
 // B + 1) sit in the warp's registers, NREG per lane, densely packed: candidate c lives in
 // lane c % 32, register c / 32.  Each pop takes the lane maxima, a warp maximum (two redux steps)
@@ -470,7 +504,6 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
   extern __shared__ __align__(16) unsigned char smem[];
   const int s = blockIdx.x, tid = threadIdx.x;
   const int n = B + 1;
-  const int W = (n + 31) / 32;
   float* val = reinterpret_cast<float*>(smem);                                       // [D][K]
   int32_t* n_par = reinterpret_cast<int32_t*>(val + ((D * K + 1) & ~1));             // [n]
   int32_t* n_dep = n_par + n;                                                        // [n]
@@ -538,27 +571,104 @@ __global__ void __launch_bounds__(256) ddtree_heap_kernel(const int32_t* __restr
     }
   }
   __syncthreads();
+  write_tree(s, n, D, K, topk_id, root_tok, n_par, n_dep, n_rank, n_score, tok, parent, depth, score, anc);
+}
 
-  const size_t o = (size_t)s * n;
-  const int32_t* gid = topk_id + (size_t)s * D * K;
-  for (int i = tid; i < n; i += blockDim.x) {
-    tok[o + i] = i == 0 ? (root_tok ? root_tok[s] : -1) : gid[(n_dep[i] - 1) * K + n_rank[i]];
-    parent[o + i] = n_par[i];
-    depth[o + i] = n_dep[i];
-    score[o + i] = n_score[i];
-  }
-  // Ancestor bitsets: one warp per row, lane w owns words w, w+32, ...
-  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  uint32_t* arow = anc + (size_t)s * n * W;
-  for (int i = warp; i < n; i += nwarps) {
-    for (int w0 = 0; w0 < W; w0 += 32) {
-      const int w = w0 + lane;
-      uint32_t bits = 0;
-      for (int j = i; j >= 0; j = n_par[j])
-        if ((j >> 5) == w) bits |= 1u << (j & 31);
-      if (w < W) arow[(size_t)i * W + w] = bits;
+// Warp-wide maximum of a 64-bit key: the high words with one redux, then the low words among
+// the lanes that hold the top high word.
+DF_DEV unsigned long long warp_max_key(unsigned long long v) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(v >> 32));
+  const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(v >> 32) == hi ? (uint32_t)v : 0u);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+// The same best-first selection with the candidates in a three-level tournament in shared
+// memory instead of registers.  Every node holds at most one live candidate, its best child
+// not yet selected: selecting a child c of p replaces p's candidate by c's next sibling and
+// gives c its first child.  So the candidates sit in slots indexed by node (leaf[p]), and a
+// selection changes two slots; a change recomputes the maximum of the slot's group of 32
+// (one warp maximum), of that group's group of 32, and of the few top groups.  The keys,
+// hence the order of selection, are those of ddtree_heap_kernel.
+__global__ void __launch_bounds__(256) ddtree_tourney_kernel(const int32_t* __restrict__ topk_id,
+                                                             const float* __restrict__ topk_val, int D, int K, int B,
+                                                             const int32_t* __restrict__ root_tok,
+                                                             int32_t* __restrict__ tok, int32_t* __restrict__ parent,
+                                                             int32_t* __restrict__ depth, float* __restrict__ score,
+                                                             uint32_t* __restrict__ anc, const int* status) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int s = blockIdx.x, tid = threadIdx.x;
+  const int n = B + 1;
+  const int n0 = (n + 31) & ~31, n1 = ((n0 >> 5) + 31) & ~31, n2 = n1 >> 5;  // level sizes (n2 <= 32)
+  unsigned long long* leaf = reinterpret_cast<unsigned long long*>(smem);  // [n0] candidate of each node
+  unsigned long long* lv1 = leaf + n0;                                     // [n1] maxima of 32 leaves
+  unsigned long long* lv2 = lv1 + n1;                                      // [n2] maxima of 32 lv1 entries
+  float* val = reinterpret_cast<float*>(lv2 + ((n2 + 1) & ~1));            // [D][K]
+  int32_t* n_par = reinterpret_cast<int32_t*>(val + ((D * K + 1) & ~1));   // [n]
+  int32_t* n_dep = n_par + n;
+  int32_t* n_rank = n_dep + n;
+  float* n_score = reinterpret_cast<float*>(n_rank + n);
+
+  if (status && *(volatile const int*)status == DF_ERR_NAN) return;  // NaN found by top-K
+  const float* gval = topk_val + (size_t)s * D * K;
+  for (int i = tid; i < D * K; i += blockDim.x) val[i] = gval[i];
+  for (int i = tid; i < n0 + n1 + n2; i += blockDim.x) leaf[i] = 0ull;  // 0 = no candidate
+  __syncthreads();
+
+  if (tid < 32) {
+    const int lane = tid;
+    n_par[0] = -1; n_dep[0] = 0; n_rank[0] = -1; n_score[0] = 0.f;
+    // up to 2048 nodes the (at most 64) lv1 maxima are read directly for the top (two levels)
+    const bool two_level = n1 <= 64;
+    // a slot changed: its group maxima up to the top
+    auto fix = [&](int x) {
+      const int g1 = x >> 5, g2 = g1 >> 5;
+      __syncwarp();
+      const unsigned long long m1 = warp_max_key(leaf[(g1 << 5) + lane]);
+      if (lane == 0) lv1[g1] = m1;
+      __syncwarp();
+      if (two_level) return;
+      const unsigned long long m2 = warp_max_key(lv1[(g2 << 5) + lane]);
+      if (lane == 0) lv2[g2] = m2;
+      __syncwarp();
+    };
+    if (B > 0) {
+      if (lane == 0) leaf[0] = heap_key(0.f + val[0], 1, 0, 0);
+      fix(0);
+    }
+    for (int idx = 1; idx <= B; ++idx) {
+      unsigned long long t0;
+      if (two_level) {
+        const unsigned long long a = lv1[lane], c = lane + 32 < n1 ? lv1[lane + 32] : 0ull;
+        t0 = a > c ? a : c;
+      } else {
+        t0 = lane < n2 ? lv2[lane] : 0ull;
+      }
+      const unsigned long long top = warp_max_key(t0);
+      const uint32_t lo = (uint32_t)top;
+      const int dep = 31 - (int)(lo >> 27);
+      const int par = 2047 - (int)((lo >> 16) & 0x7FF);
+      const int r = 2047 - (int)((lo >> 5) & 0x7FF);
+      const float sc = key_float((uint32_t)(top >> 32));
+      // every lane writes the node arrays (same value), so every lane reads its own writes
+      n_par[idx] = par; n_dep[idx] = dep; n_rank[idx] = r; n_score[idx] = sc;
+      const unsigned long long sib = r + 1 < K ? heap_key(n_score[par] + val[(dep - 1) * K + r + 1], dep, par, r + 1) : 0ull;
+      const unsigned long long kid = dep < D ? heap_key(sc + val[dep * K], dep + 1, idx, 0) : 0ull;
+      __syncwarp();
+      if (lane == 0) { leaf[par] = sib; leaf[idx] = kid; }
+      fix(par);
+      if ((idx >> 5) != (par >> 5)) fix(idx);
     }
   }
+  __syncthreads();
+  write_tree(s, n, D, K, topk_id, root_tok, n_par, n_dep, n_rank, n_score, tok, parent, depth, score, anc);
+}
+
+size_t ddtree_tourney_smem(int D, int K, int B) {
+  const int n = B + 1;
+  const int n0 = (n + 31) & ~31, n1 = ((n0 >> 5) + 31) & ~31, n2 = n1 >> 5;
+  return (size_t)(n0 + n1 + ((n2 + 1) & ~1)) * 8 + (size_t)((D * K + 1) & ~1) * 4 + (size_t)n * 16;
 }
 
 }  // namespace df
@@ -627,6 +737,16 @@ int launch_ddtree(const float* lp, int b, int D, int V, int B, const int32_t* ro
              score, anc, status);
     return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
   };
+  // the tournament in shared memory from 256 nodes on (its cost grows with log B, the
+  // registers' with B: equal at 256, 2.8x faster at 1024), when it fits beside the log-probs
+  const size_t smem_t = ddtree_tourney_smem(D, K > 0 ? K : 1, B);
+  if (B >= kTourneyMinB && smem_t <= 227 * 1024) {
+    if (ensure_dynamic_smem(ddtree_tourney_kernel, smem_t) != cudaSuccess) return DF_ERR_CUDA;
+    DF_TRACE("ddtree_heap", st);
+    launch_k(ddtree_tourney_kernel, dim3(b), dim3(256), smem_t, st, topk_id, topk_val, D, K > 0 ? K : 1, B, root_tok,
+             tok, parent, depth, score, anc, status);
+    return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  }
   if (nreg <= 1) return launch(ddtree_heap_kernel<1>);
   if (nreg <= 2) return launch(ddtree_heap_kernel<2>);
   if (nreg <= 4) return launch(ddtree_heap_kernel<4>);
