@@ -178,3 +178,53 @@ def test_moe_target_two_sequences_share_the_experts():
         sure = clear & ((top2[:, 1] - top2[:, 0]) > 0.02 * np.abs(ologits).max())
         np.testing.assert_array_equal(choice[s].cpu().numpy()[sure], och[sure])
     assert n_clear > 0.4 * b * T
+
+
+def test_moe_layer_at_qwen3_30b_a3b_width():
+    # One layer at the benchmarked width (d 2048, 32/4 heads, experts of width 768, 8 per row;
+    # 32 experts instead of 128 to keep the host weights small) over a 257-row tree: the
+    # grouped GEMM runs the step's k-steps (32 for gate/up, 12 for down) and feature tiles
+    # (12 and 16).  Sampled rows with clear routing are checked against the oracle.
+    shape = synth.ModelShape(1, 2048, 32, 4, 128, 0, 4000, feat_layers=(1,), block_size=16, n_experts=32, top_k=8,
+                             d_expert=768)
+    tw = synth.target_weights(shape, 8001)
+    tm = engine.DeviceModel.from_host(tw)
+    N, B, cap = 300, 256, 640
+    T = B + 1
+    t = ddtree.build_tree(ddtree.log_softmax(np.random.default_rng(8).normal(0, 2, size=(15, shape.vocab))), B)
+    t["tok"][0] = 42
+    kc = synth.normal(8001, "wk", (1, 1, 4, cap, 128))
+    vc = synth.normal(8001, "wv", (1, 1, 4, cap, 128))
+    kc[..., N:, :] = 0
+    vc[..., N:, :] = 0
+    k_t = bf16_dev(kc)
+    v_t = bf16_dev(vc).transpose(-1, -2).contiguous()
+    st = lambda key: torch.from_numpy(t[key][None].astype(np.int32)).cuda()
+    anc = torch.from_numpy(ddtree.ancestor_mask(t["parent"])[None].view(np.int32)).cuda()
+    clen = torch.tensor([N], dtype=torch.int32, device="cuda")
+    choice = torch.zeros(1, T, dtype=torch.int32, device="cuda")
+    feat = torch.zeros(1, T, shape.d_model, dtype=torch.bfloat16, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, 1, T))
+    _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k_t, v_t, clen, choice, feat, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    # oracle: attention for every row (the tree's K/V), then the feed-forward of sampled rows
+    L = tw.layers[0]
+    h = np.asarray(tw.embed, np.float64)[t["tok"]]
+    q, k_, v_ = model.qkv_rows(L, shape, model.rms_norm(h, L.attn_norm, shape.rms_eps))
+    q, k_ = model.qk_finish(L, shape, q, k_, N + t["depth"])
+    c = _oracle_cache(kc, vc)
+    c.k[0][N:N + T] = k_
+    c.v[0][N:N + T] = v_
+    rows = np.random.default_rng(9).choice(T, 40, replace=False)
+    rows.sort()
+    qs = q[rows]
+    o = model.attention_rows(shape, qs, lambda i: (np.concatenate([c.k[0][:N], c.k[0][N + np.array(
+        verify.ancestors(t["parent"], int(rows[i])))]]), np.concatenate([c.v[0][:N], c.v[0][N + np.array(
+        verify.ancestors(t["parent"], int(rows[i])))]])))
+    hs = h[rows] + model.linear(o, L.w_o)
+    lg = np.sort(model.linear(model.rms_norm(hs, L.mlp_norm, shape.rms_eps), L.w_router), axis=-1)[:, ::-1]
+    clear = (lg[:, 7] - lg[:, 8]) > 0.02
+    assert clear.sum() >= 10
+    want = model.moe_block(L, shape, hs[clear])
+    rel_close(to_np(feat[0])[rows[clear]], want)
