@@ -29,10 +29,7 @@
 namespace df {
 
 constexpr int kTopkThreads = 1024;
-#ifndef DF_TOURNEY_MIN_B
-#define DF_TOURNEY_MIN_B 256
-#endif
-constexpr int kTourneyMinB = DF_TOURNEY_MIN_B;  // budgets from which the selection runs as a tournament
+constexpr int kTourneyMinB = 256;  // budgets from which the selection runs as a tournament
 constexpr int kMaxK = 2048;
 
 DF_DEV void hist_add(uint32_t* hist, uint32_t digit, bool active) {
