@@ -267,3 +267,37 @@ def test_prefill_and_first_context_match_oracle(models):
         for l in range(DS.n_layers):
             rel_close(ck[l], ctx.k[l][:P].transpose(1, 0, 2))
             rel_close(cv[l], ctx.v[l][:P].transpose(1, 2, 0))
+
+
+def test_draft_block_qwen3_width():
+    # One drafter layer at Qwen3-8B width (d 4096, 32/8 heads, F 12288) fed 5 target feature
+    # layers (context fusion 20480 -> 4096): the drafter's GEMMs run at the benchmarked shapes
+    # and launch configuration (16 block rows, 16 + 16 rows for q/k/v, 16 context rows for the
+    # fusion), over 512 cached context keys.  Small vocabulary keeps the oracle to seconds.
+    V, nf, ctx0, n_new = 2048, 5, 512, 16
+    tshape = synth.ModelShape(0, 4096, 32, 8, 128, 12288, V, feat_layers=(), block_size=16)
+    tw = synth.target_weights(tshape, 2007)
+    ds = synth.ModelShape(1, 4096, 32, 8, 128, 12288, V, block_size=16)
+    dw = synth.drafter_weights(ds, tw, nf, 2007)
+    tm_embed = bf16_dev(tw.embed)
+    dm = engine.DeviceModel.from_host(dw, embed=tm_embed, n_feat=nf)
+    cap, L = 640, ds.block_size
+    feat = synth.normal(33, "dfq", (1, n_new, nf * ds.d_model))
+    kc = synth.normal(33, "dkq", (1, 1, ds.n_kv_heads, cap, 128))
+    vc = synth.normal(33, "dvq", (1, 1, ds.n_kv_heads, cap, 128))
+    kc[:, :, :, ctx0:] = 0
+    vc[:, :, :, ctx0:] = 0
+    k = bf16_dev(kc)
+    v = bf16_dev(vc).transpose(-1, -2).contiguous()
+    ctx_len = torch.tensor([ctx0], dtype=torch.int32, device="cuda")
+    lp = torch.zeros(1, L - 1, V, dtype=torch.float32, device="cuda")
+    ws = _lib.Workspace(_lib.draft_block_workspace_size(dm.cfg, 1, n_new))
+    _lib.draft_block(dm.cfg, dm.weights, bf16_dev(feat), torch.tensor([n_new], dtype=torch.int32, device="cuda"),
+                     k, v, ctx_len, torch.tensor([77], dtype=torch.int32, device="cuda"), lp, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0 and ctx_len.item() == ctx0 + n_new
+    ctx = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), 0)
+    olp, n1, _ = step.draft_block(dw, feat[0].astype(np.float64), ctx, ctx0, 77)
+    rel_close(lp[0].cpu().numpy(), olp)
+    rel_close(to_np(k[0, 0, :, ctx0:n1]), ctx.k[0][ctx0:n1].transpose(1, 0, 2))
+    rel_close(to_np(v[0, 0, :, :, ctx0:n1]), ctx.v[0][ctx0:n1].transpose(1, 2, 0))
