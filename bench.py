@@ -67,6 +67,9 @@ def parse():
                     help="tree: DDTree of B nodes; chain: vanilla DFlash (argmax chain of 15)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample-json", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--whole-step", action="store_true",
+                    help="with --impl reference: time one whole oracle step at full size (minutes; ~45 GB of host "
+                         "memory) instead of the bounded sample")
     ap.add_argument("--kernel-case", default=None, choices=["gemm", "attn", "ddtree", "draft", "layer", "moe"],
                     help="run one small isolated case of a kernel a few times (for ncu captures), no JSON")
     ap.add_argument("--case-n", type=int, default=24576, help="gemm case: weight rows (output features)")
@@ -114,6 +117,8 @@ def workload_name(a):
 
 def config(a, impl="gb300"):
     timing = ("CUDA graph replay of whole steps, CUDA events on the launching stream" if impl == "gb300" else
+              "oracle on the host cores: wall-clock of one whole step, not extrapolated"
+              if getattr(a, "whole_step", False) else
               "oracle on the host cores: wall-clock of a bounded sample of one step, scaled to the whole step")
     TS, DS = shapes(a)
     gb = 2 * (TS.n_layers * layer_params(TS) + DS.n_layers * layer_params(DS) + TS.vocab * TS.d_model) / 1e9
@@ -133,9 +138,12 @@ def config(a, impl="gb300"):
 def oracle_sample(a, budget_s=25.0):
     """Time the oracle on a bounded sample of one step and scale to a whole step.
 
-    Sample: DDTree build (full, B tree), one target layer on 8 of the B+1 tree rows
-    (attention over the full context), one drafter layer on the 16 block rows, 8 rows
-    of the target LM head and 15 of the drafter's; scaled to 36 / 5 layers and B+1 rows.
+    Sample: DDTree build (full, B tree); one target layer with its projections on all B+1
+    tree rows and its ancestor-masked attention (a Python loop per row and head) on 8 rows
+    scaled to B+1; one drafter layer on the 16 block rows; all LM-head rows against a slice
+    of the vocabulary; scaled to 36 / 5 layers.  (Each weight matrix is converted to
+    float64 once per call in the oracle, so calls are timed at their real row counts.)
+    A whole step, timed without extrapolation, is `--whole-step`.
     """
     import numpy as np
 
@@ -152,23 +160,32 @@ def oracle_sample(a, budget_s=25.0):
     t0 = time.perf_counter()
     tree = ddtree.build_tree(lp, B)
     t_tree = time.perf_counter() - t0
-    # one target layer, 8 tree rows (a mixture-of-experts layer holds 16 of its experts: a
-    # row's cost is its top_k experts' products whatever the expert count)
+    # one target layer: the projections (and a dense feed-forward) on all B+1 tree rows, as
+    # the oracle runs them (each weight matrix converted to float64 once per call); the
+    # ancestor-masked attention (a Python loop over rows and heads) on 8 rows, scaled to B+1.
+    # A mixture-of-experts layer holds 16 of its experts (a row's cost is its top_k experts'
+    # products whatever the expert count) and its feed-forward is timed on the 8 rows too.
     TSs = dataclasses.replace(TS, n_experts=16) if TS.n_experts else TS
     lw = synth.layer_weights(TSs, 1005, "bench.layer")
     rows = 8
-    h = synth.normal(1005, "bench.h", (rows, TS.d_model))
+    h = synth.normal(1005, "bench.h", (T, TS.d_model)).astype(np.float64)
+    o_all = synth.normal(1005, "bench.o", (T, TS.n_q_heads * TS.head_dim)).astype(np.float64)
     kc = synth.normal(1005, "bench.k", (N + T, TS.n_kv_heads, 128)).astype(np.float64)
     vc = synth.normal(1005, "bench.v", (N + T, TS.n_kv_heads, 128)).astype(np.float64)
     t0 = time.perf_counter()
     x = model.rms_norm(h, lw.attn_norm, TS.rms_eps)
     q, k, v = model.qkv_rows(lw, TS, x)
-    q, k = model.qk_finish(lw, TS, q, k, N + tree["depth"][:rows])
-    sub_parent = tree["parent"][:rows]
-    o = verify.tree_attention(TS, q, kc, vc, N, sub_parent)
-    hh = h + model.linear(o, lw.w_o)
-    hh = model.ffn_block(lw, TSs, hh)
-    t_layer = time.perf_counter() - t0
+    q, k = model.qk_finish(lw, TS, q, k, N + tree["depth"])
+    hh = h + model.linear(o_all, lw.w_o)
+    if not TS.n_experts:
+        model.ffn_block(lw, TSs, hh)
+    t_all_rows = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    verify.tree_attention(TS, q[:rows], kc, vc, N, tree["parent"][:rows])
+    if TS.n_experts:
+        model.ffn_block(lw, TSs, hh[:rows])
+    t_per_rows = time.perf_counter() - t0
+    t_layer = t_all_rows + t_per_rows * (T / rows)
     dlw = lw if (DS.d_ff == TS.d_ff and not TS.n_experts) else synth.layer_weights(DS, 1006, "bench.dlayer")
     # drafter layer on 16 rows (attention over ctx + block)
     t0 = time.perf_counter()
@@ -182,23 +199,79 @@ def oracle_sample(a, budget_s=25.0):
     hd = hd + model.linear(o, dlw.w_o)
     model.mlp_block(dlw, DS, hd)
     t_dlayer = time.perf_counter() - t0
-    # LM-head rows against a 16384-row slice of the embedding, scaled to the full vocab
+    # both LM heads' rows (B+1 target, 15 drafter) against a 16384-row slice of the
+    # embedding, scaled to the full vocabulary
     Vs = 16384
     E = synth.normal(1007, "bench.E", (Vs, TS.d_model))
+    hl = np.concatenate([h, h[:15]])
     t0 = time.perf_counter()
-    model.linear(h[:2], E)
-    t_head_row = (time.perf_counter() - t0) / 2 * (TS.vocab / Vs)
-    est = t_tree + t_layer * (T / rows) * TS.n_layers + t_dlayer * DS.n_layers + t_head_row * (T + 15)
+    model.linear(hl, E)
+    t_head = (time.perf_counter() - t0) * (TS.vocab / Vs)
+    est = t_tree + t_layer * TS.n_layers + t_dlayer * DS.n_layers + t_head
     wall = time.perf_counter() - t_all
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0) or (os.cpu_count() or 1)
     return {"value": 1.0 / est, "unit": "spec steps/s", "cores": threads, "kind": "oracle",
             "sample": (f"oracle (numpy fp64, BLAS on {threads} thread(s), Python loops on one) timed on: DDTree "
-                       f"build B={B}; 1 target layer x {rows} of {T} tree rows (ctx {N}); 1 drafter layer x 16 rows; "
-                       f"2 LM-head rows x {Vs} vocab; scaled to {TS.n_layers}+{DS.n_layers} layers, {T} tree rows, "
-                       f"{T + 15} full LM-head rows, b=1 (sample wall {wall:.1f}s)"
+                       f"build B={B}; 1 target layer: projections on all {T} tree rows, ancestor-masked attention "
+                       f"on {rows} of them (ctx {N}, scaled to {T}); 1 drafter layer x 16 rows; {T + 15} LM-head "
+                       f"rows x {Vs} of the vocab (scaled to {TS.vocab}); scaled to {TS.n_layers}+{DS.n_layers} "
+                       f"layers, b=1 (sample wall {wall:.1f}s)"
                        + (f"; {target_label(a)} target: the sampled layer holds 16 of its {TS.n_experts} experts, "
                           f"each row runs its top {TS.top_k}" if TS.n_experts else "")),
             "est_s_per_step": est, "sample_wall_s": wall}
+
+
+def oracle_whole_step(a):
+    """One whole speculative step of the oracle at full size, timed on the host cores (no
+    extrapolation): full-width random weights (float32 storage, the oracle computes in
+    float64), a KV cache of `ctx` random keys, the drafter's context cache and nine pending
+    feature rows; then `oracle.step.spec_step` at budget B.  Needs about 45 GB of host
+    memory; refused (None) when less than three times that is available."""
+    import numpy as np
+
+    import synth
+    from oracle import step
+
+    TS, DS = shapes(a)
+    need = 4 * (TS.n_layers * layer_params(TS) + DS.n_layers * layer_params(DS) + TS.vocab * TS.d_model
+                + DS.d_model * TS.n_feat * TS.d_model) + 8 * 2 * (TS.n_layers + DS.n_layers) * 128 * 8 * (a.ctx + 512)
+    try:
+        avail = int(next(l for l in open("/proc/meminfo") if l.startswith("MemAvailable")).split()[1]) * 1024
+    except Exception:
+        avail = 0
+    if avail < 3 * need:
+        return None, f"needs {need / 1e9:.0f} GB of host memory, {avail / 1e9:.0f} GB available"
+    rng = np.random.default_rng(1008)
+    block = (rng.standard_normal(1 << 24, dtype=np.float32) * np.float32(0.02))
+
+    def w(*shape):  # random-looking float32 weights: a 16M-value block tiled (values do not matter)
+        return np.resize(block, shape)
+
+    def ones(n):
+        return np.ones(n, np.float32)
+
+    def layers(S, n):
+        d, nq, nkv, F = S.d_model, S.n_q_heads * S.head_dim, S.n_kv_heads * S.head_dim, S.d_ff
+        return [synth.LayerWeights(ones(d), w(nq + 2 * nkv, d), ones(128), ones(128), w(d, nq), ones(d),
+                                   w(2 * F, d), w(d, F)) for _ in range(n)]
+    t_build = time.perf_counter()
+    embed = w(TS.vocab, TS.d_model)
+    tw = synth.ModelWeights(TS, layers(TS, TS.n_layers), ones(TS.d_model), embed)
+    dw = synth.ModelWeights(DS, layers(DS, DS.n_layers), ones(DS.d_model), embed,
+                            fc=w(DS.d_model, TS.n_feat * TS.d_model), fc_norm=ones(DS.d_model))
+    cap, N = a.ctx + 512, a.ctx
+    cache = step.KVCache.empty(TS, cap)
+    ctx = step.KVCache.empty(DS, cap)
+    for kv in (cache, ctx):
+        for arr in kv.k + kv.v:
+            arr[:N] = rng.standard_normal((N,) + arr.shape[1:])
+    st = step.SeqState(cache, N, ctx, N, 11, rng.standard_normal((9, TS.n_feat * TS.d_model)))
+    t_build = time.perf_counter() - t_build
+    t0 = time.perf_counter()
+    tree, path = step.spec_step(tw, dw, st, a.budget)
+    wall = time.perf_counter() - t0
+    return {"wall_s": wall, "build_s": t_build, "accepted": len(path), "tree_nodes": len(tree["tok"]),
+            "host_bytes": need}, None
 
 
 def oracle_sample_threads(a, threads):
@@ -1212,6 +1285,30 @@ def main():
     if a.impl == "reference":
         if a.oracle_sample_json:
             print(json.dumps(oracle_sample(a)))
+            return
+        if a.whole_step:
+            if rank != 0:
+                return
+            if a.target != "qwen3-8b":
+                print(json.dumps({"impl": "reference", "unavailable": "the whole-step timing covers the dense target"}))
+                return
+            r, why = oracle_whole_step(a)
+            if r is None:
+                print(json.dumps({"impl": "reference", "unavailable": why}))
+                return
+            threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0) or (os.cpu_count() or 1)
+            v = 1.0 / r["wall_s"]
+            cpu = {"value": v, "unit": "spec steps/s", "cores": threads, "kind": "oracle", "nproc": os.cpu_count(),
+                   "sample": f"one whole oracle spec step at full size, timed (no extrapolation): {r['tree_nodes']} "
+                             f"tree rows, {a.ctx} cached keys, 36 + 5 layers, vocab 151936; weights built in "
+                             f"{r['build_s']:.0f} s (not timed)"}
+            print(json.dumps({"impl": "reference", "metric": metric_of(a), "value": v, "unit": "spec steps/s",
+                              "n_gpus": 1, "steps": 1, "warmup": 0, "ms_per_step": r["wall_s"] * 1e3,
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                              "data": "synthetic", "config": config(a, impl="reference"), "cpu_baseline": cpu,
+                              "whole_step": r,
+                              "e2e": {"value": v, "unit": "spec steps/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}))
             return
         if rank != 0:
             return
