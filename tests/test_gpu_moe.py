@@ -228,3 +228,41 @@ def test_moe_layer_at_qwen3_30b_a3b_width():
     assert clear.sum() >= 10
     want = model.moe_block(L, shape, hs[clear])
     rel_close(to_np(feat[0])[rows[clear]], want)
+
+
+def test_moe_prompt_pass_1024_rows():
+    # the prompt pass with a mixture-of-experts target: 1024 rows as one causal chain (the
+    # library masks the chain itself), 4096 routed rows, so the experts hold up to ~1000 rows
+    # each and the dispatch picks chunks; rows with clear routing against the oracle
+    shape = _shape(32, 4)
+    tw = synth.target_weights(shape, 9001)
+    tm = engine.DeviceModel.from_host(tw)
+    P, cap = 1024, 1088
+    prompt = synth.uniform_ints(9001, "moe.prompt", (1, P), 0, shape.vocab).astype(np.int32)
+    k_t = torch.zeros(1, 1, 2, cap, 128, dtype=torch.bfloat16, device="cuda")
+    v_t = torch.zeros(1, 1, 2, 128, cap, dtype=torch.bfloat16, device="cuda")
+    clen = torch.zeros(1, dtype=torch.int32, device="cuda")
+    choice = torch.zeros(1, P, dtype=torch.int32, device="cuda")
+    feat = torch.zeros(1, P, shape.d_model, dtype=torch.bfloat16, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, 1, P))
+    _lib.target_tree_forward(tm.cfg, tm.weights, torch.from_numpy(prompt).cuda(), None, None, k_t, v_t, clen, choice,
+                             feat, ws)
+    counts = torch.zeros(1, 32, dtype=torch.int32, device="cuda")
+    _lib.target_expert_counts(tm.cfg, 1, P, ws, counts)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert counts.cpu().numpy().sum() == P * 4
+    parent, depth = np.arange(-1, P - 1), np.arange(P)
+    L = tw.layers[0]
+    h = np.asarray(tw.embed, np.float64)[prompt[0]]
+    q, k_, v_ = model.qkv_rows(L, shape, model.rms_norm(h, L.attn_norm, shape.rms_eps))
+    q, k_ = model.qk_finish(L, shape, q, k_, depth)
+    c = step.KVCache.empty(shape, cap)
+    c.k[0][:P] = k_
+    c.v[0][:P] = v_
+    h = h + model.linear(verify.tree_attention(shape, q, c.k[0], c.v[0], 0, parent), L.w_o)
+    lg = np.sort(model.linear(model.rms_norm(h, L.mlp_norm, shape.rms_eps), L.w_router), axis=-1)[:, ::-1]
+    clear = (lg[:, 3] - lg[:, 4]) > 0.02
+    assert clear.mean() > 0.4
+    want = model.moe_block(L, shape, h[clear])
+    rel_close(to_np(feat[0])[clear], want)
