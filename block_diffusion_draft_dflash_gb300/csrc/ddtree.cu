@@ -68,6 +68,24 @@ DF_DEV uint32_t block_scan_incl(uint32_t v, uint32_t* warp_tmp) {
 
 // Whole-row radix top-K by one CTA of 1024 threads (also the fallback of the chunked
 // path when the threshold bin holds too many candidates, e.g. rows of equal values).
+// Block-wide bitonic sort, descending; n a power of two.  One thread per compared pair:
+// pair p joins element lo (p with a 0 inserted at the stride's bit) and lo + stride.
+DF_DEV void bitonic_desc(unsigned long long* a, int n) {
+  const int half = n >> 1;
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int p = threadIdx.x; p < half; p += blockDim.x) {
+        const int lo = ((p & ~(stride - 1)) << 1) | (p & (stride - 1));
+        const int hi = lo + stride;
+        const unsigned long long x = a[lo], y = a[hi];
+        const bool desc = (lo & size) == 0;
+        if (desc ? (x < y) : (x > y)) { a[lo] = y; a[hi] = x; }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 template <bool kVec4>
 DF_DEV void topk_row_full(const float* __restrict__ lp, size_t row, int V, int K, int32_t* __restrict__ out_id,
                           float* __restrict__ out_val, int* status) {
@@ -187,19 +205,7 @@ DF_DEV void topk_row_full(const float* __restrict__ lp, size_t row, int V, int K
   while (n < K) n <<= 1;
   for (int i = K + tid; i < n; i += kTopkThreads) sel[i] = 0ull;
   __syncthreads();
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < n; i += kTopkThreads) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const unsigned long long a = sel[i], b = sel[j];
-          const bool desc = (i & size) == 0;
-          if (desc ? (a < b) : (a > b)) { sel[i] = b; sel[j] = a; }
-        }
-      }
-      __syncthreads();
-    }
-  }
+  bitonic_desc(sel, n);
   for (int r = tid; r < K; r += kTopkThreads) {
     const unsigned long long c = sel[r];
     out_id[row * K + r] = (int32_t)(~(uint32_t)(c & 0xFFFFFFFFull));
@@ -231,6 +237,7 @@ constexpr int kChunk = 8192;          // keys per collect block
 constexpr int kChunkThreads = 512;
 constexpr int kSampleLines = 16;      // one line of 32 keys in 16 is sampled
 constexpr int kCapCand = 8192;        // candidates kept per row
+constexpr int kSampleU = 8;           // sampled lines a warp loads before counting them
 constexpr int kLocCand = 2048;        // candidates one collect block holds (more: the row falls back)
 
 struct TopkRow {     // per row, in the workspace
@@ -252,9 +259,17 @@ __global__ void __launch_bounds__(256) topk_sample_kernel(const float* __restric
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int n_lines = V / 32;
   int n_sample = 0;
-  for (int l = warp * kSampleLines; l < n_lines; l += nw * kSampleLines) {
-    const float f = __ldg(x + (size_t)l * 32 + lane);
-    if (!isnan(f)) atomicAdd(&hist[float_key(f) >> 20], 1u);
+  // the sampled lines' loads are issued kSampleU at a time (independent DRAM round trips)
+  for (int l0 = warp * kSampleLines; l0 < n_lines; l0 += nw * kSampleLines * kSampleU) {
+    float f[kSampleU];
+#pragma unroll
+    for (int u = 0; u < kSampleU; ++u) {
+      const int l = l0 + u * nw * kSampleLines;
+      f[u] = l < n_lines ? __ldg(x + (size_t)l * 32 + lane) : __int_as_float(0x7fc00000);  // NaN: skipped
+    }
+#pragma unroll
+    for (int u = 0; u < kSampleU; ++u)
+      if (!isnan(f[u])) atomicAdd(&hist[float_key(f[u]) >> 20], 1u);
   }
   n_sample = ((n_lines + kSampleLines - 1) / kSampleLines) * 32;
   __syncthreads();
@@ -302,10 +317,18 @@ __global__ void __launch_bounds__(256) topk_sample_kernel(const float* __restric
     __syncthreads();
     for (int i = threadIdx.x; i < 4096; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int l = warp * kSampleLines; l < n_lines; l += nw * kSampleLines) {
-      const float f = __ldg(x + (size_t)l * 32 + lane);
-      const uint32_t k = float_key(f);
-      if (!isnan(f) && (k >> 20) == hi_bin) atomicAdd(&hist[(k >> 8) & 0xFFF], 1u);
+    for (int l0 = warp * kSampleLines; l0 < n_lines; l0 += nw * kSampleLines * kSampleU) {
+      float f[kSampleU];
+#pragma unroll
+      for (int u = 0; u < kSampleU; ++u) {
+        const int l = l0 + u * nw * kSampleLines;
+        f[u] = l < n_lines ? __ldg(x + (size_t)l * 32 + lane) : __int_as_float(0x7fc00000);
+      }
+#pragma unroll
+      for (int u = 0; u < kSampleU; ++u) {
+        const uint32_t k = float_key(f[u]);
+        if (!isnan(f[u]) && (k >> 20) == hi_bin) atomicAdd(&hist[(k >> 8) & 0xFFF], 1u);
+      }
     }
     __syncthreads();
     const uint32_t r2 = r - above;  // >= 1: the bin holds the r-th sampled key
@@ -399,21 +422,6 @@ __global__ void __launch_bounds__(kChunkThreads) topk_collect_kernel(const float
       if (base + j < (uint32_t)kCapCand) cand[row * kCapCand + base + j] = loc[j];
 }
 
-DF_DEV void bitonic_desc(unsigned long long* a, int n) {  // n power of two, block-wide
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const unsigned long long x = a[i], y = a[j];
-          const bool desc = (i & size) == 0;
-          if (desc ? (x < y) : (x > y)) { a[i] = y; a[j] = x; }
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
 
 template <bool kVec4>
 __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(const float* __restrict__ lp, int V, int K,
