@@ -396,12 +396,20 @@ __global__ void __launch_bounds__(kChunkThreads) topk_collect_kernel(const float
     if (take && pos < (uint32_t)kLocCand) loc[pos] = ((unsigned long long)k << 32) | (uint32_t)(~(uint32_t)i);
   };
   if (kVec4) {
+    // every load of the chunk is issued before any is used: one DRAM round trip per block
+    constexpr int kPer = kChunk / 4 / kChunkThreads;
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    for (int b4 = i0 / 4; b4 < (i1 + 3) / 4; b4 += blockDim.x) {
-      const int q = b4 + threadIdx.x;
+    float4 f[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int q = i0 / 4 + u * kChunkThreads + threadIdx.x;
+      f[u] = q * 4 < i1 ? __ldg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int q = i0 / 4 + u * kChunkThreads + threadIdx.x;
       const bool ok = q * 4 < i1;
-      const float4 f = ok ? __ldg(x4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-      put(f.x, 4 * q, ok); put(f.y, 4 * q + 1, ok); put(f.z, 4 * q + 2, ok); put(f.w, 4 * q + 3, ok);
+      put(f[u].x, 4 * q, ok); put(f[u].y, 4 * q + 1, ok); put(f[u].z, 4 * q + 2, ok); put(f[u].w, 4 * q + 3, ok);
     }
   } else {
     for (int b = i0; b < i1; b += blockDim.x) {
