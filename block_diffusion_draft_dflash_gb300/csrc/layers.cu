@@ -220,18 +220,30 @@ __global__ void __launch_bounds__(1024) res_norm_kernel(ResNormArgs a) {
   const int per = blockDim.x * 4;
   float ss = 0.f;
   float* hrow = a.h ? a.h + (size_t)t * a.d : nullptr;
+  // every load first (the residual rows and both partial sums), the residual stores after:
+  // a store between them would keep the second element's loads behind the first's
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int n = i * per + threadIdx.x * 4;
-    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    v[i] = n < a.d ? partial_sum4(a.pv, n >> 7, t, n & 127) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float4 hv[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (hrow) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int n = i * per + threadIdx.x * 4;
+      if (n < a.d) hv[i] = *reinterpret_cast<const float4*>(hrow + n);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int n = i * per + threadIdx.x * 4;
     if (n >= a.d) continue;
-    float4 y = partial_sum4(a.pv, n >> 7, t, n & 127);
+    float4& y = v[i];
     if (hrow) {
-      const float4 hv = *reinterpret_cast<const float4*>(hrow + n);
-      y.x += hv.x; y.y += hv.y; y.z += hv.z; y.w += hv.w;
+      y.x += hv[i].x; y.y += hv[i].y; y.z += hv[i].z; y.w += hv[i].w;
       *reinterpret_cast<float4*>(hrow + n) = y;
     }
-    v[i] = y;
     ss += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
   }
   ss = warp_sum(ss);
