@@ -333,6 +333,27 @@ __global__ void __launch_bounds__(256) sub_lse_kernel(float* __restrict__ x, int
   const int r = blockIdx.x;
   const float l = lse[r];
   float* row = x + (size_t)r * V;
+  if ((V & 3) == 0) {
+    // float4s, four per thread loaded before any is written back (an in-place update would
+    // otherwise keep each load behind the previous store)
+    constexpr int U = 4;
+    const int V4 = V >> 2, chunk4 = (V4 + gridDim.y - 1) / gridDim.y;
+    const int q0 = blockIdx.y * chunk4, q1 = min(V4, q0 + chunk4);
+    float4* row4 = reinterpret_cast<float4*>(row);
+    for (int q = q0 + threadIdx.x; q < q1; q += blockDim.x * U) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (q + u * (int)blockDim.x < q1) v[u] = row4[q + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (q + u * (int)blockDim.x >= q1) continue;
+        v[u].x -= l; v[u].y -= l; v[u].z -= l; v[u].w -= l;
+        row4[q + u * blockDim.x] = v[u];
+      }
+    }
+    return;
+  }
   const int chunk = (V + gridDim.y - 1) / gridDim.y;
   const int i0 = blockIdx.y * chunk, i1 = min(V, i0 + chunk);
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) row[i] -= l;
