@@ -19,10 +19,10 @@
 //                V stored transposed in the cache so that its tile is K-major)
 // Warp roles: warps 0 .. 4 kCG - 1 softmax/epilogue (kCG warps per 32-row group, one per
 // 128/kCG-column group, exchanging row maxima through shared memory), then a Q/K TMA
-// producer warp, the TMEM owner + MMA issuer warp and a V TMA producer warp.  The single
-// MMA thread issues whichever product has its operands (S of a later block, or PV of the
-// oldest block whose P is written), S first, so neither a late K nor a late V tile holds
-// up the other product.
+// producer warp, the TMEM owner + MMA issuer warp and a V TMA producer warp.  The MMA warp
+// (in lockstep, one elected lane issuing) issues whichever product has its operands (S of a
+// later block, or PV of the oldest block whose P is written), S first, so neither a late K
+// nor a late V tile holds up the other product.
 // The key range of a sequence is split over CTAs (split-KV) when the grid would
 // otherwise not fill the GPU; partial (O, max, sum) are merged by attn_combine_kernel.
 #include "attention.h"
@@ -186,68 +186,86 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_wait(&fullb[j % NS], (j / NS) & 1, nullptr, 0);
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0 && nblk > 0) {
+    if (nblk > 0) {
       // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs the issue loop in lockstep (every decision is a warp vote), so
+      // the operand descriptors are warp-uniform values; one elected lane issues the MMAs
+      // and their commits.
       const uint32_t idesc = idesc_bf16_f32(128, 128);
       const uint32_t qa = smem_u32(q_smem);
-      bool ok = mbar_wait(q_full, 0, p.status, 12);
+      const bool leader = elect_one();
+      bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.status, 12));
       tc_fence_after();
       // operands already present: issue only
       auto issue_pv = [&](int j) {
         tc_fence_after();
         const uint32_t vb = smem_u32(v_smem + (j % kVStages) * kTileBytes);
         const uint32_t pt = tmem + (j % kSBufs) * 128;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // keys 16kk..16kk+15: P of column group 16kk / kCols
-          constexpr int kPer = kCols / 16;  // 16-key steps per column group
-          const uint32_t boff = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          mma_bf16_ts(tmem + kOCol, pt + (kk / kPer) * kCols + (kk % kPer) * 8, sdesc_kmajor_sw128(vb + boff), idesc,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {  // keys 16kk..16kk+15: P of column group 16kk / kCols
+            constexpr int kPer = kCols / 16;  // 16-key steps per column group
+            const uint32_t boff = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+            mma_bf16_ts(tmem + kOCol, pt + (kk / kPer) * kCols + (kk % kPer) * 8, sdesc_kmajor_sw128(vb + boff), idesc,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&o_done[j % kSBufs]);
+          mma_commit(&v_empty[j % kVStages]);
         }
-        mma_commit(&o_done[j % kSBufs]);
-        mma_commit(&v_empty[j % kVStages]);
+        __syncwarp();
       };
       auto issue_s = [&](int j) {
         tc_fence_after();
         const int st = j % kKStages;
         const uint32_t kb = smem_u32(k_smem + st * kTileBytes);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          mma_bf16(tmem + (j % kSBufs) * 128, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off), idesc,
-                   kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+            mma_bf16(tmem + (j % kSBufs) * 128, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off), idesc,
+                     kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[j % kSBufs]);
+          mma_commit(&k_empty[st]);
         }
-        mma_commit(&s_full[j % kSBufs]);
-        mma_commit(&k_empty[st]);
+        __syncwarp();
       };
       // Whichever product has its operands goes next, S first (its scores gate the next
       // softmax block), so a late K tile never holds up a ready PV or the other way round.
       // S_k reuses the buffer of block k - 3, so it waits until PV_{k-3} has been issued:
       // the tensor core runs one CTA's MMAs in issue order, so a buffer is rewritten only
       // after its P was read, and S_k complete implies every PV up to k - 3 complete.
+      // A barrier phase seen complete by any lane is complete, so each test is an any-vote.
       int s_next = 0, pv_next = 0, idle = 0;
-      uint64_t t_last = globaltimer();
+      uint64_t t_idle = 0;  // time of the first idle check since the last issue (0: none yet)
       const uint64_t limit = wait_limit(p.status);
       while (ok && pv_next < nblk) {
         if (s_next < nblk && s_next - pv_next < kSBufs &&
-            mbar_test_wait(&k_full[s_next % kKStages], (s_next / kKStages) & 1)) {
+            __any_sync(0xffffffffu, mbar_test_wait(&k_full[s_next % kKStages], (s_next / kKStages) & 1))) {
           issue_s(s_next++);
-        } else if (pv_next < s_next && mbar_test_wait(&p_full[pv_next % kSBufs], (pv_next / kSBufs) & 1) &&
-                   mbar_test_wait(&v_full[pv_next % kVStages], (pv_next / kVStages) & 1)) {
+        } else if (pv_next < s_next &&
+                   __any_sync(0xffffffffu, mbar_test_wait(&p_full[pv_next % kSBufs], (pv_next / kSBufs) & 1) &&
+                                               mbar_test_wait(&v_full[pv_next % kVStages], (pv_next / kVStages) & 1))) {
           issue_pv(pv_next++);
         } else {
           if ((++idle & 1023) == 0) {  // bounded: give up after the wait limit without progress
-            if (globaltimer() - t_last > limit) { set_status(p.status, DF_ERR_TIMEOUT, 13); ok = false; }
-            else if (p.status && *(volatile int*)p.status == DF_ERR_TIMEOUT) ok = false;
+            const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+            if (t_idle == 0) t_idle = now;
+            else if (now - t_idle > limit) {
+              if (leader) set_status(p.status, DF_ERR_TIMEOUT, 13);
+              ok = false;
+            }
+            if (__any_sync(0xffffffffu, p.status && *(volatile int*)p.status == DF_ERR_TIMEOUT)) ok = false;
           }
           continue;
         }
         idle = 0;
-        t_last = globaltimer();
+        t_idle = 0;
       }
       if (!ok && (s_next > 0 || pv_next > 0)) {
         // giving up: the MMAs already issued must finish before TMEM is freed
-        mma_commit(mma_drain);
+        if (leader) mma_commit(mma_drain);
+        __syncwarp();
         mbar_wait(mma_drain, 0, nullptr, 0);
       }
     }

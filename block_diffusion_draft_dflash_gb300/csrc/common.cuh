@@ -176,6 +176,14 @@ DF_DEV void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.ct
 DF_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// One lane of a converged warp (the lowest active one), chosen with a warp-uniform
+// predicate: MMAs issued under it keep their operand descriptors in warp-uniform values.
+DF_DEV bool elect_one() {
+  uint32_t r;
+  asm volatile("{\n .reg .b32 x;\n .reg .pred p;\n elect.sync x|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(r));
+  return r != 0;
+}
+
 DF_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 DF_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 

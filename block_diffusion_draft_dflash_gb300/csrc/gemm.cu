@@ -243,10 +243,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_wait(&full[st], ph, nullptr, 0);
       }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // The whole warp walks the stages in lockstep (every wait ends in a warp vote), so the
+    // operand descriptors are warp-uniform values; one elected lane issues the MMAs and
+    // their commits.
     const uint32_t idesc0 = idesc_bf16_f32(kBM, p.sub0);
     const uint32_t idesc1 = idesc_bf16_f32(kBM, p.sub1 ? p.sub1 : 16);
+    const bool leader = elect_one();
     int stage = 0;
     uint32_t phase = 0;
     long long it = it0;
@@ -254,36 +258,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int si = 0;
     // failure-path test hook: with the header's hold word set, issue no MMA and give up (the
     // producer then finds no stage released, times out and drains its loads)
-    bool ok = wait_hold_clear(p.status, 5), issued_any = false;
+    bool ok = __all_sync(0xffffffffu, !leader || wait_hold_clear(p.status, 5)), issued_any = false;
     while (ok && next_segment(p, it, it1, sg)) {
       const int acc = si % p.nbuf, use = si / p.nbuf;
-      if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 2)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 2))) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int k = sg.k0; k < sg.k1; ++k) {
-        if (!mbar_wait(&full[stage], phase, p.status, 3)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, p.status, 3))) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + (size_t)stage * stage_bytes);
         const uint64_t adesc = sdesc_kmajor_sw128(sa);
         const uint64_t bdesc = sdesc_kmajor_sw128(sa + w_bytes);
         const uint64_t bdesc1 = sdesc_kmajor_sw128(sa + w_bytes + p.sub0 * 128);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t accum = (k > sg.k0 || kk > 0) ? 1u : 0u;
-          mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc0, accum);
-          if (p.sub1) mma_bf16(d_tmem + p.sub0, adesc + 2 * kk, bdesc1 + 2 * kk, idesc1, accum);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t accum = (k > sg.k0 || kk > 0) ? 1u : 0u;
+            mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc0, accum);
+            if (p.sub1) mma_bf16(d_tmem + p.sub0, adesc + 2 * kk, bdesc1 + 2 * kk, idesc1, accum);
+          }
+          mma_commit(&empty[stage]);
         }
+        __syncwarp();
         issued_any = true;
-        mma_commit(&empty[stage]);
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      mma_commit(&tfull[acc]);
+      if (leader) mma_commit(&tfull[acc]);
+      __syncwarp();
       ++si;
     }
     if (issued_any && !ok) {
       // giving up: the MMAs already issued must finish before TMEM is freed
-      mma_commit(mma_drain);
+      if (leader) mma_commit(mma_drain);
+      __syncwarp();
       mbar_wait(mma_drain, 0, nullptr, 0);
     }
   } else if (warp >= 2) {

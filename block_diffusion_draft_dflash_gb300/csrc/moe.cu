@@ -317,8 +317,12 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
     // every load issued has landed before the CTA may exit (bounded waits)
     for (long long g = issued - S > released ? issued - S : released; g < issued; ++g)
       mbar_wait(&full[g % S], (uint32_t)((g / S) & 1), nullptr, 0);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // The whole warp walks the k-steps in lockstep (every wait ends in a warp vote), so the
+    // operand descriptors are warp-uniform values; one elected lane issues the MMAs and
+    // their commits.
+    const bool leader = elect_one();
     long long g = 0;  // k-steps consumed
     int si = 0;
     bool ok = true, issued_any = false;
@@ -326,28 +330,33 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
       const int4 ch = p.chunks[it / p.n_wt];
       const uint32_t idesc = idesc_bf16_f32(128, (ch.z + 15) & ~15);
       const int acc = si & 1, use = si >> 1;
-      if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 22)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], (use & 1) ^ 1, p.status, 22))) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * kMoeChunk;
       for (int k = 0; k < p.k_iters; ++k, ++g) {
         const int sl = (int)(g % S);
-        if (!mbar_wait(&full[sl], (uint32_t)((g / S) & 1), p.status, 23)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[sl], (uint32_t)((g / S) & 1), p.status, 23))) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + slot_off[sl]);
         const uint64_t adesc = sdesc_kmajor_sw128(sa), bdesc = sdesc_kmajor_sw128(sa + kMoeWBytes);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kMoeBK / 16; ++kk)
-          mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kMoeBK / 16; ++kk)
+            mma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[sl]);
+        }
+        __syncwarp();
         issued_any = true;
-        mma_commit(&empty[sl]);
       }
       if (!ok) break;
-      mma_commit(&tfull[acc]);
+      if (leader) mma_commit(&tfull[acc]);
+      __syncwarp();
       ++si;
     }
     if (issued_any && !ok) {
       // giving up: the MMAs already issued must finish before TMEM is freed
-      mma_commit(mma_drain);
+      if (leader) mma_commit(mma_drain);
+      __syncwarp();
       mbar_wait(mma_drain, 0, nullptr, 0);
     }
   } else if (warp >= 2) {
