@@ -402,7 +402,7 @@ def moe_expert_algorithmic(b, B, TS, active):
 # target tree forward (B=256): the four projection launches of one layer read + wrote
 # 53.14 (q/k/v), 35.72 (o), 210.23 (gate/up) and 108.79 (down) MB.  Valid only for the GEMM
 # code it was taken on (its hash below, comments aside); any other build reports traffic null.
-GEMM_TRAFFIC = {"src_sha256_16": "f9cb47b5d98e7364", "bytes_per_layer": 407834880,
+GEMM_TRAFFIC = {"src_sha256_16": "4322e08193df3b3e", "bytes_per_layer": 407568384,
                 "capture": "profiles/gemm_traffic_ncu_qwen3_8b_2layer_B256.md"}
 GEMM_SOURCES = ("gemm.cu", "common.cuh", "partials.cuh")
 

@@ -188,57 +188,71 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   long long it0, it1;
   cta_range(p, it0, it1);
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
+    // The whole warp walks the k-steps in lockstep (waits end in warp votes), one elected
+    // lane issuing the copies; the (weight tile, token tile, k) coordinates advance
+    // incrementally from the range's first k-step.
+    const bool leader = elect_one();
     const uint64_t pol_w = p.w_keep ? policy_evict_last() : policy_evict_first(), pol_x = policy_evict_last();
     const long long n = it1 - it0;
-    auto coords = [&](long long it, int& wt, int& tt, int& k) {
-      const long long tile = it / p.k_iters;
-      k = (int)(it - tile * p.k_iters);
-      wt = (int)(tile / p.n_ttiles);
-      tt = (int)(tile % p.n_ttiles);
+    struct Pos {
+      int wt, tt, k;
     };
-    auto load_x = [&](int st, int tt, int k) {
+    Pos pos0;
+    {
+      const long long tile = it0 / p.k_iters;
+      pos0.k = (int)(it0 - tile * p.k_iters);
+      pos0.wt = (int)(tile / p.n_ttiles);
+      pos0.tt = (int)(tile % p.n_ttiles);
+    }
+    auto advance = [&](Pos& q) {
+      if (++q.k == p.k_iters) {
+        q.k = 0;
+        if (++q.tt == p.n_ttiles) { q.tt = 0; ++q.wt; }
+      }
+    };
+    auto load_x = [&](int st, const Pos& q) {
       unsigned char* xb = smem + (size_t)st * stage_bytes + w_bytes;
-      tma_load_2d(xb, &tmX, &full[st], k * kBK, tt * BN, pol_x);
-      if (p.sub1) tma_load_2d(xb + p.sub0 * 128, &tmX1, &full[st], k * kBK, tt * BN + p.sub0, pol_x);
+      tma_load_2d(xb, &tmX, &full[st], q.k * kBK, q.tt * BN, pol_x);
+      if (p.sub1) tma_load_2d(xb + p.sub0 * 128, &tmX1, &full[st], q.k * kBK, q.tt * BN + p.sub0, pol_x);
     };
     // Weights are constant: the first ring's worth of weight tiles is requested before the
     // previous kernel has finished.  Each stage's transaction count covers both halves, so
     // it completes only once its token rows (loaded after the wait) have arrived too.
     const int npre = (int)(n < S ? n : S);
-    for (int i = 0; i < npre; ++i) {
-      int wt, tt, k;
-      coords(it0 + i, wt, tt, k);
-      mbar_arrive_expect_tx(&full[i], stage_bytes);
-      tma_load_2d(smem + (size_t)i * stage_bytes, &tmW, &full[i], k * kBK, wt * kBM, pol_w);
+    Pos q = pos0;
+    for (int i = 0; i < npre; ++i, advance(q)) {
+      if (leader) {
+        mbar_arrive_expect_tx(&full[i], stage_bytes);
+        tma_load_2d(smem + (size_t)i * stage_bytes, &tmW, &full[i], q.k * kBK, q.wt * kBM, pol_w);
+      }
     }
     pdl_wait();  // token rows are the previous kernel's output
-    for (int i = 0; i < npre; ++i) {
-      int wt, tt, k;
-      coords(it0 + i, wt, tt, k);
-      load_x(i, tt, k);
-    }
+    q = pos0;
+    for (int i = 0; i < npre; ++i, advance(q))
+      if (leader) load_x(i, q);
     int stage = npre % S;
     uint32_t phase = npre == S ? 1u : 0u;
     long long issued = npre;
-    for (long long i = npre; i < n; ++i) {
-      if (!mbar_wait(&empty[stage], phase ^ 1, p.status, 1)) break;
-      int wt, tt, k;
-      coords(it0 + i, wt, tt, k);
-      mbar_arrive_expect_tx(&full[stage], stage_bytes);
-      tma_load_2d(smem + (size_t)stage * stage_bytes, &tmW, &full[stage], k * kBK, wt * kBM, pol_w);
-      load_x(stage, tt, k);
+    for (long long i = npre; i < n; ++i, advance(q)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, p.status, 1))) break;
+      if (leader) {
+        mbar_arrive_expect_tx(&full[stage], stage_bytes);
+        tma_load_2d(smem + (size_t)stage * stage_bytes, &tmW, &full[stage], q.k * kBK, q.wt * kBM, pol_w);
+        load_x(stage, q);
+      }
+      __syncwarp();
       ++issued;
       if (++stage == S) { stage = 0; phase ^= 1; }
     }
-    {
+    if (leader) {
       // Drain: every load issued must have landed before the CTA may exit, also when the MMA
       // issuer gave up before consuming it (bounded waits; already complete in normal runs).
-      const long long n = issued < S ? issued : S;
+      const long long m = issued < S ? issued : S;
       int st = stage;
       uint32_t ph = phase;
-      for (long long i = 0; i < n; ++i) {
+      for (long long i = 0; i < m; ++i) {
         if (--st < 0) { st = S - 1; ph ^= 1; }
         mbar_wait(&full[st], ph, nullptr, 0);
       }

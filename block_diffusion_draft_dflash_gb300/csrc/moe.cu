@@ -273,8 +273,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
   pdl_trigger();
   const int n_items = *p.n_chunks * p.n_wt;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
+    // The whole warp keeps the ring's books in lockstep (waits end in warp votes), one
+    // elected lane issuing the copies.
+    const bool leader = elect_one();
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
     uint32_t head = 0, used = 0;  // next free byte of the ring; bytes held by k-steps in flight
     uint32_t held[S];             // bytes each slot holds (a wrapped k-step also holds the skipped tail)
@@ -290,33 +293,37 @@ __global__ void __launch_bounds__(kMoeThreads, 1)
         // the oldest k-steps give their bytes back until this one fits and a slot is free
         while (used + take > kMoeRing || issued - released == S) {
           const int so = (int)(released % S);
-          if (!mbar_wait(&empty[so], (uint32_t)((released / S) & 1), p.status, 21)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty[so], (uint32_t)((released / S) & 1), p.status, 21))) { ok = false; break; }
           used -= held[so];
           ++released;
         }
         if (!ok) break;
         const int sl = (int)(issued % S);
         held[sl] = take;
-        slot_off[sl] = start;
         used += take;
         head = start + need;
-        unsigned char* sb = smem + start;
-        mbar_arrive_expect_tx(&full[sl], need);
-        if (MODE == kMoeGateUp) {
-          const int g0 = ch.x * 2 * p.Fe + wt * 64;  // 64 gate rows, then the matching 64 up rows
-          tma_load_2d(sb, &tmW, &full[sl], k * kMoeBK, g0, pol_w);
-          tma_load_2d(sb + kMoeWBytes / 2, &tmW, &full[sl], k * kMoeBK, g0 + p.Fe, pol_w);
-        } else {
-          tma_load_2d(sb, &tmW, &full[sl], k * kMoeBK, ch.x * p.d + wt * 128, pol_w);
+        if (leader) {
+          slot_off[sl] = start;
+          unsigned char* sb = smem + start;
+          mbar_arrive_expect_tx(&full[sl], need);
+          if (MODE == kMoeGateUp) {
+            const int g0 = ch.x * 2 * p.Fe + wt * 64;  // 64 gate rows, then the matching 64 up rows
+            tma_load_2d(sb, &tmW, &full[sl], k * kMoeBK, g0, pol_w);
+            tma_load_2d(sb + kMoeWBytes / 2, &tmW, &full[sl], k * kMoeBK, g0 + p.Fe, pol_w);
+          } else {
+            tma_load_2d(sb, &tmW, &full[sl], k * kMoeBK, ch.x * p.d + wt * 128, pol_w);
+          }
+          for (int j = 0; j < nbox; ++j)
+            tma_load_2d(sb + kMoeWBytes + j * kMoeXBox, &tmX, &full[sl], k * kMoeBK, ch.y + 64 * j, pol_x);
         }
-        for (int j = 0; j < nbox; ++j)
-          tma_load_2d(sb + kMoeWBytes + j * kMoeXBox, &tmX, &full[sl], k * kMoeBK, ch.y + 64 * j, pol_x);
+        __syncwarp();
         ++issued;
       }
     }
     // every load issued has landed before the CTA may exit (bounded waits)
-    for (long long g = issued - S > released ? issued - S : released; g < issued; ++g)
-      mbar_wait(&full[g % S], (uint32_t)((g / S) & 1), nullptr, 0);
+    if (leader)
+      for (long long g = issued - S > released ? issued - S : released; g < issued; ++g)
+        mbar_wait(&full[g % S], (uint32_t)((g / S) & 1), nullptr, 0);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // The whole warp walks the k-steps in lockstep (every wait ends in a warp vote), so the
