@@ -39,11 +39,13 @@ class KVCache:
         return KVCache([z() for _ in range(shape.n_layers)], [z() for _ in range(shape.n_layers)])
 
 
-def target_tree_forward(tw, tok, parent, depth, cache: KVCache, N):
+def target_tree_forward(tw, tok, parent, depth, cache: KVCache, N, choose=None):
     """Target forward over a flattened tree (or one token, or a chain).
 
     Writes node i's K/V to slot N + i of every layer, attends ancestor-only, and returns
-    (greedy choice per node, feature rows [T, n_feat*d], logits [T, V]).
+    (choice per node, feature rows [T, n_feat*d], logits [T, V]).  The choice is the greedy
+    one (argmax, lowest id on ties), or choose(logits, positions) with the absolute
+    position N + depth + 1 of the token each node predicts (sampling, see sample.py).
     """
     shape = tw.shape
     tok = np.asarray(tok)
@@ -63,7 +65,8 @@ def target_tree_forward(tw, tok, parent, depth, cache: KVCache, N):
         if li + 1 in shape.feat_layers:
             feats.append(h.copy())
     logits = model.lm_head(tw, h)
-    return model.argmax_lowest(logits), np.concatenate(feats, axis=-1), logits
+    choice = model.argmax_lowest(logits) if choose is None else choose(logits, pos + 1)
+    return choice, np.concatenate(feats, axis=-1), logits
 
 
 def fuse_context(dw, feat):
@@ -117,24 +120,25 @@ class SeqState:
     out: list = field(default_factory=list)
 
 
-def prefill(tw, dw, prompt, cap):
+def prefill(tw, dw, prompt, cap, choose=None):
     """Causal prompt pass, one token at a time; yields the first bonus token and the features."""
     cache = KVCache.empty(tw.shape, cap)
     feats = []
     choice = None
     for i, t in enumerate(prompt):
-        ch, f, _ = target_tree_forward(tw, [t], [-1], [0], cache, i)
+        ch, f, _ = target_tree_forward(tw, [t], [-1], [0], cache, i, choose)
         feats.append(f[0])
         choice = int(ch[0])
     ctx = KVCache.empty(dw.shape, cap) if dw is not None else None
     return SeqState(cache, len(prompt), ctx, 0, choice, np.array(feats), [choice])
 
 
-def spec_step(tw, dw, st: SeqState, B, plant=None):
+def spec_step(tw, dw, st: SeqState, B, plant=None, choose=None):
     """Draft -> DDTree -> verify -> accept -> compact.  Returns (tree, path).
 
     plant(st, logits) -> logits may bias the drafter's logits before the log-softmax
     (test harness only: random-init drafters rarely agree with random-init targets).
+    choose: the target's choice per node (greedy when None; see target_tree_forward).
     """
     lp, st.ctx_len, logits = draft_block(dw, st.feat, st.ctx, st.ctx_len, st.bonus)
     if plant is not None:
@@ -142,7 +146,7 @@ def spec_step(tw, dw, st: SeqState, B, plant=None):
     tree = ddtree.build_tree(lp, B)
     tok = tree["tok"].copy()
     tok[0] = st.bonus
-    choice, feats, _ = target_tree_forward(tw, tok, tree["parent"], tree["depth"], st.cache, st.N)
+    choice, feats, _ = target_tree_forward(tw, tok, tree["parent"], tree["depth"], st.cache, st.N, choose)
     path, new_bonus = verify.greedy_walk(choice, tok, tree["parent"])
     for li in range(tw.shape.n_layers):
         verify.compact(st.cache.k[li], st.N, path)
@@ -154,19 +158,20 @@ def spec_step(tw, dw, st: SeqState, B, plant=None):
     return tree, path
 
 
-def spec_generate(tw, dw, prompt, n_new, B, cap, plant=None):
-    st = prefill(tw, dw, prompt, cap)
+def spec_generate(tw, dw, prompt, n_new, B, cap, plant=None, choose=None):
+    st = prefill(tw, dw, prompt, cap, choose)
     steps = []
     while len(st.out) < n_new:
-        _, path = spec_step(tw, dw, st, B, plant)
+        _, path = spec_step(tw, dw, st, B, plant, choose)
         steps.append(len(path))
     return st.out[:n_new], steps
 
 
-def greedy_generate(tw, prompt, n_new, cap):
-    st = prefill(tw, None, prompt, cap)
+def greedy_generate(tw, prompt, n_new, cap, choose=None):
+    """Plain decoding, one target forward per token (greedy, or drawing with choose)."""
+    st = prefill(tw, None, prompt, cap, choose)
     while len(st.out) < n_new:
-        ch, _, _ = target_tree_forward(tw, [st.bonus], [-1], [0], st.cache, st.N)
+        ch, _, _ = target_tree_forward(tw, [st.bonus], [-1], [0], st.cache, st.N, choose)
         st.N += 1
         st.bonus = int(ch[0])
         st.out.append(st.bonus)
