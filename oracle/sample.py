@@ -49,11 +49,12 @@ def row_seed(seed: int, s: int, n: int) -> np.uint32:
 
 
 def uniforms(seed: int, s: int, n: int, V: int) -> np.ndarray:
-    """u_v in (0, 1) for v < V, float32 (24 random bits + 1/2, scaled: exact in float32)."""
+    """u_v for v < V, float32: (23 random bits + 1/2) / 2^23, exact in float32 and inside
+    [2^-24, 1 - 2^-24], so neither logarithm of the Gumbel transform meets 0 or 1."""
     r = np.uint64(row_seed(seed, s, n))
     v = np.arange(V, dtype=np.uint64)
     h = fmix32(r ^ ((v * C_TOK) & 0xFFFFFFFF))
-    return ((h >> 8).astype(np.float32) + np.float32(0.5)) * np.float32(1.0 / 16777216.0)
+    return ((h >> 9).astype(np.float32) + np.float32(0.5)) * np.float32(1.0 / 8388608.0)
 
 
 def gumbel(seed: int, s: int, n: int, V: int) -> np.ndarray:
