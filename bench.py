@@ -65,6 +65,10 @@ def parse():
                          "Qwen3-Coder-30B-A3B-shaped one (48 layers, 128 experts, 8 per token)")
     ap.add_argument("--draft-mode", default="tree", choices=["tree", "chain"],
                     help="tree: DDTree of B nodes; chain: vanilla DFlash (argmax chain of 15)")
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="verification at this temperature: the target draws its token after every node "
+                         "(keyed to a seed, the sequence and the position) and the walk follows the draws; "
+                         "0: greedy")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample-json", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--whole-step", action="store_true",
@@ -112,7 +116,8 @@ def workload_name(a):
     return (f"DFlash+DDTree spec step, {target_label(a)}-shaped target ({TS.n_layers}L{moe}) + {DS.n_layers}L "
             f"drafter, block 16, {draft}, ctx {a.ctx}, b={a.batch}, acceptance planted at {a.accept_rate}"
             + (f" (near misses elsewhere: the target's token second at bias {a.plant_miss_bias:g})"
-               if getattr(a, "plant_miss_bias", 0) else ""))
+               if getattr(a, "plant_miss_bias", 0) else "")
+            + (f", verification at temperature {a.temperature:g}" if getattr(a, "temperature", 0) else ""))
 
 
 def config(a, impl="gb300"):
@@ -124,7 +129,8 @@ def config(a, impl="gb300"):
     gb = 2 * (TS.n_layers * layer_params(TS) + DS.n_layers * layer_params(DS) + TS.vocab * TS.d_model) / 1e9
     cfg = {"workload": workload_name(a), "global_batch": a.batch * a.gpus, "block": 16,
            "budget": a.budget if a.draft_mode == "tree" else 15, "draft_mode": a.draft_mode,
-           "accept_rate": a.accept_rate, "ctx": a.ctx, "target_layers": TS.n_layers,
+           "accept_rate": a.accept_rate, "ctx": a.ctx, "temperature": getattr(a, "temperature", 0.0),
+           "target_layers": TS.n_layers,
            "drafter_layers": DS.n_layers, "vocab": TS.vocab,
            "l2": f"inputs larger than L2 (about {gb:.0f} GB of weights streamed per step)",
            "timing": timing, "parallelism": f"replicas x{a.gpus}"}
@@ -402,7 +408,7 @@ def moe_expert_algorithmic(b, B, TS, active):
 # target tree forward (B=256): the four projection launches of one layer read + wrote
 # 53.14 (q/k/v), 35.72 (o), 210.23 (gate/up) and 108.79 (down) MB.  Valid only for the GEMM
 # code it was taken on (its hash below, comments aside); any other build reports traffic null.
-GEMM_TRAFFIC = {"src_sha256_16": "4322e08193df3b3e", "bytes_per_layer": 407568384,
+GEMM_TRAFFIC = {"src_sha256_16": "e817aa4591aa5466", "bytes_per_layer": 407864576,
                 "capture": "profiles/gemm_traffic_ncu_qwen3_8b_2layer_B256.md"}
 GEMM_SOURCES = ("gemm.cu", "common.cuh", "partials.cuh")
 
@@ -545,7 +551,7 @@ def lookahead_table(dec, n_steps, table, dev, max_fix=6):
         pos = dec.cache_len.long()
         for d in range(D):
             _lib.target_tree_forward(dec.t.cfg, dec.t.weights, tok, depth, anc, dec.k_cache, dec.v_cache, clen, ch,
-                                     None, ws)
+                                     None, ws, dec.temperature, dec.seed)
             for s_, f in enumerate(forced):
                 if d in f:
                     ch[s_, 0] = f[d]
@@ -622,7 +628,8 @@ def run_gpu(a, rank, world, local_rank):
     b, N = a.batch, a.ctx
     n_steps = 1 + a.warmup + 2 + 2 * a.steps + 3
     cap = ((N + (a.budget + 1) + 16 * (n_steps + 2) + 64) + 127) // 128 * 128
-    dec = engine.SpecDecoder(tm, dm, b, a.budget, cap, prompt_len=N, device=dev, mode=a.draft_mode)
+    dec = engine.SpecDecoder(tm, dm, b, a.budget, cap, prompt_len=N, device=dev, mode=a.draft_mode,
+                             temperature=a.temperature, seed=20261)
     B, T = dec.B, dec.T
     prompt = torch.from_numpy(synth.uniform_ints(seed, "prompt", (b, N), 0, TS.vocab)).to(dev)
     ref = None

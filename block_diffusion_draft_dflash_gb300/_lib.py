@@ -66,12 +66,18 @@ _SIGS = {
     "dflash_target_tree_forward_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
     "dflash_target_tree_forward": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int] + [C.c_void_p] * 5 +
                                    [C.c_int] + [C.c_void_p] * 4 + [C.c_size_t, C.c_void_p]),
+    "dflash_target_tree_forward_sampled": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int] + [C.c_void_p] * 5 +
+                                           [C.c_int, C.c_void_p, C.c_float, C.c_ulonglong] + [C.c_void_p] * 3 +
+                                           [C.c_size_t, C.c_void_p]),
     "dflash_target_expert_counts": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p,
                                               C.c_void_p]),
     "dflash_linear_workspace_size": (C.c_size_t, []),
     "dflash_linear_argmax_workspace_size": (C.c_size_t, [C.c_int]),
     "dflash_linear_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                        C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dflash_linear_sample_workspace_size": (C.c_size_t, [C.c_int]),
+    "dflash_linear_sample": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_float, C.c_ulonglong,
+                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_linear": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int,
                       C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_linear_logsoftmax_workspace_size": (C.c_size_t, [C.c_int, C.c_int]),
@@ -245,9 +251,17 @@ def target_tree_forward_workspace_size(cfg: ModelCfg, b, n_tree):
 
 
 def target_tree_forward(cfg: ModelCfg, weights: ModelWeights, tok, depth, anc, k_cache, v_cache, cache_len, choice,
-                        tree_feat, ws: Workspace):
+                        tree_feat, ws: Workspace, temperature: float = 0.0, seed: int = 0):
+    """temperature 0: the greedy choice per node; > 0: the target's temperature draw per node
+    (dflash_target_tree_forward_sampled, keyed to seed, sequence and position)."""
     b, T = tok.shape
     cap = k_cache.shape[3]
+    if temperature > 0:
+        _check("dflash_target_tree_forward_sampled", load().dflash_target_tree_forward_sampled(
+            C.byref(cfg), C.byref(weights), b, T, _p(tok), _p(depth), _p(anc), _p(k_cache), _p(v_cache), cap,
+            _p(cache_len), float(temperature), seed & 0xFFFFFFFFFFFFFFFF, _p(choice), _p(tree_feat), ws.ptr,
+            ws.nbytes, _stream()))
+        return
     _check("dflash_target_tree_forward", load().dflash_target_tree_forward(
         C.byref(cfg), C.byref(weights), b, T, _p(tok), _p(depth), _p(anc), _p(k_cache), _p(v_cache), cap,
         _p(cache_len), _p(choice), _p(tree_feat), ws.ptr, ws.nbytes, _stream()))
@@ -297,6 +311,22 @@ def linear_argmax(X, W, out, ws: Workspace = None):
     ws = ws or Workspace(load().dflash_linear_argmax_workspace_size(M), X.device)
     _check("dflash_linear_argmax", load().dflash_linear_argmax(_p(X), _p(W), M, N, K, _p(out), ws.ptr, ws.nbytes,
                                                                _stream()))
+    return ws
+
+
+def linear_sample(X, W, temperature, seed, row_seq, row_pos, out, ws: Workspace = None):
+    """out[t] = the temperature draw of row t from softmax((X W^T)[t] / T), keyed to
+    (seed, row_seq[t], row_pos[t]); X [M][K] bf16, W [N][K] bf16, row_seq/row_pos/out [M] int32."""
+    _dev(X, torch.bfloat16, "X")
+    _dev(W, torch.bfloat16, "W")
+    for t, name in ((row_seq, "row_seq"), (row_pos, "row_pos"), (out, "out")):
+        _dev(t, torch.int32, name)
+    M, K = X.shape
+    N = W.shape[0]
+    ws = ws or Workspace(load().dflash_linear_sample_workspace_size(M), X.device)
+    _check("dflash_linear_sample", load().dflash_linear_sample(
+        _p(X), _p(W), M, N, K, float(temperature), seed & 0xFFFFFFFFFFFFFFFF, _p(row_seq), _p(row_pos), _p(out),
+        ws.ptr, ws.nbytes, _stream()))
     return ws
 
 

@@ -3,6 +3,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <cmath>
 #include <vector>
 
 #include "attention.h"
@@ -183,6 +184,7 @@ int run_layer(const LayerRun& L, LayerBufs& B, cudaStream_t st) {
 struct TargetWs {
   LayerBufs B;
   unsigned long long* amax;
+  uint32_t* draw_key;  // per-row keys of the LM head's temperature draw
 };
 size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs* out) {
   const int d = c->d_model, Hq = c->n_q_heads, Hkv = c->n_kv_heads, F = c->d_ff;
@@ -196,6 +198,7 @@ size_t target_ws(const df_model_cfg* c, int b, int n_tree, void* base, TargetWs*
   w.B.act = cv.take<df_bf16>(R * (c->n_experts > 0 ? 1 : F));
   w.B.part = cv.take<float>(layer_partial_bytes(c, (int)R, (int)R) / 4 + 1);
   w.amax = cv.take<unsigned long long>(R);
+  w.draw_key = cv.take<uint32_t>(R);
   if (c->n_experts > 0) {
     size_t sz[kMoeBufCount];
     moe_buf_elems((int)R, c->top_k, c->n_experts, d, c->d_expert, sz);
@@ -470,11 +473,12 @@ int dflash_target_expert_counts(const df_model_cfg* c, int b, int n_tree, const 
              : DF_ERR_CUDA;
 }
 
-int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w, int b, int n_tree, const int32_t* tok,
-                               const int32_t* depth, const uint32_t* anc, df_bf16* k_cache, df_bf16* v_cache, int cap,
-                               const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat, void* ws,
-                               size_t ws_bytes, df_stream stream) {
-  DF_NVTX("dflash_target_tree_forward");
+// The target's forward over the flattened tree; the choice per node is the argmax
+// (temperature 0) or a temperature draw keyed to (seed, sequence, position).
+static int target_forward_run(const df_model_cfg* c, const df_model_weights* w, int b, int n_tree, const int32_t* tok,
+                              const int32_t* depth, const uint32_t* anc, df_bf16* k_cache, df_bf16* v_cache, int cap,
+                              const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat, void* ws,
+                              size_t ws_bytes, float temperature, uint64_t seed, cudaStream_t st) {
   if (!cfg_ok(c)) return DF_ERR_SHAPE;
   if (!w || !w->layers || !w->embed || !w->final_norm || b < 0 || n_tree < 1 || cap <= 0) return DF_ERR_ARG;
   DF_TRY(layers_ok(c, w));
@@ -484,7 +488,6 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
   if ((depth == nullptr) != (anc == nullptr)) return DF_ERR_ARG;  // both NULL: a causal chain
   if (!al16(k_cache) || !al16(v_cache) || (anc && !al16(anc)) || (tree_feat && !al16(tree_feat))) return DF_ERR_ALIGN;
   if (!ws || ws_bytes < dflash_target_tree_forward_workspace_size(c, b, n_tree)) return DF_ERR_WORKSPACE;
-  cudaStream_t st = (cudaStream_t)stream;
   TargetWs W;
   target_ws(c, b, n_tree, ws, &W);
   int* status = status_of(ws);
@@ -529,8 +532,33 @@ int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w,
   GemmDesc g{};
   g.X = W.B.x; g.W = w->embed; g.M = R; g.N = c->vocab; g.K = d; g.ldx = d; g.ldw = d;
   g.mode = kGemmArgmax; g.amax = W.amax; g.status = status;
+  if (temperature > 0.f) {
+    DF_TRY(launch_draw_keys(R, seed, nullptr, nullptr, n_tree, cache_len, depth, W.draw_key, st));
+    g.draw_key = W.draw_key;
+    g.inv_temp = (float)(1.0 / (double)temperature);
+  }
   DF_TRY(launch_gemm(g, st));
   return launch_argmax_finalize(W.amax, R, choice, st);
+}
+
+int dflash_target_tree_forward(const df_model_cfg* c, const df_model_weights* w, int b, int n_tree, const int32_t* tok,
+                               const int32_t* depth, const uint32_t* anc, df_bf16* k_cache, df_bf16* v_cache, int cap,
+                               const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat, void* ws,
+                               size_t ws_bytes, df_stream stream) {
+  DF_NVTX("dflash_target_tree_forward");
+  return target_forward_run(c, w, b, n_tree, tok, depth, anc, k_cache, v_cache, cap, cache_len, choice, tree_feat, ws,
+                            ws_bytes, 0.f, 0, (cudaStream_t)stream);
+}
+
+int dflash_target_tree_forward_sampled(const df_model_cfg* c, const df_model_weights* w, int b, int n_tree,
+                                       const int32_t* tok, const int32_t* depth, const uint32_t* anc,
+                                       df_bf16* k_cache, df_bf16* v_cache, int cap, const int32_t* cache_len,
+                                       float temperature, uint64_t seed, int32_t* choice, df_bf16* tree_feat,
+                                       void* ws, size_t ws_bytes, df_stream stream) {
+  DF_NVTX("dflash_target_tree_forward_sampled");
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return DF_ERR_ARG;
+  return target_forward_run(c, w, b, n_tree, tok, depth, anc, k_cache, v_cache, cap, cache_len, choice, tree_feat, ws,
+                            ws_bytes, temperature, seed, (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------------ draft block
@@ -643,6 +671,37 @@ int dflash_linear_argmax(const df_bf16* X, const df_bf16* W, int M, int N, int K
   GemmDesc g{};
   g.X = X; g.W = W; g.M = M; g.N = N; g.K = K; g.ldx = K; g.ldw = K;
   g.mode = kGemmArgmax; g.amax = keys; g.status = status_of(ws);
+  DF_TRY(launch_gemm(g, st));
+  return launch_argmax_finalize(keys, M, out, st);
+}
+
+size_t dflash_linear_sample_workspace_size(int M) {
+  Carver cv(nullptr);
+  cv.take<unsigned long long>(M > 0 ? (size_t)M : 1);
+  cv.take<uint32_t>(M > 0 ? (size_t)M : 1);
+  return cv.off;
+}
+
+int dflash_linear_sample(const df_bf16* X, const df_bf16* W, int M, int N, int K, float temperature, uint64_t seed,
+                         const int32_t* row_seq, const int32_t* row_pos, int32_t* out, void* ws, size_t ws_bytes,
+                         df_stream stream) {
+  DF_NVTX("dflash_linear_sample");
+  if (M < 0 || N <= 0 || K <= 0 || !(temperature > 0.f) || !std::isfinite(temperature)) return DF_ERR_ARG;
+  if (K % 64) return DF_ERR_SHAPE;
+  if (M == 0) return DF_OK;
+  if (!X || !W || !out || !row_seq || !row_pos) return DF_ERR_ARG;
+  if (!al16(X) || !al16(W)) return DF_ERR_ALIGN;
+  if (!ws || ws_bytes < dflash_linear_sample_workspace_size(M)) return DF_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  Carver cv(ws);
+  unsigned long long* keys = cv.take<unsigned long long>((size_t)M);
+  uint32_t* dkeys = cv.take<uint32_t>((size_t)M);
+  if (cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * M, st) != cudaSuccess) return DF_ERR_CUDA;
+  DF_TRY(launch_draw_keys(M, seed, row_seq, row_pos, 0, nullptr, nullptr, dkeys, st));
+  GemmDesc g{};
+  g.X = X; g.W = W; g.M = M; g.N = N; g.K = K; g.ldx = K; g.ldw = K;
+  g.mode = kGemmArgmax; g.amax = keys; g.status = status_of(ws);
+  g.draw_key = dkeys; g.inv_temp = (float)(1.0 / (double)temperature);
   DF_TRY(launch_gemm(g, st));
   return launch_argmax_finalize(keys, M, out, st);
 }

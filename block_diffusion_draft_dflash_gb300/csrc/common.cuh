@@ -15,6 +15,7 @@
 #include "../../include/dflash.h"
 
 #define DF_DEV __device__ __forceinline__
+#define DF_HD __host__ __device__ __forceinline__
 
 namespace df {
 
@@ -310,6 +311,35 @@ DF_DEV float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); 
 DF_DEV uint16_t f_to_bf16(float f) {  // round to nearest even
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// --------------------------------------------------------------------------- drawing tokens
+// Temperature-T draws of the target's token are Gumbel-max: argmax_v (logit_v / T + g_v),
+// g_v = -log(-log u_v), with u_v from a counter-based generator keyed to (seed, sequence,
+// position of the drawn token, v): the 32-bit finalizer of MurmurHash3 (A. Appleby, public
+// domain) applied in a fixed chain.  Keying to the absolute position makes speculative
+// decoding reproduce plain sampling under the same seed.
+DF_HD uint32_t fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85EBCA6Bu;
+  h ^= h >> 13;
+  h *= 0xC2B2AE35u;
+  h ^= h >> 16;
+  return h;
+}
+// Key of the draw for sequence s at absolute position n.
+DF_HD uint32_t draw_key(uint64_t seed, int s, int n) {
+  uint32_t a = fmix32((uint32_t)seed ^ (0x9E3779B9u * (uint32_t)(s + 1)));
+  a = fmix32(a ^ (uint32_t)(seed >> 32));
+  return fmix32(a + 0xC2B2AE35u * (uint32_t)n);
+}
+// g_v of token v for the draw keyed by k; u = (23 random bits + 1/2) / 2^23, exact in fp32
+// and inside [2^-24, 1 - 2^-24].  The inner logarithm is the accurate one: for u near 1,
+// -log u is tiny and an approximate logarithm's absolute error would dominate it.
+DF_DEV float draw_noise(uint32_t k, int v) {
+  const uint32_t h = fmix32(k ^ ((uint32_t)v * 0x27D4EB2Fu));
+  const float u = ((float)(h >> 9) + 0.5f) * (1.f / 8388608.f);
+  return -__logf(-logf(u));
 }
 
 }  // namespace df

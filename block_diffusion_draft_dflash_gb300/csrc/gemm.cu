@@ -58,6 +58,8 @@ struct GemmParams {
   float* out;
   int ldo;
   unsigned long long* amax;  // argmax keys [M]
+  const uint32_t* draw_key;  // argmax: per-token draw keys, or NULL (greedy)
+  float inv_temp;
   float* part;               // kGemmPartial: [G * max_seg][BN][128] fp32 slots
   int* meta;                 // kGemmPartial: [tiles][meta_stride] piece count, then slots in CTA order
   int meta_stride;
@@ -108,13 +110,24 @@ DF_DEV bool next_segment(const GemmParams& p, long long& it, long long it1, Segm
 // 32 columns at a time: a transposing butterfly (offsets 16, 8, 4, 2, 1) halves the
 // columns each lane holds while taking maxima, so lane L ends with column L after 31
 // exchanges instead of 5 per column.
-DF_DEV void argmax_tile(uint32_t taddr, int BN, int n, bool n_ok, unsigned long long* run, int lane) {
+// DRAW: the keys are of value * inv_temp + draw_noise(key of the column's token, row), the
+// product and the sum rounded separately (no fused multiply-add), so that a temperature
+// draw is the argmax the same way; dk = the tile's per-column draw keys, nk columns valid.
+template <bool DRAW>
+DF_DEV void argmax_tile(uint32_t taddr, int BN, int n, bool n_ok, unsigned long long* run, int lane,
+                        const uint32_t* dk = nullptr, int nk = 0, float inv_temp = 1.f) {
   for (int c0 = 0; c0 < BN; c0 += 32) {
     float v[32];
     tmem_ld16(taddr + c0, v);
     const bool two = c0 + 16 < BN;  // BN is a multiple of 16; never read past the tile
     if (two) tmem_ld16(taddr + c0 + 16, v + 16);
     tmem_ld_wait();
+    if constexpr (DRAW) {
+      const uint32_t mine = c0 + lane < nk ? dk[c0 + lane] : 0u;  // lane j: column c0 + j's key
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        v[j] = __fadd_rn(__fmul_rn(v[j], inv_temp), draw_noise(__shfl_sync(0xffffffffu, mine, j), n));
+    }
     unsigned long long k[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
@@ -350,7 +363,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           argmax_flush(p, run, run_tt, lane);
           run_tt = tt;
         }
-        argmax_tile(taddr, BN, n, n_ok, run, lane);
+        if (p.draw_key)
+          argmax_tile<true>(taddr, BN, n, n_ok, run, lane, p.draw_key + (size_t)tt * BN, p.M - tt * BN, p.inv_temp);
+        else
+          argmax_tile<false>(taddr, BN, n, n_ok, run, lane);
       } else if constexpr (MODE == kGemmPartial) {
         // this segment's accumulator -> its slot, [token][feature row], plain stores; 64
         // columns per TMEM round trip, then 16 at a time for the rest
@@ -629,6 +645,8 @@ int launch_gemm(const GemmDesc& g, cudaStream_t st) {
   p.out = g.out;
   p.ldo = g.ldo;
   p.amax = g.amax;
+  p.draw_key = g.draw_key;
+  p.inv_temp = g.inv_temp;
   p.stats = reinterpret_cast<float2*>(g.stats);
   p.n_stats = 4 * ((g.N + kBM - 1) / kBM);
   p.status = g.status;

@@ -18,6 +18,9 @@ struct GemmDesc {
   float* out;      // kGemmAtomicAdd: out[t*ldo + n] += ...;  kGemmStore: out[t*ldo + n] = ...
   int ldo;
   unsigned long long* amax;  // kGemmArgmax: per-token packed (value key << 32 | ~index), max-reduced
+  const uint32_t* draw_key;  // kGemmArgmax, optional: per-token draw keys (draw_key()); the argmax is
+                             // then taken over value * inv_temp + Gumbel noise (a temperature draw)
+  float inv_temp;
   float* stats;    // kGemmStore, optional: [M][4 * ceil(N/128)] float2 (max, sum exp(x - max)) partials
   int* status;
   float* part;     // kGemmPartial: slot buffer (size from gemm_partial_bytes)

@@ -11,6 +11,7 @@
 //   lse_from_stats_kernel  log-sum-exp of each LM-head row from the GEMM's softmax partials
 //   sub_lse_kernel         x - lse, in place (the drafter's log-probs)
 //   argmax_finalize_kernel token id from the packed argmax keys
+//   draw_keys_kernel       per-row keys of the LM head's temperature draw
 // Readings: Qwen3-style pre-norm layer (see the oracle); RMSNorm eps and rotary base
 // come from the model config.
 #include "common.cuh"
@@ -366,6 +367,24 @@ __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ am
   if (r < rows) out[r] = (int32_t)(~(uint32_t)(amax[r] & 0xFFFFFFFFull));
 }
 
+__global__ void draw_keys_kernel(int rows, uint64_t seed, const int32_t* __restrict__ row_seq,
+                                 const int32_t* __restrict__ row_pos, int T, const int32_t* __restrict__ cache_len,
+                                 const int32_t* __restrict__ depth, uint32_t* __restrict__ keys) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= rows) return;
+  int s, n;
+  if (row_seq) {
+    s = row_seq[t];
+    n = row_pos[t];
+  } else {
+    s = t / T;
+    n = cache_len[s] + (depth ? depth[t] : t - s * T) + 1;
+  }
+  keys[t] = draw_key(seed, s, n);
+}
+
 // ----------------------------------------------------------------------------- launchers
 int launch_embed(const df_bf16* E, int d, int V, const int32_t* tok, const int32_t* bonus, int L, int mask_id,
                  float* h, int rows, int* status, cudaStream_t st) {
@@ -423,6 +442,13 @@ int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, 
   DF_TRACE("logsoftmax", st);
   launch_k(lse_from_stats_kernel, dim3(rows), dim3(1024), 0, st, reinterpret_cast<const float2*>(stats), n_stats, lse);
   launch_k(sub_lse_kernel, dim3(dim3(rows, 32)), dim3(256), 0, st, x, V, lse);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+int launch_draw_keys(int rows, uint64_t seed, const int32_t* row_seq, const int32_t* row_pos, int T,
+                     const int32_t* cache_len, const int32_t* depth, uint32_t* keys, cudaStream_t st) {
+  DF_TRACE("draw_keys", st);
+  launch_k(draw_keys_kernel, dim3((rows + 255) / 256), dim3(256), 0, st, rows, seed, row_seq, row_pos, T, cache_len,
+           depth, keys);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st) {

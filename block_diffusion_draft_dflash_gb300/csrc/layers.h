@@ -79,5 +79,11 @@ int launch_swiglu_partial(const SwigluArgs& a, cudaStream_t st);
 int launch_logsoftmax_from_stats(float* x, int rows, int V, const float* stats, int n_stats, float* lse,
                                  cudaStream_t st);
 int launch_argmax_finalize(const unsigned long long* amax, int rows, int32_t* out, cudaStream_t st);
+// Draw keys (draw_key() in common.cuh) of `rows` token rows, for the LM head's temperature
+// draw.  Row t draws the token at absolute position pos_t of sequence s_t: given per row
+// (row_seq, row_pos) when row_seq is non-NULL; otherwise the rows are b sequences of T tree
+// (or chain) nodes, s_t = t / T, pos_t = cache_len[s_t] + (depth ? depth[t] : t % T) + 1.
+int launch_draw_keys(int rows, uint64_t seed, const int32_t* row_seq, const int32_t* row_pos, int T,
+                     const int32_t* cache_len, const int32_t* depth, uint32_t* keys, cudaStream_t st);
 
 }  // namespace df

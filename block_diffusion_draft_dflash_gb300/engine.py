@@ -124,11 +124,16 @@ class SpecDecoder:
     mode "tree": DDTree, the B most probable prefixes verified as one flattened tree.
     mode "chain": vanilla DFlash, the drafter's most likely token at each of the D
     positions verified as one chain (B is then D).
+    temperature 0: greedy verification; > 0: the target draws its token after every node at
+    that temperature (keyed to seed, sequence and position; see dflash.h), and the walk
+    follows the drawn tokens.
     """
 
     def __init__(self, target: DeviceModel, drafter: DeviceModel, b: int, B: int, cap: int, prompt_len: int = 0,
-                 device="cuda", mode: str = "tree"):
+                 device="cuda", mode: str = "tree", temperature: float = 0.0, seed: int = 0):
         assert mode in ("tree", "chain")
+        assert temperature >= 0.0
+        self.temperature, self.seed = float(temperature), int(seed)
         ts, ds = target.shape, drafter.shape
         self.t, self.d = target, drafter
         self.mode = mode
@@ -186,7 +191,8 @@ class SpecDecoder:
         self.ctx_len.zero_()
         # depth and ancestor rows omitted: the library runs the rows as a causal chain
         _lib.target_tree_forward(self.t.cfg, self.t.weights, prompt.to(torch.int32).contiguous(), None, None,
-                                 self.k_cache, self.v_cache, self.cache_len, choice, self.prompt_feat, self.ws_prefill)
+                                 self.k_cache, self.v_cache, self.cache_len, choice, self.prompt_feat, self.ws_prefill,
+                                 self.temperature, self.seed)
         self.cache_len.fill_(P)
         self.bonus.copy_(choice[:, -1])
         self.n_new.fill_(P)
@@ -211,7 +217,7 @@ class SpecDecoder:
     def verify(self):
         _lib.target_tree_forward(self.t.cfg, self.t.weights, self.tree["tok"], self.tree["depth"], self.tree["anc"],
                                  self.k_cache, self.v_cache, self.cache_len, self.choice, self.tree_feat,
-                                 self.ws_verify)
+                                 self.ws_verify, self.temperature, self.seed)
 
     def accept(self):
         _lib.accept_and_compact(self.choice, self.tree["tok"], self.tree["parent"], self.k_cache, self.v_cache,

@@ -7,6 +7,7 @@
  *   ddtree_build               top-K per position + best-first max-heap tree of B nodes
  *   dflash_target_tree_forward target forward over the flattened tree (its attention
  *                              layers call tree_verify_attention), greedy choice per node
+ *                              (_sampled: the target's temperature draw per node)
  *   tree_verify_attention      ancestor-only attention of tree rows over the KV cache
  *   accept_and_compact         greedy longest-path walk and KV-cache compaction
  *
@@ -275,6 +276,31 @@ int dflash_target_tree_forward(const df_model_cfg* tcfg, const df_model_weights*
                                const int32_t* cache_len, int32_t* choice, df_bf16* tree_feat,
                                void* ws, size_t ws_bytes, df_stream stream);
 
+/* dflash_target_tree_forward_sampled -- as dflash_target_tree_forward, with the choice
+ * after every node drawn from the target's distribution at temperature T instead of its
+ * argmax.
+ *
+ * [DFlash] and [DDTree] "실험 결과" evaluate temperature 1.0 but state no acceptance rule.
+ * Reading: the verifier follows the target's own outputs ([DDTree] "방법론 자세히 보기"),
+ * so at temperature T the output after node i is a token the target draws, and
+ * accept_and_compact walks the tree along the drawn tokens unchanged; every emitted token
+ * is then the target's own draw (lossless).  The draw is Gumbel-max, argmax over v of
+ * fp32(logit_v * (1/T)) + g_v, g_v = -log(-log u_v), u_v = (23 bits of a counter-based hash +
+ * 1/2) / 2^23 keyed to (seed, sequence s, position N_s + depth_i + 1 of the drawn token, v)
+ * (MurmurHash3's 32-bit finalizer in a fixed chain, also exposed through
+ * dflash_linear_sample).  Keyed to the absolute position, speculative decoding emits the
+ * tokens plain sampling emits under the same seed.
+ *   temperature > 0 and finite (DF_ERR_ARG otherwise); seed: any 64-bit value.  Every other
+ *   argument and the workspace are those of dflash_target_tree_forward.
+ * ------------------------------------------------------------------------------------ */
+int dflash_target_tree_forward_sampled(const df_model_cfg* tcfg, const df_model_weights* tw,
+                                       int b, int n_tree, const int32_t* tok,
+                                       const int32_t* depth, const uint32_t* anc,
+                                       df_bf16* k_cache, df_bf16* v_cache, int cap,
+                                       const int32_t* cache_len, float temperature, uint64_t seed,
+                                       int32_t* choice, df_bf16* tree_feat, void* ws,
+                                       size_t ws_bytes, df_stream stream);
+
 /* dflash_target_expert_counts -- routing statistics of the last mixture-of-experts
  * dflash_target_tree_forward run on this workspace (same tcfg, b, n_tree): per layer, the
  * rows routed to each expert (each row goes to top_k distinct experts, so a layer's counts
@@ -334,6 +360,17 @@ int dflash_linear(const df_bf16* X, const df_bf16* W, int M, int N, int K, float
  *   Workspace: dflash_linear_argmax_workspace_size(M) bytes (per-row keys + status). */
 size_t dflash_linear_argmax_workspace_size(int M);
 int dflash_linear_argmax(const df_bf16* X, const df_bf16* W, int M, int N, int K, int32_t* out,
+                         void* ws, size_t ws_bytes, df_stream stream);
+
+/* dflash_linear_sample -- out[t] = the token row t draws at temperature T from
+ * softmax((X W^T)[t] / T): the LM head of dflash_target_tree_forward_sampled, with each row's
+ * draw keyed to (seed, row_seq[t], row_pos[t]) instead of to the tree (see that call).
+ *   X [M][K] bf16, W [N][K] bf16, K a multiple of 64; row_seq, row_pos [M] int32 (device);
+ *   temperature > 0 and finite (DF_ERR_ARG otherwise); out [M] int32.
+ *   Workspace: dflash_linear_sample_workspace_size(M) bytes. */
+size_t dflash_linear_sample_workspace_size(int M);
+int dflash_linear_sample(const df_bf16* X, const df_bf16* W, int M, int N, int K, float temperature,
+                         uint64_t seed, const int32_t* row_seq, const int32_t* row_pos, int32_t* out,
                          void* ws, size_t ws_bytes, df_stream stream);
 
 /* dflash_linear_logsoftmax -- out[t][n] = log-softmax over n of (X W^T)[t]: the drafter's LM
