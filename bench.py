@@ -211,7 +211,11 @@ def oracle_sample(a, budget_s=25.0):
     E = synth.normal(1007, "bench.E", (Vs, TS.d_model))
     hl = np.concatenate([h, h[:15]])
     t0 = time.perf_counter()
-    model.linear(hl, E)
+    lg = model.linear(hl, E)
+    if getattr(a, "temperature", 0.0) > 0:  # the target rows' draws (Gumbel noise over the slice)
+        from oracle import sample as osample
+        for i in range(T):
+            osample.draw(lg[i], a.temperature, 1, 0, N + i)
     t_head = (time.perf_counter() - t0) * (TS.vocab / Vs)
     est = t_tree + t_layer * TS.n_layers + t_dlayer * DS.n_layers + t_head
     wall = time.perf_counter() - t_all
