@@ -140,15 +140,16 @@ def test_target_tree_forward_sampled_matches_oracle(models, b, B, Ns):
     assert n_clear > 0.5 * b * T
 
 
-def test_speculative_sampling_loop_matches_plain_sampling(models):
+@pytest.mark.parametrize("mode,B", [("tree", 16), ("chain", 0)])  # DDTree, and vanilla DFlash
+def test_speculative_sampling_loop_matches_plain_sampling(models, mode, B):
     """At temperature 1 the emitted tokens are the target's own draws: teacher-forced, the
     oracle draws each generated token from the GPU's prefix, wherever the draw is clear."""
     tw, dw, tm, dm = models
-    b, P, n_gen, cap, B, temperature, seed = 2, 40, 48, 512, 16, 1.0, 4242
+    b, P, n_gen, cap, temperature, seed = 2, 40, 48, 512, 1.0, 4242
     prompt = synth.uniform_ints(2102, "prompt", (b, P), 0, TS.vocab)
     ref = [step.greedy_generate(tw, prompt[s], n_gen + 16, cap, sample.sampler(temperature, seed, s))
            for s in range(b)]
-    dec = engine.SpecDecoder(tm, dm, b, B, cap, prompt_len=P, temperature=temperature, seed=seed)
+    dec = engine.SpecDecoder(tm, dm, b, B, cap, prompt_len=P, mode=mode, temperature=temperature, seed=seed)
     dec.prefill(torch.from_numpy(prompt).cuda())
     outs = [[int(x)] for x in dec.bonus.cpu().tolist()]
     rng = np.random.default_rng(6)
@@ -188,3 +189,40 @@ def test_speculative_sampling_loop_matches_plain_sampling(models):
         assert len(bad) == 0, (s, bad, pred[bad], got[bad])
         # and the run is not the greedy one
         assert np.mean(got != model.argmax_lowest(ologits[P - 1:Tn - 1])) > 0.1
+
+
+def test_moe_target_tree_forward_sampled_matches_oracle():
+    """The sampled head after a mixture-of-experts target (an all-zero router: every row to
+    experts 0 .. k-1 on both sides, so the routing is exact): draws against the oracle's."""
+    shape = synth.ModelShape(1, 512, 8, 2, 128, 0, 4000, feat_layers=(1,), block_size=8, n_experts=32, top_k=4,
+                             d_expert=128)
+    tw = synth.target_weights(shape, 2103)
+    tw.layers[0].w_router[:] = 0
+    tm = engine.DeviceModel.from_host(tw)
+    B, N, cap, temperature, seed = 60, 37, 256, 1.0, 31337
+    T = B + 1
+    rng = np.random.default_rng(2103)
+    t = ddtree.build_tree(ddtree.log_softmax(rng.normal(0, 2, size=(5, shape.vocab))), B)
+    t["tok"][0] = 9
+    kc = synth.normal(2103, "smk", (1, 1, shape.n_kv_heads, cap, 128))
+    vc = synth.normal(2103, "smv", (1, 1, shape.n_kv_heads, cap, 128))
+    kc[..., N:, :] = 0
+    vc[..., N:, :] = 0
+    k = bf16_dev(kc)
+    v = bf16_dev(vc).transpose(-1, -2).contiguous()
+    st = lambda key: torch.from_numpy(t[key][None].astype(np.int32)).cuda()
+    anc = torch.from_numpy(ddtree.ancestor_mask(t["parent"])[None].view(np.int32)).cuda()
+    clen = torch.tensor([N], dtype=torch.int32, device="cuda")
+    choice = torch.zeros(1, T, dtype=torch.int32, device="cuda")
+    ws = _lib.Workspace(_lib.target_tree_forward_workspace_size(tm.cfg, 1, T))
+    _lib.target_tree_forward(tm.cfg, tm.weights, st("tok"), st("depth"), anc, k, v, clen, choice, None, ws,
+                             temperature, seed)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    cache = cache_to_oracle(torch.from_numpy(kc).to(torch.bfloat16), torch.from_numpy(vc).transpose(-1, -2), 0)
+    och, _, ologits = step.target_tree_forward(tw, t["tok"], t["parent"], t["depth"], cache, N,
+                                               sample.sampler(temperature, seed, 0))
+    gap = _gaps(ologits, temperature, seed, 0, N + t["depth"] + 1)
+    clear = gap > 0.02 * np.abs(ologits).max()
+    assert clear.mean() > 0.5
+    np.testing.assert_array_equal(choice[0].cpu().numpy()[clear], och[clear])
