@@ -341,10 +341,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float mb = -m_run * scale2;
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < kCols; c += 2) {
+        for (int c = 0; c < kCols; c += 4) {  // three additions per four probabilities
           const float p0 = ex2_approx(fmaf(sv[c], scale2, mb)), p1 = ex2_approx(fmaf(sv[c + 1], scale2, mb));
-          s4[(c >> 1) & 3] += p0 + p1;
+          const float p2 = ex2_approx(fmaf(sv[c + 2], scale2, mb)), p3 = ex2_approx(fmaf(sv[c + 3], scale2, mb));
+          s4[(c >> 2) & 3] += (p0 + p1) + (p2 + p3);
           packed[c >> 1] = pack_bf16x2(p0, p1);
+          packed[(c >> 1) + 1] = pack_bf16x2(p2, p3);
         }
         l_part = l_part * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       } else {
