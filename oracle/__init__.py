@@ -34,6 +34,11 @@ Parity pins (see tests/test_oracle_*.py):
                           with one expert, brute force over expert subsets, relabelling
                           invariance, a torch-library formulation, tree rows = sequential
                           decode.                                      PINNED
+  sample.draw / sampler   (temperature verification, a reading: the pages state no rule)
+                          fmix32 bijection, uniform and Gumbel laws of the noise, draw
+                          frequencies = softmax(logits / T), small-T limit = argmax;
+                          step.spec_generate with drawn choices token-identical to plain
+                          sampling (losslessness at temperature 1).    PINNED
   model.layer_forward     pinned only through the invariants above: the pages
                           print no layer equations or values (a Qwen3-style
                           pre-norm layer is the stated reading).
